@@ -1,0 +1,439 @@
+/*
+ * mla_oracle.c -- plain, slow, fp64 CPU oracle for MLA over the 576-wide latent cache.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the yardstick the CUDA kernels are checked
+ * against.  Only the test-suite, the smoke check and the benchmark's CPU-baseline leg may
+ * load it; the product path never does.  It shares no code, header, table or constant with
+ * the CUDA library: every codec and formula below is written out again from its definition.
+ *
+ * Sources (pages on vLLM's Kimi-K3 MLA):
+ *  - "vllm.models.kimi_k3.amd.ops.flydsl_sparse_mla", flydsl_sparse_mla_fp8ds_fwd docstring:
+ *    record = 512 e4m3 | 4 fp32 per-128 scales | 64 bf16 rope; CSR rows
+ *    kv_indices[kv_indptr[t]:kv_indptr[t+1]]; entries < 0 masked when has_invalid;
+ *    lse = natural-log log-sum-exp of softmax_scale * q.k over unmasked keys; a row with no
+ *    unmasked key gives out = 0 and lse = -inf.
+ *  - "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.mla.prepared", PreparedMla and
+ *    trtllm_decode: paged decode of q query tokens per request, causal among them;
+ *    bmm1_scale = softmax_scale * q_scale * k_scale and bmm2_scale = k_scale for the plain
+ *    fp8 cache.
+ *  - "vllm.models.kimi_k3.nvidia.ops.fused_mla_key_concat_kv_cache",
+ *    fused_mla_decode_q_concat_kv_cache_insert: mqa_q = [ql_nope | q_pe] and insertion of
+ *    [kv_c_normed | k_pe] at slot_mapping, dispatched by cache format (bf16; plain fp8 with
+ *    q_scale_inv / cache_scale_inv; fp8_ds_mla with per-tile scales), optional GPT-J RoPE
+ *    from an fp32 cos/sin table.
+ *  - "vllm.models.kimi_k3.amd.specialized_decode.mono.attention.mla", fp8_word: the fp8
+ *    write is vLLM's saturating E4M3 quant.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *  - fp8_ds_mla tile scale on insert: s = 2^k with k the smallest integer such that
+ *    amax <= 448 * 2^k (k clamped to >= -126), s = 1 when amax == 0; code = e4m3(x / s).
+ *  - E4M3 saturating quant: clamp |x| to 448, round to nearest even on the E4M3 grid
+ *    (subnormals included), NaN -> 0x7F, sign kept.
+ *  - cos/sin table row p: columns 0..31 cos(p*theta_i), 32..63 sin(p*theta_i); GPT-J pairs
+ *    (2i, 2i+1): y0 = fma(x0, c, -(x1*s)), y1 = fma(x1, c, x0*s), fp32 arithmetic.
+ *  - spec-verify: seq_lens count the q new tokens; query row i of a request of length L
+ *    sees key positions 0 .. L-q+i.
+ *
+ * Build: gcc -O2 -fopenmp -ffp-contract=off -shared -fPIC (no fused multiply-adds except
+ * the explicit fmaf calls of the RoPE contract).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define KV_LORA 512
+#define ROPE 64
+#define ENTRY 576
+
+enum { ORC_BF16 = 0, ORC_FP8 = 1, ORC_DS_MLA = 2 };
+
+/* ------------------------------------------------------------------------------------ */
+/* Codecs, from the number formats' definitions.                                        */
+/* ------------------------------------------------------------------------------------ */
+
+/* OCP FP8 E4M3 ("fn"): 1 sign bit, 4 exponent bits (bias 7), 3 mantissa bits, no
+ * infinities, S.1111.111 is NaN, largest finite magnitude 448. */
+double orc_e4m3_to_double(uint8_t b) {
+  int sign = b >> 7, e = (b >> 3) & 15, m = b & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m, -9);           /* subnormal: m/8 * 2^(1-7) */
+  else
+    v = ldexp(8.0 + (double)m, e - 10); /* (1 + m/8) * 2^(e-7) */
+  return sign ? -v : v;
+}
+
+/* Saturating round-to-nearest-even into E4M3, by brute force over the 127 non-negative
+ * finite codes (they are ordered by value).  Ties go to the even code. */
+uint8_t orc_e4m3_from_float_sat(float xf) {
+  double x = (double)xf, a;
+  int neg, c, best = 0;
+  double bestd = INFINITY;
+  if (isnan(x)) return 0x7F;
+  neg = signbit(x) ? 1 : 0;
+  a = fabs(x);
+  if (a > 448.0) a = 448.0;
+  for (c = 0; c <= 0x7E; ++c) {
+    double d = fabs(orc_e4m3_to_double((uint8_t)c) - a);
+    if (d < bestd || (d == bestd && (c & 1) == 0)) {
+      bestd = d;
+      best = c;
+    }
+  }
+  return (uint8_t)(best | (neg << 7));
+}
+
+/* bfloat16: the top half of an IEEE binary32. */
+double orc_bf16_to_double(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return (double)f;
+}
+
+/* binary32 -> bfloat16, round to nearest even; NaN becomes the quiet NaN 0x7FC0 (sign kept). */
+uint16_t orc_bf16_from_float(float f) {
+  uint32_t u, lsb;
+  memcpy(&u, &f, 4);
+  if (isnan(f)) return (uint16_t)(((u >> 16) & 0x8000u) | 0x7FC0u);
+  lsb = (u >> 16) & 1u;
+  u += 0x7FFFu + lsb;
+  return (uint16_t)(u >> 16);
+}
+
+static float bf16_to_float(uint16_t h) {
+  uint32_t u = (uint32_t)h << 16;
+  float f;
+  memcpy(&f, &u, 4);
+  return f;
+}
+
+static uint16_t rd16(const uint8_t* p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+static void wr16(uint8_t* p, uint16_t v) {
+  p[0] = (uint8_t)(v & 0xFF);
+  p[1] = (uint8_t)(v >> 8);
+}
+static float rdf32(const uint8_t* p) {
+  float f;
+  memcpy(&f, p, 4); /* both hosts are little-endian, as is the device */
+  return f;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Cache entry decode.                                                                   */
+/* ------------------------------------------------------------------------------------ */
+
+/* One cache entry -> 576 exact values.  fp8_ds_mla: NoPE d < 512 is e4m3(b[d]) times the
+ * fp32 scale of its 128-wide tile (bytes 512 + 4*(d/128)); rope is the bf16 at bytes
+ * 528 + 2i.  Plain fp8: all 576 are e4m3 (the per-tensor k_scale is applied by the
+ * caller).  bf16: 576 little-endian bf16 values. */
+void orc_decode_entry(int fmt, const uint8_t* e, double* k) {
+  int d;
+  if (fmt == ORC_BF16) {
+    for (d = 0; d < ENTRY; ++d) k[d] = orc_bf16_to_double(rd16(e + 2 * d));
+  } else if (fmt == ORC_FP8) {
+    for (d = 0; d < ENTRY; ++d) k[d] = orc_e4m3_to_double(e[d]);
+  } else {
+    double s[4];
+    for (d = 0; d < 4; ++d) s[d] = (double)rdf32(e + KV_LORA + 4 * d);
+    for (d = 0; d < KV_LORA; ++d) k[d] = orc_e4m3_to_double(e[d]) * s[d / 128];
+    for (d = 0; d < ROPE; ++d) k[KV_LORA + d] = orc_bf16_to_double(rd16(e + KV_LORA + 16 + 2 * d));
+  }
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Attention of one query vector over a key set (plain two-pass definition).            */
+/* ------------------------------------------------------------------------------------ */
+
+/* x_k = sigma * sum_d q[d] K_k[d];  lse = ln sum_k exp(x_k);
+ * out[d] = out_scale * sum_k exp(x_k - lse) * K_k[d] for d < 512.
+ * n == 0: out = 0, lse = -inf. */
+static void attend_one(const double* qv, const double* K, int64_t n, double sigma,
+                       double out_scale, double* x, double* out, double* lse) {
+  int64_t k;
+  int d;
+  double m = -INFINITY, l = 0.0, ls;
+  for (d = 0; d < KV_LORA; ++d) out[d] = 0.0;
+  if (n == 0) {
+    *lse = -INFINITY;
+    return;
+  }
+  for (k = 0; k < n; ++k) {
+    const double* kv = K + k * ENTRY;
+    double acc = 0.0;
+    for (d = 0; d < ENTRY; ++d) acc += qv[d] * kv[d];
+    x[k] = sigma * acc;
+    if (x[k] > m) m = x[k];
+  }
+  for (k = 0; k < n; ++k) l += exp(x[k] - m);
+  ls = m + log(l);
+  for (k = 0; k < n; ++k) {
+    const double* kv = K + k * ENTRY;
+    double w = exp(x[k] - ls);
+    for (d = 0; d < KV_LORA; ++d) out[d] += w * kv[d];
+  }
+  for (d = 0; d < KV_LORA; ++d) out[d] *= out_scale;
+  *lse = ls;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Sparse forward over fp8_ds_mla records (CSR key lists).                               */
+/* ------------------------------------------------------------------------------------ */
+
+/* q: bf16 [T, H, 576] with element strides q_s0 / q_s1 (unit last stride).
+ * records: num_records entries of 656 bytes at record_stride bytes.
+ * indptr [T+1], indices [indptr[T]] (int64 here; the test harness widens).
+ * rows: optional list of n_rows query rows to compute (NULL = all T, in order).
+ * out: [n_rows, H, 512] fp64; lse: [n_rows, H] fp64.
+ * Returns 0, or -1 when an index is out of range and not a masked negative. */
+int orc_sparse_fwd(const uint16_t* q, int64_t q_s0, int64_t q_s1, const uint8_t* records,
+                   int64_t record_stride, int64_t num_records, const int64_t* indptr,
+                   const int64_t* indices, double softmax_scale, int has_invalid, int T, int H,
+                   const int32_t* rows, int n_rows, double* out, double* lse) {
+  int bad = 0;
+  int ri;
+  if (rows == NULL) n_rows = T;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (ri = 0; ri < n_rows; ++ri) {
+    int t = rows ? rows[ri] : ri;
+    int64_t b = indptr[t], e = indptr[t + 1], j, n = 0;
+    double* K = (double*)malloc(sizeof(double) * ENTRY * (size_t)((e - b) > 0 ? (e - b) : 1));
+    double* x = (double*)malloc(sizeof(double) * (size_t)((e - b) > 0 ? (e - b) : 1));
+    double qv[ENTRY];
+    int h, d;
+    for (j = b; j < e; ++j) {
+      int64_t idx = indices[j];
+      if (idx < 0 && has_invalid) continue;
+      if (idx < 0 || idx >= num_records) {
+        bad = 1;
+        continue;
+      }
+      orc_decode_entry(ORC_DS_MLA, records + idx * record_stride, K + n * ENTRY);
+      ++n;
+    }
+    for (h = 0; h < H; ++h) {
+      const uint16_t* qp = q + (int64_t)t * q_s0 + (int64_t)h * q_s1;
+      for (d = 0; d < ENTRY; ++d) qv[d] = orc_bf16_to_double(qp[d]);
+      attend_one(qv, K, n, softmax_scale, 1.0, x, out + ((int64_t)ri * H + h) * KV_LORA,
+                 lse + (int64_t)ri * H + h);
+    }
+    free(K);
+    free(x);
+  }
+  return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Paged decode / spec-verify.                                                           */
+/* ------------------------------------------------------------------------------------ */
+
+/* q: [B*q_len, H, 576], bf16 (formats bf16, ds_mla) or e4m3 bytes (plain fp8); byte
+ * strides q_s0_bytes / q_s1_bytes.  Request b's key positions are 0 .. L_b-1 with
+ * L_b = seq_lens[b]; query row i (0 <= i < q_len) sees positions 0 .. L_b - q_len + i.
+ * Position p lives at block block_table[b*bt_stride + p/block_size], offset p%block_size:
+ * entry address = cache + block*block_stride + (p%block_size)*entry_stride (bytes).
+ * sigma = softmax_scale (bf16, ds_mla) or softmax_scale*q_scale*k_scale (plain fp8, with
+ * q and K the raw e4m3 values); the fp8 output is multiplied by k_scale.
+ * rows: optional list of query rows (b*q_len + i); NULL = all.
+ * Returns 0, or -1 if a block id is out of [0, num_blocks). */
+int orc_paged_decode(int fmt, const uint8_t* q, int64_t q_s0_bytes, int64_t q_s1_bytes,
+                     const uint8_t* cache, int64_t num_blocks, int64_t block_stride,
+                     int64_t entry_stride, int block_size, const int32_t* block_table,
+                     int64_t bt_stride, const int32_t* seq_lens, int B, int q_len, int H,
+                     double softmax_scale, double q_scale, double k_scale, const int32_t* rows,
+                     int n_rows, double* out, double* lse) {
+  int bad = 0;
+  int ri;
+  double sigma = softmax_scale, oscale = 1.0;
+  if (fmt == ORC_FP8) {
+    sigma = softmax_scale * q_scale * k_scale;
+    oscale = k_scale;
+  }
+  if (rows == NULL) n_rows = B * q_len;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (ri = 0; ri < n_rows; ++ri) {
+    int row = rows ? rows[ri] : ri;
+    int b = row / q_len, i = row % q_len;
+    int64_t L = seq_lens[b];
+    int64_t n = L - q_len + i + 1, p, nn = 0;
+    double *K, *x, qv[ENTRY];
+    int h, d;
+    if (n < 0) n = 0;
+    K = (double*)malloc(sizeof(double) * ENTRY * (size_t)(n > 0 ? n : 1));
+    x = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+    for (p = 0; p < n; ++p) {
+      int64_t blk = block_table[(int64_t)b * bt_stride + p / block_size];
+      if (blk < 0 || blk >= num_blocks) {
+        bad = 1;
+        continue;
+      }
+      orc_decode_entry(fmt, cache + blk * block_stride + (p % block_size) * entry_stride,
+                       K + nn * ENTRY);
+      ++nn;
+    }
+    for (h = 0; h < H; ++h) {
+      const uint8_t* qp = q + (int64_t)row * q_s0_bytes + (int64_t)h * q_s1_bytes;
+      for (d = 0; d < ENTRY; ++d)
+        qv[d] = (fmt == ORC_FP8) ? orc_e4m3_to_double(qp[d]) : orc_bf16_to_double(rd16(qp + 2 * d));
+      attend_one(qv, K, nn, sigma, oscale, x, out + ((int64_t)ri * H + h) * KV_LORA,
+                 lse + (int64_t)ri * H + h);
+    }
+    free(K);
+    free(x);
+  }
+  return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Merge of partial attentions by their log-sum-exp (the chunk / split combine).         */
+/* ------------------------------------------------------------------------------------ */
+
+/* parts: S partial outputs of width 512 (each normalised by its own sum), lse_parts: S.
+ * lse = ln sum_s exp(lse_s); out = sum_s exp(lse_s - lse) * parts_s.  All -inf -> 0, -inf. */
+void orc_merge(int S, const double* parts, const double* lse_parts, double* out, double* lse) {
+  double m = -INFINITY, l = 0.0;
+  int s, d;
+  for (d = 0; d < KV_LORA; ++d) out[d] = 0.0;
+  for (s = 0; s < S; ++s)
+    if (lse_parts[s] > m) m = lse_parts[s];
+  if (m == -INFINITY) {
+    *lse = -INFINITY;
+    return;
+  }
+  for (s = 0; s < S; ++s) l += exp(lse_parts[s] - m);
+  *lse = m + log(l);
+  for (s = 0; s < S; ++s) {
+    double w = exp(lse_parts[s] - *lse);
+    for (d = 0; d < KV_LORA; ++d) out[d] += w * parts[(int64_t)s * KV_LORA + d];
+  }
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Decode epilogue: q concat + latent insert.                                            */
+/* ------------------------------------------------------------------------------------ */
+
+/* GPT-J rotation of one 64-wide vector in fp32 (the epilogue's RoPE contract). */
+static void rope_fp32(const float* x, const float* cs_row, float* y) {
+  int i;
+  for (i = 0; i < ROPE / 2; ++i) {
+    float c = cs_row[i], s = cs_row[ROPE / 2 + i];
+    float x0 = x[2 * i], x1 = x[2 * i + 1];
+    float t0 = x1 * s; /* rounded fp32 product (no contraction in this file) */
+    float t1 = x0 * s;
+    y[2 * i] = fmaf(x0, c, -t0);
+    y[2 * i + 1] = fmaf(x1, c, t1);
+  }
+}
+
+/* Smallest integer k with amax <= 448 * 2^k, clamped to k >= -126; amax == 0 -> k = 0. */
+static int ds_tile_exponent(double amax) {
+  int e, k;
+  double f;
+  if (amax == 0.0) return 0;
+  f = frexp(amax, &e); /* amax = f * 2^e, 0.5 <= f < 1; 448 = 0.875 * 2^9 */
+  k = e - 9 + (f > 0.875 ? 1 : 0);
+  if (k < -126) k = -126;
+  return k;
+}
+
+/* Inputs are bf16 tensors given by element strides (unit last stride):
+ *   ql_nope [B, H, 512], q_pe [B, H, 64], kv_c [B, 512], k_pe [B, 64].
+ * mqa_q out: [B, H, 576] contiguous, bf16 (bf16 / ds_mla formats) or e4m3 bytes (plain fp8).
+ * cache: num_blocks blocks at block_stride bytes, entries at entry_stride bytes.
+ * slot_mapping [B] int64, < 0 skips the insert (mqa_q is still written); a slot whose
+ * block is out of range is skipped too and reported by the return value -1.
+ * positions [B] int64 and cos_sin [max_position, 64] fp32: both NULL (no RoPE) or both set.
+ * q_scale_inv / cache_scale_inv: used by the plain fp8 format only. */
+int orc_q_concat_cache_insert(int fmt, const uint16_t* ql_nope, int64_t ql_s0, int64_t ql_s1,
+                              const uint16_t* q_pe, int64_t qp_s0, int64_t qp_s1,
+                              const uint16_t* kv_c, int64_t kv_s0, const uint16_t* k_pe,
+                              int64_t kp_s0, uint8_t* mqa_q, uint8_t* cache, int64_t num_blocks,
+                              int64_t block_stride, int64_t entry_stride, int block_size,
+                              const int64_t* slot_mapping, float q_scale_inv,
+                              float cache_scale_inv, const int64_t* positions,
+                              const float* cos_sin, int64_t max_position, int B, int H) {
+  int bad = 0, b;
+  for (b = 0; b < B; ++b) {
+    const float* cs = NULL;
+    float kp[ROPE], kpr[ROPE], x[KV_LORA];
+    int h, d;
+    int64_t slot;
+    if (positions) {
+      int64_t pos = positions[b];
+      if (pos < 0 || pos >= max_position) {
+        bad = 1;
+        pos = pos < 0 ? 0 : max_position - 1;
+      }
+      cs = cos_sin + pos * ROPE;
+    }
+    /* query concat */
+    for (h = 0; h < H; ++h) {
+      const uint16_t* qn = ql_nope + (int64_t)b * ql_s0 + (int64_t)h * ql_s1;
+      const uint16_t* qp = q_pe + (int64_t)b * qp_s0 + (int64_t)h * qp_s1;
+      float qpf[ROPE], qpr[ROPE];
+      uint8_t* dst = mqa_q + ((int64_t)b * H + h) * ENTRY * (fmt == ORC_FP8 ? 1 : 2);
+      for (d = 0; d < ROPE; ++d) qpf[d] = bf16_to_float(qp[d]);
+      if (cs)
+        rope_fp32(qpf, cs, qpr);
+      else
+        memcpy(qpr, qpf, sizeof qpr);
+      if (fmt == ORC_FP8) {
+        for (d = 0; d < KV_LORA; ++d) dst[d] = orc_e4m3_from_float_sat(bf16_to_float(qn[d]) * q_scale_inv);
+        for (d = 0; d < ROPE; ++d) dst[KV_LORA + d] = orc_e4m3_from_float_sat(qpr[d] * q_scale_inv);
+      } else {
+        for (d = 0; d < KV_LORA; ++d) wr16(dst + 2 * d, qn[d]);
+        for (d = 0; d < ROPE; ++d) wr16(dst + 2 * (KV_LORA + d), orc_bf16_from_float(qpr[d]));
+      }
+    }
+    /* latent insert */
+    slot = slot_mapping[b];
+    if (slot < 0) continue;
+    if (slot / block_size >= num_blocks) {
+      bad = 1;
+      continue;
+    }
+    {
+      uint8_t* ent = cache + (slot / block_size) * block_stride + (slot % block_size) * entry_stride;
+      const uint16_t* kc = kv_c + (int64_t)b * kv_s0;
+      const uint16_t* kr = k_pe + (int64_t)b * kp_s0;
+      for (d = 0; d < ROPE; ++d) kp[d] = bf16_to_float(kr[d]);
+      if (cs)
+        rope_fp32(kp, cs, kpr);
+      else
+        memcpy(kpr, kp, sizeof kpr);
+      for (d = 0; d < KV_LORA; ++d) x[d] = bf16_to_float(kc[d]);
+      if (fmt == ORC_BF16) {
+        for (d = 0; d < KV_LORA; ++d) wr16(ent + 2 * d, kc[d]);
+        for (d = 0; d < ROPE; ++d) wr16(ent + 2 * (KV_LORA + d), orc_bf16_from_float(kpr[d]));
+      } else if (fmt == ORC_FP8) {
+        for (d = 0; d < KV_LORA; ++d) ent[d] = orc_e4m3_from_float_sat(x[d] * cache_scale_inv);
+        for (d = 0; d < ROPE; ++d) ent[KV_LORA + d] = orc_e4m3_from_float_sat(kpr[d] * cache_scale_inv);
+      } else {
+        int j;
+        for (j = 0; j < 4; ++j) {
+          double amax = 0.0, s;
+          float sf;
+          int k;
+          for (d = 0; d < 128; ++d) {
+            double a = fabs((double)x[128 * j + d]);
+            if (a > amax) amax = a;
+          }
+          k = ds_tile_exponent(amax);
+          s = ldexp(1.0, k);
+          sf = (float)s;
+          memcpy(ent + KV_LORA + 4 * j, &sf, 4);
+          for (d = 0; d < 128; ++d)
+            ent[128 * j + d] = orc_e4m3_from_float_sat((float)((double)x[128 * j + d] / s));
+        }
+        for (d = 0; d < ROPE; ++d) wr16(ent + KV_LORA + 16 + 2 * d, orc_bf16_from_float(kpr[d]));
+      }
+    }
+  }
+  return bad ? -1 : 0;
+}
+
+/* Exposed for the self-tests: the tile exponent rule and the fp32 rotation. */
+int orc_ds_tile_exponent(double amax) { return ds_tile_exponent(amax); }
+void orc_rope_fp32(const float* x, const float* cs_row, float* y) { rope_fp32(x, cs_row, y); }
