@@ -1,0 +1,436 @@
+#!/usr/bin/env python
+"""Benchmark of the MLA latent-cache hot path on GB300.
+
+Default workload: paged bf16 decode with the fused epilogue in front (B=32, q=1, H=16,
+seq_lens ~ U[1024, 8192], block_size 64).  One step = mla_q_concat_cache_insert followed by
+mla_paged_decode (attention + split-K merge) over the whole batch.  Other workloads
+(--workload): sparse_prefill (T=4096, H=16, top-2048 over 65536 fp8_ds_mla records),
+fp8_spec_verify (B=64, q=4, H=16, plain fp8, L ~ U[16k, 128k]) and ds_mla_h96_decode
+(B=128, H=96, fp8_ds_mla, L ~ U[8k, 32k]).
+
+Metric: achieved GB/s of algorithmic bytes (entries gathered + query read + output written
+(+ lse)), with query-rows/s beside it.  Timing: CUDA events per step after warm-up, L2
+flushed (256 MiB write) between steps outside the timed events; max over ranks.
+`--impl reference` times the fp64 CPU oracle on a bounded sample of the same workload.
+Multi-GPU (torchrun): every rank runs an independent replica ("replicas only").
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MLA attention achieved HBM GB/s (% of GB300 peak); query-rows/s at 1 GPU"
+WORKLOADS = ("decode_bf16_epilogue", "sparse_prefill", "fp8_spec_verify", "ds_mla_h96_decode")
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------------------------------ workloads
+
+class Work:
+    """Host inputs of one workload plus its byte / row accounting."""
+
+    def __init__(self, name: str):
+        from mla_latent_cache_attention_gb300 import synth
+        self.name = name
+        self.synth = synth
+        if name == "decode_bf16_epilogue":
+            self.case, self.epi = synth.config1()
+            self.kind = "paged"
+        elif name == "sparse_prefill":
+            self.case = synth.config2()
+            self.kind = "sparse"
+        elif name == "fp8_spec_verify":
+            self.case = synth.config3()
+            self.kind = "paged"
+        elif name == "ds_mla_h96_decode":
+            self.case = synth.config4()
+            self.kind = "paged"
+        else:
+            raise SystemExit(f"unknown workload {name}")
+        c = self.case
+        if self.kind == "sparse":
+            self.attn_bytes = synth.algorithmic_bytes_sparse(c)
+            self.rows = c.q.shape[0]
+            self.heads = c.q.shape[1]
+            self.cfg = dict(workload=name, T=int(c.q.shape[0]), H=int(c.q.shape[1]), records=int(c.records.shape[0]),
+                            indices_per_row=2048, masked_frac=0.05, cache="fp8_ds_mla", return_lse=True)
+            self.dtype = "bf16"
+        else:
+            self.attn_bytes = synth.algorithmic_bytes_paged(c)
+            self.rows = c.seq_lens.size * c.q_len
+            self.heads = c.H
+            fmtname = {0: "bf16", 1: "fp8", 2: "fp8_ds_mla"}[c.fmt]
+            self.cfg = dict(workload=name, B=int(c.seq_lens.size), q_len=c.q_len, H=c.H, cache=fmtname,
+                            block_size=int(c.cache.shape[1]), seq_len_lo=int(c.meta["L_lo"]),
+                            seq_len_hi=int(c.meta["L_hi"]), max_context=c.max_context, return_lse=c.return_lse)
+            self.dtype = {0: "bf16", 1: "fp8 e4m3 operands (f16 MMA)", 2: "bf16/f16 (fp8_ds_mla)"}[c.fmt]
+        self.epi_bytes = 0
+        if name == "decode_bf16_epilogue":
+            B, H = self.epi.ql_nope.shape[:2]
+            # epilogue: ql_nope + q_pe + kv_c + k_pe read, cos/sin rows, mqa_q and the entries written
+            self.epi_bytes = 2 * (B * H * 576 + B * 576) + B * 64 * 4 + 2 * B * H * 576 + B * 1152
+        self.step_bytes = self.attn_bytes + self.epi_bytes
+
+
+# ------------------------------------------------------------------------------------ GPU arm
+
+def to_dev(a, torch, dev, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.to(dev)
+
+
+class GpuRunner:
+    def __init__(self, w: Work, dev):
+        import torch
+        import mla_latent_cache_attention_gb300 as m
+        self.torch, self.m, self.w, self.dev = torch, m, w, dev
+        c = w.case
+        if w.kind == "sparse":
+            self.q = to_dev(c.q.view(np.int16), torch, dev).view(torch.bfloat16)
+            self.rec = to_dev(c.records, torch, dev)
+            self.indptr = to_dev(c.indptr, torch, dev)
+            self.indices = to_dev(c.indices, torch, dev)
+            self.out = torch.empty((self.q.shape[0], self.q.shape[1], 512), dtype=torch.bfloat16, device=dev)
+            self.launches_per_step = 1
+        else:
+            self.cache = to_dev(c.cache, torch, dev)
+            self.bt = to_dev(c.block_table, torch, dev)
+            self.sl = to_dev(c.seq_lens, torch, dev)
+            if c.fmt == 1:
+                self.q = to_dev(c.q, torch, dev)
+            else:
+                self.q = to_dev(c.q.view(np.int16), torch, dev).view(torch.bfloat16).reshape(c.q.shape[0], c.H, 576)
+            self.out = torch.empty((self.q.shape[0], c.H, 512), dtype=torch.bfloat16, device=dev)
+            need = m.paged_decode_workspace_size(c.seq_lens.size, c.q_len, c.H, c.max_context)
+            self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
+            self.launches_per_step = 1 + (1 if need > 0 else 0)
+            if w.name == "decode_bf16_epilogue":
+                e = w.epi
+                b16 = lambda a: to_dev(a.view(np.int16), torch, dev).view(torch.bfloat16)
+                self.ql, self.qp, self.kvc, self.kpe = b16(e.ql_nope), b16(e.q_pe), b16(e.kv_c), b16(e.k_pe)
+                self.slots = to_dev(e.slot_mapping, torch, dev)
+                self.pos = to_dev(e.positions, torch, dev)
+                self.cs = to_dev(e.cos_sin, torch, dev)
+                self.launches_per_step += 1
+        self.lse = torch.empty((self.q.shape[0], self.q.shape[1]), dtype=torch.float32, device=dev)
+
+    def step(self):
+        m, w, c = self.m, self.w, self.w.case
+        if w.kind == "sparse":
+            m.sparse_fwd(self.q, self.rec, self.indptr, self.indices, c.softmax_scale, has_invalid=True,
+                         out=self.out, return_lse=True)
+            return
+        q = self.q
+        if w.name == "decode_bf16_epilogue":
+            q = m.q_concat_cache_insert(self.ql, self.qp, self.kvc, self.kpe, self.cache, self.slots,
+                                        fmt=c.fmt, positions=self.pos, cos_sin_cache=self.cs, mqa_q=self.q)
+        m.paged_decode(q, self.cache, self.bt, self.sl, fmt=c.fmt, q_len=c.q_len, max_context=c.max_context,
+                       softmax_scale=c.softmax_scale, q_scale=c.q_scale, k_scale=c.k_scale, out=self.out,
+                       return_lse=c.return_lse, workspace=self.ws)
+
+    # ---- end-to-end: the per-step inputs come from pinned host memory, the result goes back
+    def e2e_setup(self):
+        torch, w, c = self.torch, self.w, self.w.case
+        pin = lambda a, dt=None: (torch.from_numpy(np.ascontiguousarray(a)).view(dt) if dt is not None else
+                                  torch.from_numpy(np.ascontiguousarray(a))).pin_memory()
+        self.h_in = []
+        if w.kind == "sparse":
+            self.h_in = [(pin(c.q.view(np.int16), torch.bfloat16), self.q), (pin(c.indptr), self.indptr),
+                         (pin(c.indices), self.indices)]
+        elif w.name == "decode_bf16_epilogue":
+            e = w.epi
+            b = lambda a: pin(a.view(np.int16), torch.bfloat16)
+            self.h_in = [(b(e.ql_nope), self.ql), (b(e.q_pe), self.qp), (b(e.kv_c), self.kvc), (b(e.k_pe), self.kpe),
+                         (pin(e.slot_mapping), self.slots), (pin(e.positions), self.pos), (pin(c.block_table), self.bt),
+                         (pin(c.seq_lens), self.sl)]
+        else:
+            qh = pin(c.q) if c.fmt == 1 else pin(c.q.view(np.int16), torch.bfloat16).reshape(self.q.shape)
+            self.h_in = [(qh, self.q), (pin(c.block_table), self.bt), (pin(c.seq_lens), self.sl)]
+        self.h_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.h_lse = torch.empty(self.lse.shape, dtype=self.lse.dtype).pin_memory()
+        self.h2d = sum(h.numel() * h.element_size() for h, _ in self.h_in)
+        self.d2h = self.h_out.numel() * self.h_out.element_size()
+        ret_lse = (w.kind == "sparse") or c.return_lse
+        if ret_lse:
+            self.d2h += self.h_lse.numel() * 4
+        self.ret_lse = ret_lse
+
+    def e2e_step(self):
+        for h, d in self.h_in:
+            d.copy_(h, non_blocking=True)
+        self.step()
+        self.h_out.copy_(self.out, non_blocking=True)
+        if self.ret_lse:
+            self.h_lse.copy_(self.lse, non_blocking=True)
+
+
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index = index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.proc = None
+
+    def start(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                smax.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def run_native(args, rank, world, dist):
+    import torch
+    import mla_latent_cache_attention_gb300 as m
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    m.lib()
+    w = Work(args.workload)
+    r = GpuRunner(w, dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        r.step()
+    torch.cuda.synchronize()
+    assert m.read_device_errors() == 0, "device error word set during warm-up"
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    ea = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    for a, b in ea:      # materialise the handles
+        a.record()
+        b.record()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = ClockSampler(local)
+    clk.start()
+    time.sleep(0.3)
+    torch.cuda.synchronize()
+    for i in range(K):
+        flush.fill_(i & 255)
+        m.profile_attention_events(*ea[i])
+        ev[i][0].record()
+        r.step()
+        ev[i][1].record()
+    m.profile_attention_events(None, None)
+    torch.cuda.synchronize()
+    clocks = clk.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    attn_ms = [a.elapsed_time(b) for a, b in ea]
+    total_ms = float(sum(step_ms))
+    # e2e through the public API with host buffers
+    r.e2e_setup()
+    for _ in range(2):
+        r.e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_ms = 0.0
+    for i in range(K):
+        flush.fill_(i & 255)
+        e0.record()
+        r.e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        e2e_ms += e0.elapsed_time(e1)
+    assert m.read_device_errors() == 0, "device error word set during the timed steps"
+    if dist is not None:
+        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, e2e_ms = float(t[0]), float(t[1])
+    peak, peak_kind = peaks()
+    value = world * w.step_bytes * K / (total_ms * 1e-3) / 1e9
+    attn_avg = float(np.mean(attn_ms))
+    achieved = w.attn_bytes / (attn_avg * 1e-3) / 1e9
+    prof = load_traffic(args.workload)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded numpy)",
+        "config": dict(w.cfg, l2="flushed between steps (256 MiB write, outside the timed events)",
+                       parallelism="replicas" if world > 1 else "single GPU"),
+        "query_rows_per_s": round(world * w.rows * K / (total_ms * 1e-3), 1),
+        "row_heads_per_s": round(world * w.rows * w.heads * K / (total_ms * 1e-3), 1),
+        "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": prof, "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel": "mla_attn_kernel (attention only; epilogue and merge outside)",
+                     "kernel_ms": round(attn_avg, 5), "bytes_per_launch": w.attn_bytes},
+        "e2e": {"value": round(world * w.step_bytes * K / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(r.h2d), "d2h_bytes_per_step": int(r.d2h)},
+        "gpu_launches": int(r.launches_per_step * K),
+        "clocks": clocks,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    return line
+
+
+def load_traffic(workload):
+    """dram bytes per launch of the attention kernel from the committed ncu summary, if any."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            return json.load(f).get(workload)
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------------------------------ CPU oracle arm
+
+def cpu_sample(w: Work, budget_s: float):
+    """Time the oracle on a bounded sample of the workload's query rows; returns
+    (bytes-equivalent processed per second, rows sampled, seconds)."""
+    import oracle
+    c = w.case
+    rng = np.random.default_rng(0)
+    nrows = w.rows
+
+    def run(rows):
+        t = time.perf_counter()
+        if w.kind == "sparse":
+            oracle.sparse_fwd(c.q, c.records, c.indptr, c.indices, c.softmax_scale, True, rows=rows)
+        else:
+            oracle.paged_decode(c.fmt, c.q, c.cache, c.block_table, c.seq_lens, c.q_len, c.softmax_scale,
+                                c.q_scale, c.k_scale, rows=rows)
+        return time.perf_counter() - t
+
+    probe = np.sort(rng.choice(nrows, size=min(nrows, 4), replace=False))
+    t0 = max(run(probe), 1e-3)
+    n = int(max(1, min(nrows, len(probe) * budget_s / t0)))
+    rows = np.sort(rng.choice(nrows, size=n, replace=False))
+    secs = run(rows)
+    frac = (secs, n)
+    # the attention bytes of the sampled rows, prorated by rows (q and out) and keys
+    if w.kind == "sparse":
+        valid = np.zeros(nrows)
+        for i, rr in enumerate(rows):
+            seg = c.indices[c.indptr[rr]:c.indptr[rr + 1]]
+            valid[i] = (seg >= 0).sum()
+        b = valid.sum() * 656 + n * w.heads * (576 * 2 + 512 * 2 + 4)
+    else:
+        eb = w.synth.ENTRY_BYTES[c.fmt]
+        qe = 1 if c.fmt == 1 else 2
+        # a request's entries are read once for all its q_len rows: charge them per row
+        L = c.seq_lens[rows // c.q_len].astype(np.float64)
+        b = (L * eb / c.q_len).sum() + n * w.heads * (576 * qe + 512 * 2 + (4 if c.return_lse else 0))
+    return b / secs / 1e9, n, secs, frac
+
+
+def cpu_baseline(w: Work, budget_s: float = 15.0):
+    gbs, n, secs, _ = cpu_sample(w, budget_s)
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": f"{n} of {w.rows} query rows of {w.name} (all heads), {secs:.1f} s, fp64 C oracle, OpenMP",
+            "query_rows_per_s": round(n / secs, 2)}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = Work(args.workload)
+    budget = max(1.0, args.cpu_seconds / max(1, args.steps))
+    vals, rows, secs = [], 0, 0.0
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        cpu_sample(w, min(budget, 2.0))
+    for _ in range(args.steps):
+        gbs, n, s, _ = cpu_sample(w, budget)
+        vals.append(gbs)
+        rows += n
+        secs += s
+    value = float(np.mean(vals))
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * secs / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded numpy)", "config": dict(w.cfg),
+        "query_rows_per_s": round(rows / secs, 2),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
+                         "sample": f"{rows} sampled query rows over {args.steps} steps"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="decode_bf16_epilogue", choices=WORKLOADS)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "native":
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+        backend = "nccl" if args.impl == "native" else "gloo"
+        dist_mod.init_process_group(backend)
+        dist = dist_mod
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_native(args, rank, world, dist)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,218 @@
+/*
+ * mla.h -- C ABI of libmla: Multi-head Latent Attention over the 576-wide latent KV cache
+ * on one GB300 (sm_103a).
+ *
+ * A cache entry is [kv_c_normed (512) | k_pe (64)], one "head" shared by all query heads
+ * (MQA, num_kv_heads = 1).  Queries are absorbed to [ql_nope (512) | q_pe (64)]; the value
+ * is the first 512 values of the same entry.  Three entry formats:
+ *
+ *   MLA_CACHE_BF16        576 bf16 values, 1152 bytes.
+ *   MLA_CACHE_FP8         576 E4M3 values, 576 bytes, one per-tensor scale (k_scale).
+ *   MLA_CACHE_FP8_DS_MLA  656-byte record: 512 E4M3 | 4 fp32 scales, one per 128-wide
+ *                         tile of the 512 | 64 bf16 rope values ("self-scaling").
+ *
+ * Conventions for every entry point:
+ *   - Pointers marked "device" are device memory owned by the caller; the library never
+ *     allocates, frees or keeps them.  Strides are in elements of the tensor's own type
+ *     unless named *_bytes; the innermost dimension is always contiguous.
+ *   - Work is enqueued on `stream` (0 = legacy default stream); no call synchronises the
+ *     host, except mla_read_device_errors.
+ *   - Return value: MLA_OK (0); MLA_ERR_INVALID (-1) for an argument that breaks the stated
+ *     contract (message in mla_last_error()); MLA_ERR_UNSUPPORTED (-2) for a shape or format
+ *     outside what the kernels serve; MLA_ERR_CUDA (-3) when a launch fails.  Nothing is
+ *     enqueued unless the return value is MLA_OK.  Problems of size zero return MLA_OK
+ *     without launching anything.
+ *   - Index checks that need device data (slot ids, block ids, positions) run inside the
+ *     kernels: a bad index is skipped (masked for attention, not written for inserts) and a
+ *     bit is set in the device error word, readable with mla_read_device_errors.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define MLA_API __attribute__((visibility("default")))
+#else
+#define MLA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MLA_CACHE_BF16 = 0,
+  MLA_CACHE_FP8 = 1,
+  MLA_CACHE_FP8_DS_MLA = 2
+} mla_cache_format;
+
+#define MLA_OK 0
+#define MLA_ERR_INVALID (-1)
+#define MLA_ERR_UNSUPPORTED (-2)
+#define MLA_ERR_CUDA (-3)
+
+/* Device error word bits (mla_read_device_errors). */
+#define MLA_DEVERR_INDEX 1u       /* sparse index outside [0, num_records) that is not a masked negative */
+#define MLA_DEVERR_BLOCK 2u       /* block id outside [0, num_blocks) */
+#define MLA_DEVERR_SLOT 4u        /* insert slot whose block is outside [0, num_blocks) */
+#define MLA_DEVERR_POSITION 8u    /* RoPE position outside [0, max_position) (clamped) */
+#define MLA_DEVERR_TIMEOUT 16u    /* an in-kernel wait gave up (pipeline fault); outputs invalid */
+
+/* Message of the last non-OK return on the calling thread ("" if none). */
+MLA_API const char* mla_last_error(void);
+
+/* Library version string. */
+MLA_API const char* mla_version(void);
+
+/* Synchronise `stream`, copy the device error word (bits above) into *flags and clear it.
+ * Returns MLA_ERR_CUDA if the copy fails. */
+MLA_API int mla_read_device_errors(uint32_t* flags, cudaStream_t stream);
+
+/*
+ * Profiling aid.  While both events are non-NULL, every attention-kernel launch made by
+ * mla_sparse_fwd / mla_paged_decode on the calling host thread is bracketed by
+ * cudaEventRecord(start) and cudaEventRecord(stop) on the call's stream (the split-K merge
+ * and the epilogue are outside the bracket).  Pass NULL, NULL to stop.  The events are the
+ * caller's; the library only records them.
+ */
+MLA_API void mla_profile_attention_events(cudaEvent_t start, cudaEvent_t stop);
+
+/*
+ * Decode epilogue: build the latent query and insert the new latent into the paged cache,
+ * in one launch.
+ * Follows: "vllm.models.kimi_k3.nvidia.ops.fused_mla_key_concat_kv_cache",
+ * fused_mla_decode_q_concat_kv_cache_insert (argument list and format dispatch), with the
+ * saturating E4M3 quant of "vllm.models.kimi_k3.amd.specialized_decode.mono.attention.mla"
+ * (fp8_word).
+ *
+ *   ql_nope      device bf16 [B, H, 512], strides (ql_s0, ql_s1).
+ *   q_pe         device bf16 [B, H, 64], strides (qp_s0, qp_s1).
+ *   kv_c_normed  device bf16 [B, 512], row stride kv_s0.
+ *   k_pe         device bf16 [B, 64] (or [B, 1, 64]), row stride kp_s0.
+ *   mqa_q        device out, contiguous [B, H, 576]: bf16 for MLA_CACHE_BF16 and
+ *                MLA_CACHE_FP8_DS_MLA; E4M3 bytes for MLA_CACHE_FP8, where every element is
+ *                e4m3_sat(x * q_scale_inv).
+ *   kv_cache     device cache: num_blocks blocks at block_stride_bytes, block_size entries
+ *                each at entry_stride_bytes (>= the format's entry size).  Entry of slot s:
+ *                block s / block_size, offset s % block_size.  Written in place:
+ *                  BF16:   [kv_c | rope(k_pe)] as bf16;
+ *                  FP8:    e4m3_sat(x * cache_scale_inv) for all 576 values;
+ *                  DS_MLA: per 128-tile scale s = 2^k, k the least integer with
+ *                          amax <= 448 * 2^k (s = 1 for an all-zero tile, k >= -126),
+ *                          codes e4m3(x / s), scales as fp32, rope as bf16.
+ *   slot_mapping device int64 [B]; a negative slot skips that token's insert (the query is
+ *                still written).
+ *   q_scale_inv, cache_scale_inv  device fp32 scalars; required for MLA_CACHE_FP8, must be
+ *                NULL otherwise.
+ *   positions    device int64 [B] and cos_sin_cache device fp32 [max_position, 64]
+ *                (columns 0..31 cos, 32..63 sin): both NULL (no RoPE) or both set.  RoPE is
+ *                GPT-J style on pairs (2i, 2i+1): y0 = fma(x0, c, -(x1*s)),
+ *                y1 = fma(x1, c, x0*s) in fp32, applied to q_pe and k_pe before storing.
+ * Errors: MLA_ERR_INVALID for NULL tensors, bad strides, mismatched scale / RoPE arguments,
+ * misaligned pointers (bf16 tensors 2-byte aligned; bf16 / fp8_ds_mla cache entries
+ * 4-byte aligned).
+ */
+MLA_API int mla_q_concat_cache_insert(const void* ql_nope, int64_t ql_s0, int64_t ql_s1,
+                              const void* q_pe, int64_t qp_s0, int64_t qp_s1,
+                              const void* kv_c_normed, int64_t kv_s0, const void* k_pe,
+                              int64_t kp_s0, void* mqa_q, void* kv_cache, mla_cache_format fmt,
+                              int64_t num_blocks, int64_t block_stride_bytes,
+                              int64_t entry_stride_bytes, int32_t block_size,
+                              const int64_t* slot_mapping, const float* q_scale_inv,
+                              const float* cache_scale_inv, const int64_t* positions,
+                              const float* cos_sin_cache, int64_t max_position, int32_t B,
+                              int32_t H, cudaStream_t stream);
+
+/*
+ * Sparse MLA forward over fp8_ds_mla records with CSR key lists.
+ * Follows: "vllm.models.kimi_k3.amd.ops.flydsl_sparse_mla", flydsl_sparse_mla_fp8ds_fwd
+ * (sparse_mla_fwd semantics) and flydsl_sparse_mla_fp8ds_supported (argument checks).
+ *
+ *   q            device bf16 [T, H, 576], strides (q_s0, q_s1) in elements, 1 <= H <= 128.
+ *   kv_records   device, num_records records of 656 bytes at record_stride_bytes
+ *                (a multiple of 16, >= 656; base 16-byte aligned).  Any per-128 scale is
+ *                accepted (not only powers of two).
+ *   kv_indptr    device int32 [T + 1], non-decreasing, kv_indptr[0] = 0.
+ *   kv_indices   device int32 [n_indices], flat global record ids (n_indices < 2^31).
+ *                Row t attends to kv_indices[kv_indptr[t] .. kv_indptr[t+1]); duplicates
+ *                count as separate keys.  With has_invalid, entries < 0 are masked; without
+ *                it every entry must be in [0, num_records) (violations are masked and
+ *                reported as MLA_DEVERR_INDEX).
+ *   softmax_scale  logits are softmax_scale * q.k over all 576 values.
+ *   out          device bf16 [T, H, >= 512], strides (o_s0, o_s1); columns 0..511 written
+ *                with softmax(logits) . V, V the 512 dequantised latent values.
+ *   lse          device fp32 [T, H] contiguous, natural-log log-sum-exp of the logits over
+ *                the unmasked keys; NULL to skip.
+ * A row without an unmasked key gets out = 0 and lse = -inf.
+ */
+MLA_API int mla_sparse_fwd(const void* q, int64_t q_s0, int64_t q_s1, const void* kv_records,
+                   int64_t record_stride_bytes, int64_t num_records, const int32_t* kv_indptr,
+                   const int32_t* kv_indices, int64_t n_indices, float softmax_scale,
+                   int has_invalid, void* out, int64_t o_s0, int64_t o_s1, float* lse,
+                   int32_t T, int32_t H, cudaStream_t stream);
+
+/*
+ * Workspace bytes mla_paged_decode needs for this shape (split-K partials).  The split count
+ * depends only on (B * q_len, H, max_context, the device's SM count), never on seq_lens, so
+ * a graph captured once stays valid.  num_sms <= 0 means "the current device's".
+ */
+MLA_API size_t mla_paged_decode_workspace_size(int32_t B, int32_t q_len, int32_t H, int32_t max_context,
+                                       int32_t num_sms);
+
+/*
+ * Paged MLA decode and spec-verify.
+ * Follows: "vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.mla.prepared" --
+ * PreparedMla.stock_core / trtllm_decode (q query tokens per request, causal among them;
+ * split count bounded by max_context; bmm1_scale = softmax_scale * q_scale * k_scale and
+ * bmm2_scale = k_scale for plain fp8) and pad_requests (length 0 -> zero output).
+ *
+ *   q            device [B * q_len, H, 576], strides (q_s0, q_s1) in elements; bf16 for the
+ *                BF16 and DS_MLA caches, E4M3 bytes (raw codes, scale q_scale) for FP8.
+ *                Rows are grouped by request: row b*q_len + i is request b's query i.
+ *   kv_cache     device, num_blocks blocks at block_stride_bytes, block_size entries each at
+ *                entry_stride_bytes (multiple of 16, >= entry size).
+ *   block_table  device int32 [B, >= ceil(max seq_len / block_size)], row stride bt_stride.
+ *   seq_lens     device int32 [B]: keys of request b are positions 0 .. seq_lens[b]-1 (the
+ *                q_len new tokens included); query row i sees positions 0 .. L - q_len + i.
+ *                0 <= seq_lens[b]; lengths beyond max_context are served but unbalanced.
+ *   max_context  upper bound of seq_lens used to fix the split count (> 0).
+ *   softmax_scale, q_scale, k_scale  logits = softmax_scale * q.k (BF16, DS_MLA) or
+ *                softmax_scale * q_scale * k_scale * q8.k8 (FP8, raw codes), FP8 output
+ *                multiplied by k_scale; q_scale / k_scale are ignored for BF16 and DS_MLA.
+ *   out          device bf16 [B * q_len, H, >= 512], strides (o_s0, o_s1).
+ *   lse          device fp32 [B * q_len, H] contiguous, natural log; NULL to skip.
+ *   workspace    device scratch of >= mla_paged_decode_workspace_size(...) bytes, 256-byte
+ *                aligned (may be NULL when that size is 0).  Contents need no initialising
+ *                and are garbage afterwards.
+ * A query row with no visible key gets out = 0 and lse = -inf.
+ */
+MLA_API int mla_paged_decode(const void* q, int64_t q_s0, int64_t q_s1, const void* kv_cache,
+                     mla_cache_format fmt, int64_t num_blocks, int64_t block_stride_bytes,
+                     int64_t entry_stride_bytes, int32_t block_size, const int32_t* block_table,
+                     int64_t bt_stride, const int32_t* seq_lens, int32_t B, int32_t q_len,
+                     int32_t H, int32_t max_context, float softmax_scale, float q_scale,
+                     float k_scale, void* out, int64_t o_s0, int64_t o_s1, float* lse,
+                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Gather-and-dequantise (test and debugging aid): out[i, 0..575] = the exact fp32 values of
+ * the entry at slots[i] (paged addressing as in mla_paged_decode; NoPE times its tile scale
+ * for DS_MLA, raw E4M3 values for FP8).  Same record addressing and decode as the attention
+ * kernels.  Follows "vllm.models.kimi_k3.nvidia.mla", _gather_context_latent's
+ * cp_gather_and_upconvert_fp8_kv_cache (paged latent -> dense values).
+ *   slots device int64 [n]; a negative slot or a bad block id gives a row of zeros.
+ *   out   device fp32 [n, 576] contiguous.
+ */
+MLA_API int mla_gather_dequant(const void* kv_cache, mla_cache_format fmt, int64_t num_blocks,
+                       int64_t block_stride_bytes, int64_t entry_stride_bytes,
+                       int32_t block_size, const int64_t* slots, int64_t n, float* out,
+                       cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

@@ -1,0 +1,405 @@
+// mla_api.cu -- the C ABI declared in include/mla.h: argument checks, split-K planning,
+// workspace carving and kernel launches.  Host code only; every step of the computation
+// runs in the library's kernels.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "mla.h"
+#include "mla_attn.cuh"
+#include "mla_internal.h"
+
+namespace mla {
+namespace {
+
+__device__ uint32_t g_mla_device_errors;
+
+thread_local char g_msg[512] = "";
+thread_local cudaEvent_t g_prof_start = nullptr, g_prof_stop = nullptr;
+
+void prof_begin(cudaStream_t s) {
+  if (g_prof_start && g_prof_stop) cudaEventRecord(g_prof_start, s);
+}
+void prof_end(cudaStream_t s) {
+  if (g_prof_start && g_prof_stop) cudaEventRecord(g_prof_stop, s);
+}
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof g_msg, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int ok() {
+  g_msg[0] = '\0';
+  return MLA_OK;
+}
+
+struct DevInfo {
+  bool ready = false;
+  int sms = 0;
+  uint32_t* err = nullptr;
+};
+DevInfo g_dev[64];
+std::mutex g_dev_mu;
+
+// SM count and device error word of the current device (looked up once per device).
+int dev_info(DevInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+    return fail(MLA_ERR_CUDA, "cudaGetDevice failed");
+  std::lock_guard<std::mutex> lk(g_dev_mu);
+  DevInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return fail(MLA_ERR_CUDA, "cannot query the SM count");
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_mla_device_errors) != cudaSuccess)
+      return fail(MLA_ERR_CUDA, "cannot resolve the device error word");
+    d.err = static_cast<uint32_t*>(p);
+    d.ready = true;
+  }
+  *out = &d;
+  return MLA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int entry_bytes(mla_cache_format f) {
+  return f == MLA_CACHE_BF16 ? 1152 : f == MLA_CACHE_FP8 ? 576 : 656;
+}
+
+struct SplitPlan {
+  int n_splits;
+  int64_t chunk;
+};
+
+// Split-K plan of the paged decode.  The split count depends on the number of (row, head
+// group) units, max_context and the SM count only -- never on seq_lens -- as the pages'
+// decode core fixes its split count from the deployment's longest sequence.  Aim for about
+// eight work items per SM, with at least 8 key tiles (1024 keys) per split.
+SplitPlan plan_splits(int64_t n_rows, int n_hgroups, int max_context, int sms) {
+  const int64_t max_tiles = max_context > 0 ? (max_context + kTile - 1) / kTile : 1;
+  const int64_t base = n_rows * n_hgroups;
+  int64_t splits = base > 0 ? (8LL * sms + base - 1) / base : 1;
+  const int64_t cap = max_tiles / 8 > 1 ? max_tiles / 8 : 1;
+  if (splits > cap) splits = cap;
+  if (splits < 1) splits = 1;
+  const int64_t tiles_per = (max_tiles + splits - 1) / splits;
+  splits = (max_tiles + tiles_per - 1) / tiles_per;
+  return SplitPlan{static_cast<int>(splits), tiles_per * kTile};
+}
+
+size_t workspace_bytes_for(int64_t n_rows, int H, const SplitPlan& sp) {
+  if (sp.n_splits <= 1) return 0;
+  const size_t po = static_cast<size_t>(sp.n_splits) * n_rows * H * kLora * sizeof(float);
+  const size_t pl = static_cast<size_t>(sp.n_splits) * n_rows * H * sizeof(float);
+  return ((po + 255) & ~size_t(255)) + ((pl + 255) & ~size_t(255));
+}
+
+int grid_for(int64_t items, int sms) {
+  return static_cast<int>(items < sms ? items : sms);
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" const char* mla_last_error(void) { return g_msg; }
+
+extern "C" const char* mla_version(void) { return "libmla 0.1 (sm_103a, tcgen05)"; }
+
+extern "C" void mla_profile_attention_events(cudaEvent_t start, cudaEvent_t stop) {
+  g_prof_start = start;
+  g_prof_stop = stop;
+}
+
+extern "C" int mla_read_device_errors(uint32_t* flags, cudaStream_t stream) {
+  if (!flags) return fail(MLA_ERR_INVALID, "flags is NULL");
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return fail(MLA_ERR_CUDA, "stream synchronize failed");
+  uint32_t v = 0;
+  if (cudaMemcpy(&v, d->err, sizeof v, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return fail(MLA_ERR_CUDA, "reading the device error word failed");
+  const uint32_t zero = 0;
+  if (cudaMemcpy(d->err, &zero, sizeof zero, cudaMemcpyHostToDevice) != cudaSuccess)
+    return fail(MLA_ERR_CUDA, "clearing the device error word failed");
+  *flags = v;
+  return ok();
+}
+
+// ------------------------------------------------------------------------------------------
+extern "C" int mla_q_concat_cache_insert(const void* ql_nope, int64_t ql_s0, int64_t ql_s1,
+                                         const void* q_pe, int64_t qp_s0, int64_t qp_s1,
+                                         const void* kv_c_normed, int64_t kv_s0, const void* k_pe,
+                                         int64_t kp_s0, void* mqa_q, void* kv_cache,
+                                         mla_cache_format fmt, int64_t num_blocks,
+                                         int64_t block_stride_bytes, int64_t entry_stride_bytes,
+                                         int32_t block_size, const int64_t* slot_mapping,
+                                         const float* q_scale_inv, const float* cache_scale_inv,
+                                         const int64_t* positions, const float* cos_sin_cache,
+                                         int64_t max_position, int32_t B, int32_t H,
+                                         cudaStream_t stream) {
+  if (fmt != MLA_CACHE_BF16 && fmt != MLA_CACHE_FP8 && fmt != MLA_CACHE_FP8_DS_MLA)
+    return fail(MLA_ERR_INVALID, "unknown cache format %d", static_cast<int>(fmt));
+  if (B < 0 || H < 1) return fail(MLA_ERR_INVALID, "bad shape B=%d H=%d", B, H);
+  if (B == 0) return ok();
+  if (!ql_nope || !q_pe || !kv_c_normed || !k_pe || !mqa_q || !kv_cache || !slot_mapping)
+    return fail(MLA_ERR_INVALID, "a required pointer is NULL");
+  if (ql_s1 < 512 || ql_s0 < static_cast<int64_t>(H) * ql_s1 || qp_s1 < 64 || qp_s0 < static_cast<int64_t>(H) * qp_s1 ||
+      kv_s0 < 512 || kp_s0 < 64)
+    return fail(MLA_ERR_INVALID, "activation strides overlap rows");
+  if (!aligned(ql_nope, 2) || !aligned(q_pe, 2) || !aligned(kv_c_normed, 2) || !aligned(k_pe, 2) || !aligned(mqa_q, 2))
+    return fail(MLA_ERR_INVALID, "bf16 tensors must be 2-byte aligned");
+  if (block_size < 1 || num_blocks < 1) return fail(MLA_ERR_INVALID, "bad cache geometry");
+  if (entry_stride_bytes < entry_bytes(fmt) || block_stride_bytes < entry_stride_bytes * block_size)
+    return fail(MLA_ERR_INVALID, "cache strides smaller than the entries");
+  if (fmt != MLA_CACHE_FP8 && (entry_stride_bytes % 4 || block_stride_bytes % 4 || !aligned(kv_cache, 4)))
+    return fail(MLA_ERR_INVALID, "bf16 / fp8_ds_mla cache entries must be 4-byte aligned");
+  if (fmt == MLA_CACHE_FP8) {
+    if (!q_scale_inv || !cache_scale_inv)
+      return fail(MLA_ERR_INVALID, "the fp8 cache needs q_scale_inv and cache_scale_inv");
+  } else if (q_scale_inv || cache_scale_inv) {
+    return fail(MLA_ERR_INVALID, "q_scale_inv / cache_scale_inv are only for the fp8 cache");
+  }
+  if ((positions == nullptr) != (cos_sin_cache == nullptr))
+    return fail(MLA_ERR_INVALID, "positions and cos_sin_cache must be given together");
+  if (positions && max_position < 1) return fail(MLA_ERR_INVALID, "max_position must be >= 1");
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  EpiParams p{};
+  p.ql_nope = static_cast<const uint16_t*>(ql_nope);
+  p.ql_s0 = ql_s0;
+  p.ql_s1 = ql_s1;
+  p.q_pe = static_cast<const uint16_t*>(q_pe);
+  p.qp_s0 = qp_s0;
+  p.qp_s1 = qp_s1;
+  p.kv_c = static_cast<const uint16_t*>(kv_c_normed);
+  p.kv_s0 = kv_s0;
+  p.k_pe = static_cast<const uint16_t*>(k_pe);
+  p.kp_s0 = kp_s0;
+  p.mqa_q = mqa_q;
+  p.cache = static_cast<uint8_t*>(kv_cache);
+  p.num_blocks = num_blocks;
+  p.block_stride = block_stride_bytes;
+  p.entry_stride = entry_stride_bytes;
+  p.block_size = block_size;
+  p.slot_mapping = slot_mapping;
+  p.q_scale_inv = q_scale_inv;
+  p.cache_scale_inv = cache_scale_inv;
+  p.positions = positions;
+  p.cos_sin = cos_sin_cache;
+  p.max_position = max_position;
+  p.H = H;
+  p.err = d->err;
+  if (launch_epilogue(static_cast<int>(fmt), p, B, stream) != cudaSuccess)
+    return fail(MLA_ERR_CUDA, "epilogue launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  return ok();
+}
+
+// ------------------------------------------------------------------------------------------
+extern "C" int mla_sparse_fwd(const void* q, int64_t q_s0, int64_t q_s1, const void* kv_records,
+                              int64_t record_stride_bytes, int64_t num_records,
+                              const int32_t* kv_indptr, const int32_t* kv_indices, int64_t n_indices,
+                              float softmax_scale, int has_invalid, void* out, int64_t o_s0,
+                              int64_t o_s1, float* lse, int32_t T, int32_t H, cudaStream_t stream) {
+  if (T < 0) return fail(MLA_ERR_INVALID, "T must be >= 0");
+  if (H < 1 || H > 128) return fail(MLA_ERR_UNSUPPORTED, "H must be in [1, 128], got %d", H);
+  if (T == 0) return ok();
+  if (!q || !kv_records || !kv_indptr || !out) return fail(MLA_ERR_INVALID, "a required pointer is NULL");
+  if (n_indices < 0 || n_indices >= (int64_t(1) << 31))
+    return fail(MLA_ERR_UNSUPPORTED, "n_indices must be in [0, 2^31)");
+  if (n_indices > 0 && !kv_indices) return fail(MLA_ERR_INVALID, "kv_indices is NULL");
+  if (num_records < 1) return fail(MLA_ERR_INVALID, "num_records must be >= 1");
+  if (record_stride_bytes < 656 || record_stride_bytes % 16 || !aligned(kv_records, 16))
+    return fail(MLA_ERR_INVALID, "records need a 16-byte aligned base and a pitch that is a multiple of 16 (>= 656)");
+  if (!aligned(q, 16) || q_s1 < 576 || q_s1 % 8 || q_s0 % 8 || q_s0 < static_cast<int64_t>(H) * q_s1)
+    return fail(MLA_ERR_INVALID, "q must be 16-byte aligned with strides that are multiples of 8 elements");
+  if (!aligned(out, 2) || o_s1 < 512 || o_s0 < static_cast<int64_t>(H) * o_s1)
+    return fail(MLA_ERR_INVALID, "bad out strides");
+  if (lse && !aligned(lse, 4)) return fail(MLA_ERR_INVALID, "lse must be 4-byte aligned");
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  AttnParams p{};
+  p.q = static_cast<const uint8_t*>(q);
+  p.q_s0b = q_s0 * 2;
+  p.q_s1b = q_s1 * 2;
+  p.H = H;
+  p.n_hgroups = (H + kRows - 1) / kRows;
+  p.records = static_cast<const uint8_t*>(kv_records);
+  p.rec_stride = record_stride_bytes;
+  p.num_records = num_records;
+  p.indptr = kv_indptr;
+  p.indices = kv_indices;
+  p.has_invalid = has_invalid ? 1 : 0;
+  p.q_len = 1;
+  p.n_splits = 1;
+  p.chunk = 0;
+  p.n_rows = T;
+  p.n_items = T * p.n_hgroups;
+  p.sig2 = softmax_scale * 1.4426950408889634f;
+  p.out_scale = 1.f;
+  p.out = static_cast<uint8_t*>(out);
+  p.o_s0b = o_s0 * 2;
+  p.o_s1b = o_s1 * 2;
+  p.lse = lse;
+  p.err = d->err;
+  prof_begin(stream);
+  const cudaError_t e = launch_attn_sparse_ds(p, grid_for(p.n_items, d->sms), stream);
+  prof_end(stream);
+  if (e != cudaSuccess)
+    return fail(MLA_ERR_CUDA, "sparse attention launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  return ok();
+}
+
+// ------------------------------------------------------------------------------------------
+extern "C" size_t mla_paged_decode_workspace_size(int32_t B, int32_t q_len, int32_t H,
+                                                  int32_t max_context, int32_t num_sms) {
+  if (B <= 0 || q_len <= 0 || H <= 0 || max_context <= 0) return 0;
+  int sms = num_sms;
+  if (sms <= 0) {
+    DevInfo* d = nullptr;
+    if (dev_info(&d) != MLA_OK) return 0;
+    sms = d->sms;
+  }
+  const int64_t n_rows = static_cast<int64_t>(B) * q_len;
+  const SplitPlan sp = plan_splits(n_rows, (H + kRows - 1) / kRows, max_context, sms);
+  return workspace_bytes_for(n_rows, H, sp);
+}
+
+extern "C" int mla_paged_decode(const void* q, int64_t q_s0, int64_t q_s1, const void* kv_cache,
+                                mla_cache_format fmt, int64_t num_blocks, int64_t block_stride_bytes,
+                                int64_t entry_stride_bytes, int32_t block_size,
+                                const int32_t* block_table, int64_t bt_stride, const int32_t* seq_lens,
+                                int32_t B, int32_t q_len, int32_t H, int32_t max_context,
+                                float softmax_scale, float q_scale, float k_scale, void* out,
+                                int64_t o_s0, int64_t o_s1, float* lse, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+  if (fmt != MLA_CACHE_BF16 && fmt != MLA_CACHE_FP8 && fmt != MLA_CACHE_FP8_DS_MLA)
+    return fail(MLA_ERR_INVALID, "unknown cache format %d", static_cast<int>(fmt));
+  if (B < 0 || q_len < 1 || H < 1) return fail(MLA_ERR_INVALID, "bad shape B=%d q_len=%d H=%d", B, q_len, H);
+  if (H > 128) return fail(MLA_ERR_UNSUPPORTED, "H must be <= 128, got %d", H);
+  if (max_context < 1) return fail(MLA_ERR_INVALID, "max_context must be >= 1");
+  if (B == 0) return ok();
+  if (!q || !kv_cache || !block_table || !seq_lens || !out) return fail(MLA_ERR_INVALID, "a required pointer is NULL");
+  if (block_size < 1 || num_blocks < 1 || bt_stride < 1) return fail(MLA_ERR_INVALID, "bad cache geometry");
+  if (entry_stride_bytes < entry_bytes(fmt) || entry_stride_bytes % 16 || block_stride_bytes % 16 ||
+      block_stride_bytes < entry_stride_bytes * block_size || !aligned(kv_cache, 16))
+    return fail(MLA_ERR_INVALID, "cache entries need 16-byte alignment and non-overlapping strides");
+  const int qalign = fmt == MLA_CACHE_FP8 ? 8 : 16;
+  if (!aligned(q, qalign) || q_s1 < 576 || q_s1 % 8 || q_s0 % 8 || q_s0 < static_cast<int64_t>(H) * q_s1)
+    return fail(MLA_ERR_INVALID, "q must be %d-byte aligned with strides that are multiples of 8 elements", qalign);
+  if (!aligned(out, 2) || o_s1 < 512 || o_s0 < static_cast<int64_t>(H) * o_s1)
+    return fail(MLA_ERR_INVALID, "bad out strides");
+  if (lse && !aligned(lse, 4)) return fail(MLA_ERR_INVALID, "lse must be 4-byte aligned");
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  const int64_t n_rows = static_cast<int64_t>(B) * q_len;
+  const int n_hgroups = (H + kRows - 1) / kRows;
+  const SplitPlan sp = plan_splits(n_rows, n_hgroups, max_context, d->sms);
+  const size_t need = workspace_bytes_for(n_rows, H, sp);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need)
+      return fail(MLA_ERR_INVALID, "workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
+    if (!aligned(workspace, 256)) return fail(MLA_ERR_INVALID, "workspace must be 256-byte aligned");
+  }
+  const int64_t items = n_rows * n_hgroups * sp.n_splits;
+  if (items >= (int64_t(1) << 31)) return fail(MLA_ERR_UNSUPPORTED, "too many work items");
+  AttnParams p{};
+  const int qe = fmt == MLA_CACHE_FP8 ? 1 : 2;
+  p.q = static_cast<const uint8_t*>(q);
+  p.q_s0b = q_s0 * qe;
+  p.q_s1b = q_s1 * qe;
+  p.H = H;
+  p.n_hgroups = n_hgroups;
+  p.cache = static_cast<const uint8_t*>(kv_cache);
+  p.num_blocks = num_blocks;
+  p.block_stride = block_stride_bytes;
+  p.entry_stride = entry_stride_bytes;
+  p.block_size = block_size;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.seq_lens = seq_lens;
+  p.q_len = q_len;
+  p.chunk = sp.chunk;
+  p.n_splits = sp.n_splits;
+  p.n_rows = static_cast<int>(n_rows);
+  p.n_items = static_cast<int>(items);
+  const float sigma = fmt == MLA_CACHE_FP8 ? softmax_scale * q_scale * k_scale : softmax_scale;
+  p.sig2 = sigma * 1.4426950408889634f;
+  p.out_scale = fmt == MLA_CACHE_FP8 ? k_scale : 1.f;
+  p.out = static_cast<uint8_t*>(out);
+  p.o_s0b = o_s0 * 2;
+  p.o_s1b = o_s1 * 2;
+  p.lse = lse;
+  if (sp.n_splits > 1) {
+    const size_t po = static_cast<size_t>(sp.n_splits) * n_rows * H * kLora * sizeof(float);
+    p.part_o = static_cast<float*>(workspace);
+    p.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ((po + 255) & ~size_t(255)));
+  }
+  p.err = d->err;
+  const int grid = grid_for(items, d->sms);
+  cudaError_t e;
+  prof_begin(stream);
+  if (fmt == MLA_CACHE_BF16)
+    e = launch_attn_paged_bf16(p, grid, stream);
+  else if (fmt == MLA_CACHE_FP8)
+    e = launch_attn_paged_fp8(p, grid, stream);
+  else
+    e = launch_attn_paged_ds(p, grid, stream);
+  prof_end(stream);
+  if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "decode attention launch failed: %s", cudaGetErrorString(e));
+  if (sp.n_splits > 1) {
+    MergeParams m{};
+    m.part_o = p.part_o;
+    m.part_lse = p.part_lse;
+    m.S = sp.n_splits;
+    m.n_rows = static_cast<int>(n_rows);
+    m.H = H;
+    m.out = p.out;
+    m.o_s0b = p.o_s0b;
+    m.o_s1b = p.o_s1b;
+    m.lse = lse;
+    if (launch_merge(m, stream) != cudaSuccess)
+      return fail(MLA_ERR_CUDA, "merge launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  }
+  return ok();
+}
+
+// ------------------------------------------------------------------------------------------
+extern "C" int mla_gather_dequant(const void* kv_cache, mla_cache_format fmt, int64_t num_blocks,
+                                  int64_t block_stride_bytes, int64_t entry_stride_bytes,
+                                  int32_t block_size, const int64_t* slots, int64_t n, float* out,
+                                  cudaStream_t stream) {
+  if (fmt != MLA_CACHE_BF16 && fmt != MLA_CACHE_FP8 && fmt != MLA_CACHE_FP8_DS_MLA)
+    return fail(MLA_ERR_INVALID, "unknown cache format %d", static_cast<int>(fmt));
+  if (n < 0) return fail(MLA_ERR_INVALID, "n must be >= 0");
+  if (n == 0) return ok();
+  if (!kv_cache || !slots || !out) return fail(MLA_ERR_INVALID, "a required pointer is NULL");
+  if (block_size < 1 || num_blocks < 1 || entry_stride_bytes < entry_bytes(fmt) ||
+      block_stride_bytes < entry_stride_bytes * block_size)
+    return fail(MLA_ERR_INVALID, "bad cache geometry");
+  if (fmt != MLA_CACHE_FP8 && (entry_stride_bytes % 4 || block_stride_bytes % 4 || !aligned(kv_cache, 4)))
+    return fail(MLA_ERR_INVALID, "bf16 / fp8_ds_mla entries must be 4-byte aligned");
+  if (n > (int64_t(1) << 33)) return fail(MLA_ERR_UNSUPPORTED, "n too large");
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  GatherParams p{};
+  p.cache = static_cast<const uint8_t*>(kv_cache);
+  p.num_blocks = num_blocks;
+  p.block_stride = block_stride_bytes;
+  p.entry_stride = entry_stride_bytes;
+  p.block_size = block_size;
+  p.slots = slots;
+  p.n = n;
+  p.out = out;
+  p.err = d->err;
+  if (launch_gather(static_cast<int>(fmt), p, stream) != cudaSuccess)
+    return fail(MLA_ERR_CUDA, "gather launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  return ok();
+}

@@ -1,0 +1,64 @@
+// mla_internal.h -- parameter blocks and launchers shared by the library's translation
+// units (not part of the public C ABI).
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace mla {
+
+struct AttnParams;
+
+struct EpiParams {
+  const uint16_t* ql_nope;
+  int64_t ql_s0, ql_s1;
+  const uint16_t* q_pe;
+  int64_t qp_s0, qp_s1;
+  const uint16_t* kv_c;
+  int64_t kv_s0;
+  const uint16_t* k_pe;
+  int64_t kp_s0;
+  void* mqa_q;
+  uint8_t* cache;
+  int64_t num_blocks, block_stride, entry_stride;
+  int block_size;
+  const int64_t* slot_mapping;
+  const float* q_scale_inv;
+  const float* cache_scale_inv;
+  const int64_t* positions;
+  const float* cos_sin;
+  int64_t max_position;
+  int H;
+  uint32_t* err;
+};
+
+struct MergeParams {
+  const float* part_o;     // [S][n_rows][H][512]
+  const float* part_lse;   // [S][n_rows][H]
+  int S, n_rows, H;
+  uint8_t* out;            // bf16 rows
+  int64_t o_s0b, o_s1b;
+  float* lse;              // [n_rows, H] or null
+};
+
+struct GatherParams {
+  const uint8_t* cache;
+  int64_t num_blocks, block_stride, entry_stride;
+  int block_size;
+  const int64_t* slots;
+  int64_t n;
+  float* out;
+  uint32_t* err;
+};
+
+cudaError_t launch_epilogue(int fmt, const EpiParams& p, int B, cudaStream_t stream);
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+cudaError_t launch_gather(int fmt, const GatherParams& p, cudaStream_t stream);
+
+// Attention launchers (one translation unit per cache format).  `grid` CTAs, each looping
+// over work items; dynamic shared memory is set up on first use per device.
+cudaError_t launch_attn_sparse_ds(const AttnParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_attn_paged_bf16(const AttnParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_attn_paged_fp8(const AttnParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_attn_paged_ds(const AttnParams& p, int grid, cudaStream_t stream);
+
+}  // namespace mla

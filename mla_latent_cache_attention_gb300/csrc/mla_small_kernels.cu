@@ -1,0 +1,248 @@
+// mla_small_kernels.cu -- the memory-bound kernels around the attention core:
+//   * the decode epilogue (q concat + latent insert), one CTA per token;
+//   * the split-K merge of partial attentions by their log-sum-exp;
+//   * gather-and-dequantise of cache entries (a test aid with the kernels' addressing).
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <math_constants.h>
+
+#include "mla_internal.h"
+#include "mla_ptx.cuh"
+
+namespace mla {
+
+// ------------------------------------------------------------------------------------------
+// Decode epilogue.  "vllm.models.kimi_k3.nvidia.ops.fused_mla_key_concat_kv_cache",
+// fused_mla_decode_q_concat_kv_cache_insert: mqa_q = [ql_nope | q_pe], then the latent
+// [kv_c_normed | k_pe] is written at slot_mapping; optional GPT-J RoPE from an fp32 table.
+
+__device__ __forceinline__ float bf16_at(const uint16_t* p) {
+  return __uint_as_float(static_cast<uint32_t>(*p) << 16);
+}
+__device__ __forceinline__ uint16_t bf16_bits(float x) {
+  __nv_bfloat16 b = __float2bfloat16_rn(x);
+  return *reinterpret_cast<uint16_t*>(&b);
+}
+__device__ __forceinline__ uint8_t e4m3_sat(float x) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
+}
+
+// GPT-J rotation of pair (x0, x1) by (c, s) in fp32: y0 = x0*c - x1*s, y1 = x1*c + x0*s with
+// the product x1*s (x0*s) rounded before the fused multiply-add.
+__device__ __forceinline__ void rope_pair(float x0, float x1, float c, float s, float& y0, float& y1) {
+  y0 = __fmaf_rn(x0, c, -__fmul_rn(x1, s));
+  y1 = __fmaf_rn(x1, c, __fmul_rn(x0, s));
+}
+
+// fp8_ds_mla tile scale: 2^k with k the least integer such that amax <= 448 * 2^k,
+// clamped to k >= -126; an all-zero tile gets k = 0.  Works on the fp32 bits of amax
+// (448 * 2^k = 1.75 * 2^(8+k)).
+__device__ __forceinline__ int ds_tile_exponent(float amax) {
+  const uint32_t u = __float_as_uint(amax);
+  if (u == 0u) return 0;
+  const int e_field = static_cast<int>(u >> 23);
+  if (e_field == 0) return -126;                       // subnormal amax
+  const int E = e_field - 127;
+  const uint32_t m = u & 0x7FFFFFu;
+  int k = E - 8 + (m > 0x600000u ? 1 : 0);
+  return k < -126 ? -126 : k;
+}
+
+template <int F>
+__global__ void __launch_bounds__(256) mla_epilogue_kernel(const EpiParams p) {
+  const int b = blockIdx.x, tid = threadIdx.x;
+  const float qinv = (F == 1) ? *p.q_scale_inv : 1.f;
+  const float cinv = (F == 1) ? *p.cache_scale_inv : 1.f;
+  const float* cs = nullptr;
+  if (p.positions) {
+    int64_t pos = p.positions[b];
+    if (pos < 0 || pos >= p.max_position) {
+      if (tid == 0) set_device_error(p.err, 8u);
+      pos = pos < 0 ? 0 : p.max_position - 1;
+    }
+    cs = p.cos_sin + pos * 64;
+  }
+  // ---- query concat
+  const int H = p.H;
+  for (int i = tid; i < H * 512; i += blockDim.x) {
+    const int h = i >> 9, d = i & 511;
+    const uint16_t v = p.ql_nope[b * p.ql_s0 + h * p.ql_s1 + d];
+    const int64_t o = (static_cast<int64_t>(b) * H + h) * 576 + d;
+    if (F == 1) {
+      reinterpret_cast<uint8_t*>(p.mqa_q)[o] = e4m3_sat(__uint_as_float(static_cast<uint32_t>(v) << 16) * qinv);
+    } else {
+      reinterpret_cast<uint16_t*>(p.mqa_q)[o] = v;
+    }
+  }
+  for (int i = tid; i < H * 32; i += blockDim.x) {
+    const int h = i >> 5, pr = i & 31;
+    const uint16_t* src = p.q_pe + b * p.qp_s0 + h * p.qp_s1 + 2 * pr;
+    float y0 = bf16_at(src), y1 = bf16_at(src + 1);
+    if (cs) rope_pair(y0, y1, cs[pr], cs[32 + pr], y0, y1);
+    const int64_t o = (static_cast<int64_t>(b) * H + h) * 576 + 512 + 2 * pr;
+    if (F == 1) {
+      uint8_t* q8 = reinterpret_cast<uint8_t*>(p.mqa_q);
+      q8[o] = e4m3_sat(y0 * qinv);
+      q8[o + 1] = e4m3_sat(y1 * qinv);
+    } else {
+      uint16_t* q16 = reinterpret_cast<uint16_t*>(p.mqa_q);
+      q16[o] = bf16_bits(y0);
+      q16[o + 1] = bf16_bits(y1);
+    }
+  }
+  // ---- latent insert
+  const int64_t slot = p.slot_mapping[b];
+  if (slot < 0) return;
+  const int64_t blk = slot / p.block_size;
+  if (blk >= p.num_blocks) {
+    if (tid == 0) set_device_error(p.err, 4u);
+    return;
+  }
+  uint8_t* ent = p.cache + blk * p.block_stride + (slot % p.block_size) * p.entry_stride;
+  const uint16_t* kc = p.kv_c + b * p.kv_s0;
+  const uint16_t* kr = p.k_pe + b * p.kp_s0;
+  if (tid < 32) {   // rope part, one pair per lane
+    float y0 = bf16_at(kr + 2 * tid), y1 = bf16_at(kr + 2 * tid + 1);
+    if (cs) rope_pair(y0, y1, cs[tid], cs[32 + tid], y0, y1);
+    if (F == 0) {
+      reinterpret_cast<uint16_t*>(ent)[512 + 2 * tid] = bf16_bits(y0);
+      reinterpret_cast<uint16_t*>(ent)[512 + 2 * tid + 1] = bf16_bits(y1);
+    } else if (F == 1) {
+      ent[512 + 2 * tid] = e4m3_sat(y0 * cinv);
+      ent[512 + 2 * tid + 1] = e4m3_sat(y1 * cinv);
+    } else {
+      reinterpret_cast<uint16_t*>(ent + 528)[2 * tid] = bf16_bits(y0);
+      reinterpret_cast<uint16_t*>(ent + 528)[2 * tid + 1] = bf16_bits(y1);
+    }
+  }
+  if (F == 0) {
+    for (int d = tid; d < 512; d += blockDim.x) reinterpret_cast<uint16_t*>(ent)[d] = kc[d];
+  } else if (F == 1) {
+    for (int d = tid; d < 512; d += blockDim.x) ent[d] = e4m3_sat(bf16_at(kc + d) * cinv);
+  } else {
+    // warps 0..3: one 128-wide tile each, 4 values per lane
+    const int w = tid >> 5, lane = tid & 31;
+    if (w < 4) {
+      float x[4];
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        x[i] = bf16_at(kc + 128 * w + 4 * lane + i);
+        amax = fmaxf(amax, fabsf(x[i]));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+      const int k = ds_tile_exponent(amax);
+      const float inv = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);   // 2^-k, exact
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ent[128 * w + 4 * lane + i] = e4m3_sat(x[i] * inv);
+      if (lane == 0) {
+        const float s = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+        *reinterpret_cast<float*>(ent + 512 + 4 * w) = s;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+// Split-K merge: out = sum_s exp(lse_s - lse) * O_s, lse = ln sum_s exp(lse_s).  The same
+// combine as vLLM's merge_attn_states ("vllm.models.kimi_k3.nvidia.mla",
+// _forward_prefill_fused) applied across the key splits of one decode row.  One CTA of 128
+// threads per (row, head); each thread owns 4 of the 512 columns.
+__global__ void __launch_bounds__(128) mla_merge_kernel(const MergeParams p) {
+  const int64_t rh = blockIdx.x;
+  const int64_t stride = static_cast<int64_t>(p.n_rows) * p.H;
+  float m = -CUDART_INF_F;
+  for (int s = 0; s < p.S; ++s) m = fmaxf(m, p.part_lse[s * stride + rh]);
+  const int row = static_cast<int>(rh / p.H), h = static_cast<int>(rh % p.H);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float wsum = 0.f;
+  if (m != -CUDART_INF_F) {
+    for (int s = 0; s < p.S; ++s) {
+      const float ls = p.part_lse[s * stride + rh];
+      if (ls == -CUDART_INF_F) continue;
+      const float w = expf(ls - m);
+      wsum += w;
+      const float4 o = reinterpret_cast<const float4*>(p.part_o + (s * stride + rh) * 512)[threadIdx.x];
+      acc.x += w * o.x;
+      acc.y += w * o.y;
+      acc.z += w * o.z;
+      acc.w += w * o.w;
+    }
+  }
+  const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+  __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out + row * p.o_s0b + h * p.o_s1b) + 4 * threadIdx.x;
+  dst[0] = __float2bfloat16_rn(acc.x * inv);
+  dst[1] = __float2bfloat16_rn(acc.y * inv);
+  dst[2] = __float2bfloat16_rn(acc.z * inv);
+  dst[3] = __float2bfloat16_rn(acc.w * inv);
+  if (threadIdx.x == 0 && p.lse) p.lse[rh] = wsum > 0.f ? m + logf(wsum) : -CUDART_INF_F;
+}
+
+// ------------------------------------------------------------------------------------------
+// Gather and dequantise: one warp per slot, 18 values per lane.
+template <int F>
+__global__ void mla_gather_kernel(const GatherParams p) {
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (i >= p.n) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t slot = p.slots[i];
+  const uint8_t* ent = nullptr;
+  if (slot >= 0) {
+    const int64_t blk = slot / p.block_size;
+    if (blk < p.num_blocks)
+      ent = p.cache + blk * p.block_stride + (slot % p.block_size) * p.entry_stride;
+    else if (lane == 0)
+      set_device_error(p.err, 2u);
+  }
+  float* o = p.out + i * 576;
+  for (int d = lane; d < 576; d += 32) {
+    float v = 0.f;
+    if (ent) {
+      if (F == 0) {
+        v = bf16_at(reinterpret_cast<const uint16_t*>(ent) + d);
+      } else if (F == 1) {
+        __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(ent[d]), __NV_E4M3);
+        v = __half2float(__half(h));
+      } else if (d < 512) {
+        __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(ent[d]), __NV_E4M3);
+        v = __half2float(__half(h)) * reinterpret_cast<const float*>(ent + 512)[d >> 7];
+      } else {
+        v = bf16_at(reinterpret_cast<const uint16_t*>(ent + 528) + (d - 512));
+      }
+    }
+    o[d] = v;
+  }
+}
+
+// ------------------------------------------------------------------------------------------
+cudaError_t launch_epilogue(int fmt, const EpiParams& p, int B, cudaStream_t stream) {
+  if (fmt == 0)
+    mla_epilogue_kernel<0><<<B, 256, 0, stream>>>(p);
+  else if (fmt == 1)
+    mla_epilogue_kernel<1><<<B, 256, 0, stream>>>(p);
+  else
+    mla_epilogue_kernel<2><<<B, 256, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
+  const int64_t n = static_cast<int64_t>(p.n_rows) * p.H;
+  if (n == 0) return cudaSuccess;
+  mla_merge_kernel<<<static_cast<unsigned>(n), 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(int fmt, const GatherParams& p, cudaStream_t stream) {
+  const unsigned grid = static_cast<unsigned>((p.n + 3) / 4);
+  if (fmt == 0)
+    mla_gather_kernel<0><<<grid, 128, 0, stream>>>(p);
+  else if (fmt == 1)
+    mla_gather_kernel<1><<<grid, 128, 0, stream>>>(p);
+  else
+    mla_gather_kernel<2><<<grid, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace mla
