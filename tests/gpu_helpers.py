@@ -42,11 +42,13 @@ def assert_attn_close(out_gpu: torch.Tensor, ref: np.ndarray, what=""):
                              f"gpu {o[tuple(i[0])]} oracle {ref[tuple(i[0])]}; max err {err.max()}")
 
 
-def assert_lse_close(lse_gpu: torch.Tensor, ref: np.ndarray, what=""):
+def assert_lse_close(lse_gpu: torch.Tensor, ref: np.ndarray, what="", rel=0.0):
+    """|lse_gpu - lse_oracle| <= LSE_TOL (+ rel * |lse_oracle| where a test's logits are so
+    large that fp32 itself cannot resolve 1e-3: one fp32 ulp at 3e4 is 2e-3)."""
     l = lse_gpu.cpu().numpy().astype(np.float64)
     fin = np.isfinite(ref)
     assert np.array_equal(np.isfinite(l), fin), f"{what}: -inf pattern differs"
     assert np.all(l[~fin] == -np.inf), f"{what}: empty rows must give -inf"
     if fin.any():
-        err = np.abs(l[fin] - ref[fin]).max()
-        assert err <= LSE_TOL, f"{what}: lse max err {err}"
+        err = np.abs(l[fin] - ref[fin])
+        assert np.all(err <= LSE_TOL + rel * np.abs(ref[fin])), f"{what}: lse max err {err.max()}"

@@ -115,7 +115,8 @@ def test_power_of_two_and_large_scales(m):
     c.records[:, 512:528] = (2.0 ** rng.integers(-6, 8, size=(256, 4))).astype(np.float32).view(np.uint8)
     o, l, ro, rl = run(m, c)
     assert_attn_close(o, ro, "pow2 scales")
-    assert_lse_close(l, rl, "pow2 scales")
+    # scales up to 2^7 put |lse| near 3e4, where fp32 resolution is 2e-3: allow 1e-6 relative
+    assert_lse_close(l, rl, "pow2 scales", rel=1e-6)
 
 
 def test_out_of_range_index_is_masked_and_flagged(m):
