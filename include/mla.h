@@ -198,6 +198,33 @@ MLA_API int mla_paged_decode(const void* q, int64_t q_s0, int64_t q_s1, const vo
                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Paged decode for callers that cannot allocate device memory.  The pages have no
+ * counterpart of this entry point; it exists for callers such as code running where
+ * cudaMalloc is not allowed (e.g. while a stream is being captured), plug-ins inside an engine
+ * that owns all device memory and lends them none, and serving loops that forbid allocation
+ * on the request path.
+ *
+ * Same arguments and results as mla_paged_decode, without workspace: the split-K partials go
+ * to a scratch array inside the library (a file-scope __device__ buffer of 64 MiB, held on
+ * every device where the library's code is loaded until the process exits).  The call
+ * allocates nothing.
+ *   - Shapes whose split-K scratch (mla_paged_decode_workspace_size) exceeds 64 MiB are
+ *     rejected with MLA_ERR_UNSUPPORTED and a message in mla_last_error().
+ *   - The first call on a device looks up the scratch's device address (once per device, with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the scratch, which keeps the previous call's contents; the decode writes
+ *     every partial it reads, so nothing needs clearing.  Calls whose kernels may overlap on
+ *     the GPU (e.g. on unordered streams) race on the scratch: order them.
+ */
+MLA_API int mla_paged_decode_noalloc(const void* q, int64_t q_s0, int64_t q_s1, const void* kv_cache,
+                                     mla_cache_format fmt, int64_t num_blocks, int64_t block_stride_bytes,
+                                     int64_t entry_stride_bytes, int32_t block_size,
+                                     const int32_t* block_table, int64_t bt_stride, const int32_t* seq_lens,
+                                     int32_t B, int32_t q_len, int32_t H, int32_t max_context,
+                                     float softmax_scale, float q_scale, float k_scale, void* out,
+                                     int64_t o_s0, int64_t o_s1, float* lse, cudaStream_t stream);
+
+/*
  * Gather-and-dequantise (test and debugging aid): out[i, 0..575] = the exact fp32 values of
  * the entry at slots[i] (paged addressing as in mla_paged_decode; NoPE times its tile scale
  * for DS_MLA, raw E4M3 values for FP8).  Same record addressing and decode as the attention

@@ -57,6 +57,9 @@ def lib():
         L.mla_paged_decode_workspace_size.restype = sz
         L.mla_paged_decode.argtypes = [vp, i64, i64, vp, i32, i64, i64, i64, i32, vp, i64, vp, i32, i32, i32,
                                        i32, f32, f32, f32, vp, i64, i64, vp, vp, sz, vp]
+        L.mla_paged_decode_noalloc.argtypes = [vp, i64, i64, vp, i32, i64, i64, i64, i32, vp, i64, vp, i32, i32,
+                                               i32, i32, f32, f32, f32, vp, i64, i64, vp, vp]
+        L.mla_paged_decode_noalloc.restype = ctypes.c_int
         L.mla_profile_attention_events.argtypes = [vp, vp]
         L.mla_profile_attention_events.restype = None
         L.mla_gather_dequant.argtypes = [vp, i32, i64, i64, i64, i32, vp, i64, vp, vp]

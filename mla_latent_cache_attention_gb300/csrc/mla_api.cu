@@ -105,6 +105,9 @@ int grid_for(int64_t items, int sms) {
 }
 
 }  // namespace
+
+void set_error_message(const char* msg) { snprintf(g_msg, sizeof g_msg, "%s", msg); }
+
 }  // namespace mla
 
 using namespace mla;

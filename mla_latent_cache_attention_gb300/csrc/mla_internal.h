@@ -50,6 +50,9 @@ struct GatherParams {
   uint32_t* err;
 };
 
+// Set the message mla_last_error() returns on this thread.
+void set_error_message(const char* msg);
+
 cudaError_t launch_epilogue(int fmt, const EpiParams& p, int B, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_gather(int fmt, const GatherParams& p, cudaStream_t stream);
