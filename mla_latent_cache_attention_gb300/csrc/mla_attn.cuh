@@ -20,10 +20,11 @@
 // PV folds scale_j into P (four P matrices, one per output tile j).  Plain fp8 converts all
 // 576 codes to f16 exactly (q too); bf16 uses the cache bytes as they are.
 //
-// CTA = 6 warps: warp 0 gathers entries with 1-D bulk copies into a staging ring, warp 1
-// issues the MMAs (one thread) and owns TMEM, warps 2..5 convert staged entries into the
-// swizzled operand tile, run the online softmax (one thread per key lane) and the epilogue
-// (one thread per output column d).
+// CTA = 10 warps: warp 0 gathers entries with 1-D bulk copies into a staging ring (and
+// prefetches two tiles ahead into L2), warp 1 issues the MMAs (one thread) and owns TMEM,
+// warps 6..9 convert staged entries into the swizzled operand tile (one thread per entry),
+// warps 2..5 run the online softmax (one thread per key lane) and the epilogue (one thread
+// per output column d).
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -37,42 +38,68 @@ namespace mla {
 
 enum : int { kBF16 = 0, kFP8 = 1, kDS = 2 };
 
+#ifdef MLA_TIMELINE
+// Debug timeline (never in the product build): per CTA (first 4) and role, a log of
+// (event id, %globaltimer) pairs.
+constexpr int kTlCtas = 4, kTlRoles = 4, kTlEvents = 512;
+__device__ unsigned long long g_tl[kTlCtas][kTlRoles][kTlEvents][2];
+__device__ int g_tl_n[kTlCtas][kTlRoles];
+__device__ __forceinline__ void tl_mark(int role, int ev) {
+  if (blockIdx.x < kTlCtas) {
+    int& n = g_tl_n[blockIdx.x][role];
+    if (n < kTlEvents) {
+      g_tl[blockIdx.x][role][n][0] = ev;
+      g_tl[blockIdx.x][role][n][1] = globaltimer();
+      ++n;
+    }
+  }
+}
+#define TL(role, ev) tl_mark(role, ev)
+#else
+#define TL(role, ev) ((void)0)
+#endif
+
 constexpr int kTile = 128;               // keys per tile (MMA M, TMEM lanes)
 constexpr int kRows = 16;                // heads per CTA (MMA N)
 constexpr int kEntry = 576, kLora = 512;
 constexpr int kBlk = 9;                  // 64-wide blocks of d in 576
 constexpr int kBlkBytes = kTile * 128;   // one SW128 block of the key tile: 128 rows x 128 B
 constexpr int kQBlkBytes = kRows * 128;  // one SW128 block of the query tile
-constexpr int kStages = 2;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;            // 10 warps, see the role map below
 constexpr int kTmemCols = 256;
 constexpr int kOCol = 128;               // TMEM column of the O^T accumulators
+constexpr int kSmemLimit = 232448;       // opt-in shared memory per block on sm_100-class parts
 
+// Per-format staging: entries are gathered with one bulk copy each into a staging piece of
+// kPiece entries at a pitch of kRecPad bytes (an odd number of 16-byte units, so that one
+// thread per entry reads shared memory without bank conflicts).
 template <int F> struct Fmt;
 template <> struct Fmt<kBF16> {
-  static constexpr int kRec = 1152, kPiece = 16, kNP = 1;
+  static constexpr int kRec = 1152, kRecPad = 1168, kPiece = 16, kStages = 3, kNP = 1;
 };
 template <> struct Fmt<kFP8> {
-  static constexpr int kRec = 576, kPiece = 32, kNP = 1;
+  static constexpr int kRec = 576, kRecPad = 592, kPiece = 32, kStages = 3, kNP = 1;
 };
 template <> struct Fmt<kDS> {
-  static constexpr int kRec = 656, kPiece = 32, kNP = 4;
+  static constexpr int kRec = 656, kRecPad = 656, kPiece = 32, kStages = 2, kNP = 4;
 };
 
 template <int F> struct Smem {
   static constexpr int kKV = 0;
-  static constexpr int kQ = kKV + kBlk * kBlkBytes;              // 147456
-  static constexpr int kP = kQ + kBlk * kQBlkBytes;               // +18432
+  static constexpr int kQ = kKV + kBlk * kBlkBytes;               // 147456
+  static constexpr int kP = kQ + kBlk * kQBlkBytes;                // +18432
   static constexpr int kStage = kP + Fmt<F>::kNP * 4096;
-  static constexpr int kStageBytes = Fmt<F>::kPiece * Fmt<F>::kRec;
-  static constexpr int kScale = kStage + kStages * kStageBytes;   // [128][4] fp32
-  static constexpr int kValid = kScale + kTile * 16;              // [128] u8
-  static constexpr int kRed = kValid + kTile;                     // [2][4][16] fp32
-  static constexpr int kBar = kRed + 2 * 4 * 16 * 4;              // mbarriers (8-byte aligned)
-  static constexpr int kNumBars = 2 * kStages + 5;
-  static constexpr int kMisc = kBar + kNumBars * 8;               // meta[kStages], tmem addr, abort
+  static constexpr int kStageBytes = Fmt<F>::kPiece * Fmt<F>::kRecPad;
+  static constexpr int kScale = kStage + Fmt<F>::kStages * kStageBytes;   // [128][4] fp32
+  static constexpr int kValid = kScale + kTile * 16;               // [128] u8
+  static constexpr int kRed = kValid + kTile;                      // [2][4][16] + [4][16] fp32
+  static constexpr int kBar = kRed + 3 * 4 * 16 * 4;               // mbarriers (8-byte aligned)
+  static constexpr int kNumBars = 2 * Fmt<F>::kStages + 5;
+  static constexpr int kMisc = kBar + kNumBars * 8;                // meta[kStages], tmem addr, abort
   static constexpr int kTotal = kMisc + 64;
-  static constexpr int kAlloc = kTotal + 1024;                    // slack for 1024-B alignment
+  static constexpr int kAlloc = kTotal + 1024;                     // slack for 1024-B alignment
+  static_assert(kAlloc <= kSmemLimit, "shared memory budget");
+  static_assert(kStage % 16 == 0 && kStageBytes % 16 == 0, "bulk copy alignment");
 };
 
 struct AttnParams {
@@ -195,20 +222,8 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t v) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
-// Operand chunk (8 values = 16 bytes) of block b (0..8), chunk c (0..7) of one cache entry.
-template <int F>
-__device__ __forceinline__ uint4 entry_chunk(const uint8_t* rec, int b, int c) {
-  if (F == kBF16) {
-    return *reinterpret_cast<const uint4*>(rec + 128 * b + 16 * c);
-  } else if (F == kFP8) {
-    return e4m3x8_to_f16x8(*reinterpret_cast<const uint2*>(rec + 64 * b + 8 * c));
-  } else {
-    if (b < 8) return e4m3x8_to_f16x8(*reinterpret_cast<const uint2*>(rec + 64 * b + 8 * c));
-    return *reinterpret_cast<const uint4*>(rec + 528 + 16 * c);
-  }
-}
-
-// Query chunk in the operand type the tile uses for that block.
+// Query chunk (8 values = 16 bytes) of block b (0..8), chunk c (0..7), in the operand type
+// the key tile uses for that block: f16 for the e4m3-sourced blocks, bf16 otherwise.
 template <int F>
 __device__ __forceinline__ uint4 query_chunk(const uint8_t* qrow, int b, int c) {
   if (F == kFP8) {
@@ -237,10 +252,122 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool as_bf16) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// One converter thread turns 64 consecutive e4m3 bytes of its staged entry into one 64-wide
+// f16 block row of the key tile (8 swizzled 16-byte chunks); `sw` holds the row's swizzled
+// chunk offsets.
+__device__ __forceinline__ void cvt_block_e4m3(const uint8_t* src, uint8_t* dst_row, const uint32_t (&sw)[8],
+                                               bool valid) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    uint4 raw = valid ? *reinterpret_cast<const uint4*>(src + 16 * i) : make_uint4(0, 0, 0, 0);
+    uint4 lo = e4m3x8_to_f16x8(make_uint2(raw.x, raw.y));
+    uint4 hi = e4m3x8_to_f16x8(make_uint2(raw.z, raw.w));
+    *reinterpret_cast<uint4*>(dst_row + sw[2 * i]) = lo;
+    *reinterpret_cast<uint4*>(dst_row + sw[2 * i + 1]) = hi;
+  }
+}
+
+// Same for 64 16-bit values copied as they are.
+__device__ __forceinline__ void copy_block_16b(const uint8_t* src, uint8_t* dst_row, const uint32_t (&sw)[8],
+                                               bool valid) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint4 v = valid ? *reinterpret_cast<const uint4*>(src + 16 * i) : make_uint4(0, 0, 0, 0);
+    *reinterpret_cast<uint4*>(dst_row + sw[i]) = v;
+  }
+}
+
+// Converter warp cw (0..3) writes blocks 2cw and 2cw+1 of key-tile row `row` from the staged
+// entry `rec`; warp 3 also writes block 8 (d 512..575) and, for fp8_ds_mla, the tile scales.
+template <int F>
+__device__ __forceinline__ void convert_row(const uint8_t* rec, bool valid, uint8_t* kv, int row, int cw,
+                                            float* scales) {
+  uint32_t sw[8];
+#pragma unroll
+  for (int c = 0; c < 8; ++c) sw[c] = static_cast<uint32_t>(((c ^ (row & 7)) << 4));
+  uint8_t* base = kv + row * 128;
+#pragma unroll
+  for (int bb = 0; bb < 2; ++bb) {
+    const int b = 2 * cw + bb;
+    if (F == kBF16)
+      copy_block_16b(rec + 128 * b, base + b * kBlkBytes, sw, valid);
+    else
+      cvt_block_e4m3(rec + 64 * b, base + b * kBlkBytes, sw, valid);
+  }
+  if (cw == 3) {
+    if (F == kBF16)
+      copy_block_16b(rec + 1024, base + 8 * kBlkBytes, sw, valid);
+    else if (F == kFP8)
+      cvt_block_e4m3(rec + 512, base + 8 * kBlkBytes, sw, valid);
+    else
+      copy_block_16b(rec + 528, base + 8 * kBlkBytes, sw, valid);
+    if (F == kDS) {
+      float4 sc = valid ? *reinterpret_cast<const float4*>(rec + 512) : make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(scales + row * 4) = sc;
+    }
+  }
+}
+
+// Warp-wide max (or sum) of 16 per-thread values, one per head: a halving butterfly leaves
+// the result for head (lane >> 1) & 15 in every lane (16 shuffles instead of 80).
+template <bool kMax>
+__device__ __forceinline__ float butterfly16(const float (&v)[16], int lane) {
+  float a[8], b4[4], c2[2];
+  const bool u16 = lane & 16, u8 = lane & 8, u4 = lane & 4, u2 = lane & 2;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float send = u16 ? v[i] : v[i + 8];
+    const float keep = u16 ? v[i + 8] : v[i];
+    const float got = __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+    a[i] = kMax ? fmaxf(keep, got) : keep + got;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float send = u8 ? a[i] : a[i + 4];
+    const float keep = u8 ? a[i + 4] : a[i];
+    const float got = __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+    b4[i] = kMax ? fmaxf(keep, got) : keep + got;
+  }
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const float send = u4 ? b4[i] : b4[i + 2];
+    const float keep = u4 ? b4[i + 2] : b4[i];
+    const float got = __shfl_xor_sync(0xFFFFFFFFu, send, 4);
+    c2[i] = kMax ? fmaxf(keep, got) : keep + got;
+  }
+  const float send = u2 ? c2[0] : c2[1];
+  const float keep = u2 ? c2[1] : c2[0];
+  float r = keep;
+  {
+    const float got = __shfl_xor_sync(0xFFFFFFFFu, send, 2);
+    r = kMax ? fmaxf(keep, got) : keep + got;
+  }
+  const float got = __shfl_xor_sync(0xFFFFFFFFu, r, 1);
+  return kMax ? fmaxf(r, got) : r + got;
+}
+// The head whose reduction butterfly16 leaves in `lane`.
+__device__ __forceinline__ int butterfly16_head(int lane) {
+  return ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+}
+
+// ------------------------------------------------------------------------------------------
+// The kernel.  Warp roles:
+//   0      producer: per-entry 1-D bulk copies into the staging ring, L2 prefetch two tiles
+//          ahead;
+//   1      MMA issuer (one thread) and TMEM owner;
+//   2..5   softmax + epilogue: thread = TMEM lane = key row of the tile (logits) and output
+//          column d (O^T readout);
+//   6..9   converters: staged entries -> swizzled f16 / bf16 key tile, thread = entry.
+// Every wait is bounded; softmax warps vote at their named barriers so they leave together.
 template <int F, bool kSparse>
 __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_constant__ AttnParams p) {
   using FT = Fmt<F>;
   using SM = Smem<F>;
+  constexpr int NST = FT::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* kv = smem + SM::kKV;
@@ -252,24 +379,24 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
   float* red = reinterpret_cast<float*>(smem + SM::kRed);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SM::kBar);
   uint64_t* full = bars;
-  uint64_t* empty = bars + kStages;
-  uint64_t* tile_full = bars + 2 * kStages;
+  uint64_t* empty = bars + NST;
+  uint64_t* tile_full = bars + 2 * NST;
   uint64_t* s_full = tile_full + 1;
   uint64_t* p_full = tile_full + 2;
   uint64_t* o_done = tile_full + 3;
   uint64_t* mma_final = tile_full + 4;
   uint32_t* meta = reinterpret_cast<uint32_t*>(smem + SM::kMisc);
-  uint32_t* tmem_slot = meta + kStages;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(meta + kStages + 1);
+  uint32_t* tmem_slot = meta + NST;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(meta + NST + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], 4);      // one arrival per converter warp
     }
-    mbar_init(tile_full, 1);
+    mbar_init(tile_full, 4);        // one arrival per converter warp
     mbar_init(s_full, 1);
     mbar_init(p_full, 1);
     mbar_init(o_done, 1);
@@ -291,18 +418,30 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
     int st = 0;
     uint32_t eph = 0;
     uint32_t errbits = 0;
-    bool armed[kStages] = {};
-    uint32_t armed_par[kStages] = {};
+    bool armed[NST] = {};
+    uint32_t armed_par[NST] = {};
     bool ok = true;
+    auto prefetch_tile = [&](const ItemInfo& it, int t) {
+      const int nk = tile_keys(it.n, t);
+      for (int k = lane; k < nk; k += 32) {
+        uint32_t e = 0;
+        const uint8_t* src = key_entry<kSparse>(p, it, static_cast<int64_t>(t) * kTile + k, e);
+        if (src) prefetch_l2(src, FT::kRec);
+      }
+    };
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
       const ItemInfo it = decode_item<kSparse>(p, item);
       const int ntiles = static_cast<int>((it.n + kTile - 1) / kTile);
+      for (int t = 0; t < ntiles && t < 2; ++t) prefetch_tile(it, t);
       for (int t = 0; t < ntiles && ok; ++t) {
+        if (t + 2 < ntiles) prefetch_tile(it, t + 2);
         const int nk = tile_keys(it.n, t);
         const int npieces = (nk + FT::kPiece - 1) / FT::kPiece;
         for (int pc = 0; pc < npieces; ++pc) {
+          if (lane == 0) TL(0, 1);
           if (!mbar_wait(&empty[st], eph ^ 1u, abort_flag)) { ok = false; break; }
-          const int kin = pc * FT::kPiece + lane;   // key index within the tile
+          if (lane == 0) TL(0, 2);
+          const int kin = pc * FT::kPiece + lane;
           const uint8_t* src = nullptr;
           if (lane < FT::kPiece && kin < nk)
             src = key_entry<kSparse>(p, it, static_cast<int64_t>(t) * kTile + kin, errbits);
@@ -312,16 +451,16 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
             mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(__popc(mask)) * FT::kRec);
           }
           __syncwarp();
-          if (src) bulk_g2s(stage + st * SM::kStageBytes + lane * FT::kRec, src, FT::kRec, &full[st]);
+          if (src) bulk_g2s(stage + st * SM::kStageBytes + lane * FT::kRecPad, src, FT::kRec, &full[st]);
+          if (lane == 0) TL(0, 3);
           armed[st] = true;
           armed_par[st] = eph;
-          if (++st == kStages) { st = 0; eph ^= 1u; }
+          if (++st == NST) { st = 0; eph ^= 1u; }
         }
       }
     }
-    // never leave bulk copies in flight behind us
-    volatile int no_abort = 0;
-    for (int s = 0; s < kStages; ++s)
+    volatile int no_abort = 0;     // never leave bulk copies in flight behind us
+    for (int s = 0; s < NST; ++s)
       if (armed[s]) mbar_wait(&full[s], armed_par[s], &no_abort);
     errbits = __reduce_or_sync(0xFFFFFFFFu, errbits);
     if (lane == 0 && errbits) set_device_error(p.err, errbits);
@@ -338,7 +477,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
         const ItemInfo it = decode_item<kSparse>(p, item);
         const int ntiles = static_cast<int>((it.n + kTile - 1) / kTile);
         for (int t = 0; t < ntiles; ++t) {
+          TL(2, 1);
           if (!mbar_wait(tile_full, ph_t, abort_flag)) { ok = false; break; }
+          TL(2, 2);
           ph_t ^= 1u;
           tc_fence_after();
           if (F == kDS) {
@@ -363,7 +504,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
             }
           }
           mma_commit(s_full);
+          TL(2, 3);
           if (!mbar_wait(p_full, ph_p, abort_flag)) { ok = false; break; }
+          TL(2, 4);
           ph_p ^= 1u;
           tc_fence_after();
           for (int j = 0; j < 4; ++j)
@@ -373,6 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
               mma_f16_ss(tmem + kOCol + 16 * j, a, b, kIdPv, (t > 0 || kk > 0) ? 1u : 0u);
             }
           mma_commit(o_done);
+          TL(2, 5);
         }
       }
       mma_commit(mma_final);
@@ -380,16 +524,72 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
       mbar_wait(mma_final, 0, &no_abort);
     }
     __syncwarp();
+  } else if (warp >= 6) {
+    // ------------------------------------------------------------------ converters
+    const int cw = warp - 6;
+    const int ct = tid - 192;           // 0..127
+    int st = 0;
+    uint32_t sph = 0, ph_o = 0;
+    bool first = true, ok = true;
+    for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
+      const ItemInfo it = decode_item<kSparse>(p, item);
+      const int ntiles = static_cast<int>((it.n + kTile - 1) / kTile);
+      const int h0 = it.hg * kRows;
+      const int nh = min(kRows, p.H - h0);
+      for (int t = 0; t < ntiles && ok; ++t) {
+        // the key tile (and at an item start the query tile) is free once the previous PV is done
+        if (cw == 0 && lane == 0) TL(1, 1);
+        if (!first) {
+          if (!mbar_wait(o_done, ph_o, abort_flag)) { ok = false; break; }
+          ph_o ^= 1u;
+        }
+        if (cw == 0 && lane == 0) TL(1, 2);
+        first = false;
+        if (t == 0) {
+          for (int i = ct; i < kRows * 72; i += 128) {
+            const int r = i / 72, rem = i % 72, b = rem >> 3, c = rem & 7;
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (r < nh) v = query_chunk<F>(p.q + it.row * p.q_s0b + (h0 + r) * p.q_s1b, b, c);
+            *reinterpret_cast<uint4*>(qs + b * kQBlkBytes + sw128(r, c)) = v;
+          }
+        }
+        const int nk = tile_keys(it.n, t);
+        const int npieces = (nk + FT::kPiece - 1) / FT::kPiece;
+        for (int pc = 0; pc < npieces; ++pc) {
+          if (cw == 0 && lane == 0) TL(1, 3);
+          if (!mbar_wait(&full[st], sph, abort_flag)) { ok = false; break; }
+          if (cw == 0 && lane == 0) TL(1, 4);
+          const uint32_t mask = meta[st];
+          if (lane < FT::kPiece) {
+            const int row = pc * FT::kPiece + lane;
+            const bool v = (mask >> lane) & 1u;
+            convert_row<F>(stage + st * SM::kStageBytes + lane * FT::kRecPad, v, kv, row, cw, scales);
+            if (cw == 3) valid_row[row] = v ? 1 : 0;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[st]);
+          if (++st == NST) { st = 0; sph ^= 1u; }
+        }
+        if (!ok) break;
+        // rows past the last piece of a short tile
+        for (int row = npieces * FT::kPiece + lane; row < kTile; row += 32) {
+          convert_row<F>(stage, false, kv, row, cw, scales);
+          if (cw == 3) valid_row[row] = 0;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tile_full);
+        if (cw == 0 && lane == 0) TL(1, 5);
+      }
+    }
   } else {
-    // ------------------------------------------------------------------ workers
-    // Every named barrier here is a vote (bar.red.and): a failed bounded wait in any thread
-    // makes all 128 workers leave together at the next barrier, so none can hang on another.
-    const int wt = tid - 64;               // 0..127
+    // ------------------------------------------------------------------ softmax + epilogue
     const int quad = warp & 3;             // TMEM lane quadrant of this warp
     const int myrow = quad * 32 + lane;    // key row (softmax) / output column d (epilogue)
+    const int st_tid = tid - 64;           // 0..127
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    int st = 0;
-    uint32_t sph = 0, ph_s = 0, ph_o = 0;
+    const int bh = butterfly16_head(lane);
+    uint32_t ph_t = 0, ph_s = 0, ph_o = 0;
     int redbuf = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
@@ -397,61 +597,17 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
       const int ntiles = static_cast<int>((it.n + kTile - 1) / kTile);
       const int h0 = it.hg * kRows;
       const int nh = min(kRows, p.H - h0);
-      // query tile: rows = heads h0..h0+15 (zero past H)
-      for (int i = wt; i < kRows * 72; i += 128) {
-        const int r = i / 72, rem = i % 72, b = rem >> 3, c = rem & 7;
-        uint4 v = make_uint4(0, 0, 0, 0);
-        if (r < nh) v = query_chunk<F>(p.q + it.row * p.q_s0b + (h0 + r) * p.q_s1b, b, c);
-        *reinterpret_cast<uint4*>(qs + b * kQBlkBytes + sw128(r, c)) = v;
-      }
       float m_run[kRows], l_t[kRows];
 #pragma unroll
       for (int r = 0; r < kRows; ++r) { m_run[r] = -CUDART_INF_F; l_t[r] = 0.f; }
 
       for (int t = 0; t < ntiles; ++t) {
-        const int nk = tile_keys(it.n, t);
-        const int npieces = (nk + FT::kPiece - 1) / FT::kPiece;
-        for (int pc = 0; pc < npieces; ++pc) {
-          bool w = mbar_wait(&full[st], sph, abort_flag);
-          const uint32_t mask = w ? meta[st] : 0u;
-          const uint8_t* sbase = stage + st * SM::kStageBytes;
-          for (int i = wt; i < FT::kPiece * 72; i += 128) {
-            const int kk = i / 72, rem = i % 72, b = rem >> 3, c = rem & 7;
-            const int row = pc * FT::kPiece + kk;
-            const bool v = (mask >> kk) & 1u;
-            uint4 val = make_uint4(0, 0, 0, 0);
-            if (v) val = entry_chunk<F>(sbase + kk * FT::kRec, b, c);
-            *reinterpret_cast<uint4*>(kv + b * kBlkBytes + sw128(row, c)) = val;
-            if (rem == 0) valid_row[row] = v ? 1 : 0;
-          }
-          if (F == kDS && wt < FT::kPiece) {
-            const int row = pc * FT::kPiece + wt;
-            float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
-            if ((mask >> wt) & 1u) sc = *reinterpret_cast<const float4*>(sbase + wt * FT::kRec + 512);
-            *reinterpret_cast<float4*>(scales + row * 4) = sc;
-          }
-          ok = named_bar_and(1, 128, w);
-          if (!ok) break;
-          if (wt == 0) mbar_arrive(&empty[st]);
-          if (++st == kStages) { st = 0; sph ^= 1u; }
-        }
-        if (!ok) break;
-        // rows past the last piece of a short tile
-        for (int i = npieces * FT::kPiece * 72 + wt; i < kTile * 72; i += 128) {
-          const int row = i / 72, rem = i % 72, b = rem >> 3, c = rem & 7;
-          *reinterpret_cast<uint4*>(kv + b * kBlkBytes + sw128(row, c)) = make_uint4(0, 0, 0, 0);
-          if (rem == 0) {
-            valid_row[row] = 0;
-            if (F == kDS) *reinterpret_cast<float4*>(scales + row * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (wt == 0) mbar_arrive(tile_full);
-
-        // ---- logits of this thread's key (TMEM lane myrow)
-        bool w = mbar_wait(s_full, ph_s, abort_flag);
+        if (st_tid == 0) TL(3, 1);
+        bool w = mbar_wait(tile_full, ph_t, abort_flag);
+        ph_t ^= 1u;
+        w = w && mbar_wait(s_full, ph_s, abort_flag);
         ph_s ^= 1u;
+        if (st_tid == 0) TL(3, 2);
         tc_fence_after();
         float s[kRows];
         float4 sc = make_float4(1.f, 1.f, 1.f, 1.f);
@@ -481,40 +637,53 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
         // ---- tile max per head across the 128 keys
         float* rb = red + redbuf * 64;
         redbuf ^= 1;
-#pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-          float v = s[r];
-#pragma unroll
-          for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
-          if (lane == r) rb[quad * 16 + r] = v;
+        {
+          const float wm = butterfly16<true>(s, lane);
+          if ((lane & 1) == 0) rb[quad * 16 + bh] = wm;
         }
         ok = named_bar_and(1, 128, w);
         if (!ok) break;
         bool changed = false;
         float alpha[kRows], pr[kRows];
 #pragma unroll
-        for (int r = 0; r < kRows; ++r) {
-          const float tmax = fmaxf(fmaxf(rb[r], rb[16 + r]), fmaxf(rb[32 + r], rb[48 + r]));
-          const float mnew = fmaxf(m_run[r], tmax);
-          const float mu = (mnew == -CUDART_INF_F) ? 0.f : mnew;
-          alpha[r] = exp2f(m_run[r] - mu);
-          pr[r] = exp2f(s[r] - mu);
-          l_t[r] = l_t[r] * alpha[r] + pr[r];
-          changed |= (mnew != m_run[r]);
-          m_run[r] = mnew;
-        }
-        // ---- rescale O^T (PV of the previous tile has completed) when a max moved
-        if (t > 0 && changed) {
-#pragma unroll 1
-          for (int j = 0; j < 4; ++j) {
-            float o[16];
-            tmem_ld16(tl + kOCol + 16 * j, o);
-            tmem_ld_wait();
+        for (int r4 = 0; r4 < 4; ++r4) {
+          const float4 q0 = reinterpret_cast<const float4*>(rb)[r4];
+          const float4 q1 = reinterpret_cast<const float4*>(rb + 16)[r4];
+          const float4 q2 = reinterpret_cast<const float4*>(rb + 32)[r4];
+          const float4 q3 = reinterpret_cast<const float4*>(rb + 48)[r4];
+          const float tm[4] = {fmaxf(fmaxf(q0.x, q1.x), fmaxf(q2.x, q3.x)), fmaxf(fmaxf(q0.y, q1.y), fmaxf(q2.y, q3.y)),
+                               fmaxf(fmaxf(q0.z, q1.z), fmaxf(q2.z, q3.z)), fmaxf(fmaxf(q0.w, q1.w), fmaxf(q2.w, q3.w))};
 #pragma unroll
-            for (int r = 0; r < kRows; ++r) o[r] *= alpha[r];
-            tmem_st16(tl + kOCol + 16 * j, o);
+          for (int e = 0; e < 4; ++e) {
+            const int r = 4 * r4 + e;
+            const float mnew = fmaxf(m_run[r], tm[e]);
+            const float mu = (mnew == -CUDART_INF_F) ? 0.f : mnew;
+            alpha[r] = exp2f(m_run[r] - mu);
+            pr[r] = exp2f(s[r] - mu);
+            l_t[r] = l_t[r] * alpha[r] + pr[r];
+            changed |= (mnew != m_run[r]);
+            m_run[r] = mnew;
           }
-          tmem_st_wait();
+        }
+        // ---- PV of the previous tile must be complete before O^T is rescaled and P reused
+        if (st_tid == 0) TL(3, 3);
+        if (t > 0) {
+          w = mbar_wait(o_done, ph_o, abort_flag);
+          ph_o ^= 1u;
+          tc_fence_after();
+          if (st_tid == 0) TL(3, 4);
+          if (w && changed) {
+#pragma unroll 1
+            for (int j = 0; j < 4; ++j) {
+              float o[16];
+              tmem_ld16(tl + kOCol + 16 * j, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int r = 0; r < kRows; ++r) o[r] *= alpha[r];
+              tmem_st16(tl + kOCol + 16 * j, o);
+            }
+            tmem_st_wait();
+          }
         }
         // ---- P^T (MN-major, no swizzle): key row myrow, heads 0..7 | 8..15
         {
@@ -538,31 +707,31 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        named_bar_sync(1, 128);
-        if (wt == 0) mbar_arrive(p_full);
+        ok = named_bar_and(1, 128, w);
+        if (!ok) break;
+        if (st_tid == 0) mbar_arrive(p_full);
+        if (st_tid == 0) TL(3, 5);
+      }
+      if (!ok) break;
+      bool w = true;
+      if (ntiles > 0) {
         w = mbar_wait(o_done, ph_o, abort_flag);
         ph_o ^= 1u;
         tc_fence_after();
-        ok = named_bar_and(1, 128, w);
-        if (!ok) break;
       }
-      if (!ok) break;
 
       // ---- epilogue: l = sum over the 128 key lanes; O^T lane myrow = output column d
-      float* rb = red + redbuf * 64;
-      redbuf ^= 1;
-#pragma unroll
-      for (int r = 0; r < kRows; ++r) {
-        float v = l_t[r];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-        if (lane == r) rb[quad * 16 + r] = v;
+      float* rl = red + 128;
+      {
+        const float ws = butterfly16<false>(l_t, lane);
+        if ((lane & 1) == 0) rl[quad * 16 + bh] = ws;
       }
-      named_bar_sync(1, 128);
+      ok = named_bar_and(1, 128, w);
+      if (!ok) break;
       float inv[kRows], lse_r[kRows];
 #pragma unroll
       for (int r = 0; r < kRows; ++r) {
-        const float l = (rb[r] + rb[16 + r]) + (rb[32 + r] + rb[48 + r]);
+        const float l = (rl[r] + rl[16 + r]) + (rl[32 + r] + rl[48 + r]);
         const bool live = (ntiles > 0) && (l > 0.f);
         inv[r] = live ? p.out_scale / l : 0.f;
         lse_r[r] = live ? (m_run[r] + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
@@ -604,7 +773,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
         }
       }
       tc_fence_before();
-      named_bar_sync(1, 128);   // O^T reads and the reduction buffer are done before the next item
+      named_bar_sync(1, 128);   // O^T reads and the reduction buffers are done before the next item
     }
   }
 

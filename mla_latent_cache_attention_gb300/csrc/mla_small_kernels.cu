@@ -1,5 +1,5 @@
 // mla_small_kernels.cu -- the memory-bound kernels around the attention core:
-//   * the decode epilogue (q concat + latent insert), one CTA per token;
+//   * the decode epilogue (q concat + latent insert), one CTA per (token, 4 heads);
 //   * the split-K merge of partial attentions by their log-sum-exp;
 //   * gather-and-dequantise of cache entries (a test aid with the kernels' addressing).
 #include <cuda_bf16.h>
@@ -49,35 +49,48 @@ __device__ __forceinline__ int ds_tile_exponent(float amax) {
   return k < -126 ? -126 : k;
 }
 
+// Grid (B, ceil(H / 4)): CTA (b, g) builds the query rows of heads 4g..4g+3 of token b; the
+// CTAs with g == 0 also insert token b's latent.  Loads go through restrict-qualified
+// pointers in batches of 8 so that they are all in flight before the stores.
 template <int F>
-__global__ void __launch_bounds__(256) mla_epilogue_kernel(const EpiParams p) {
-  const int b = blockIdx.x, tid = threadIdx.x;
+__global__ void __launch_bounds__(128) mla_epilogue_kernel(const EpiParams p) {
+  const int b = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
   const float qinv = (F == 1) ? *p.q_scale_inv : 1.f;
   const float cinv = (F == 1) ? *p.cache_scale_inv : 1.f;
-  const float* cs = nullptr;
+  const float* __restrict__ cs = nullptr;
   if (p.positions) {
     int64_t pos = p.positions[b];
     if (pos < 0 || pos >= p.max_position) {
-      if (tid == 0) set_device_error(p.err, 8u);
+      if (tid == 0 && g == 0) set_device_error(p.err, 8u);
       pos = pos < 0 ? 0 : p.max_position - 1;
     }
     cs = p.cos_sin + pos * 64;
   }
-  // ---- query concat
   const int H = p.H;
-  for (int i = tid; i < H * 512; i += blockDim.x) {
-    const int h = i >> 9, d = i & 511;
-    const uint16_t v = p.ql_nope[b * p.ql_s0 + h * p.ql_s1 + d];
-    const int64_t o = (static_cast<int64_t>(b) * H + h) * 576 + d;
+  const int h_lo = 4 * g, h_hi = min(H, 4 * g + 4);
+  const uint16_t* __restrict__ qn = p.ql_nope;
+  const uint16_t* __restrict__ qpe = p.q_pe;
+  // ---- query concat: 64 groups of 8 NoPE values and 8 rope pairs per head
+  for (int i = tid; i < (h_hi - h_lo) * 64; i += blockDim.x) {
+    const int h = h_lo + (i >> 6), d0 = (i & 63) * 8;
+    const uint16_t* src = qn + b * p.ql_s0 + h * p.ql_s1 + d0;
+    uint16_t v[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] = __ldg(src + e);
+    const int64_t o = (static_cast<int64_t>(b) * H + h) * 576 + d0;
     if (F == 1) {
-      reinterpret_cast<uint8_t*>(p.mqa_q)[o] = e4m3_sat(__uint_as_float(static_cast<uint32_t>(v) << 16) * qinv);
+      uint8_t* __restrict__ q8 = reinterpret_cast<uint8_t*>(p.mqa_q) + o;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) q8[e] = e4m3_sat(__uint_as_float(static_cast<uint32_t>(v[e]) << 16) * qinv);
     } else {
-      reinterpret_cast<uint16_t*>(p.mqa_q)[o] = v;
+      uint16_t* __restrict__ q16 = reinterpret_cast<uint16_t*>(p.mqa_q) + o;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) q16[e] = v[e];
     }
   }
-  for (int i = tid; i < H * 32; i += blockDim.x) {
-    const int h = i >> 5, pr = i & 31;
-    const uint16_t* src = p.q_pe + b * p.qp_s0 + h * p.qp_s1 + 2 * pr;
+  for (int i = tid; i < (h_hi - h_lo) * 32; i += blockDim.x) {
+    const int h = h_lo + (i >> 5), pr = i & 31;
+    const uint16_t* src = qpe + b * p.qp_s0 + h * p.qp_s1 + 2 * pr;
     float y0 = bf16_at(src), y1 = bf16_at(src + 1);
     if (cs) rope_pair(y0, y1, cs[pr], cs[32 + pr], y0, y1);
     const int64_t o = (static_cast<int64_t>(b) * H + h) * 576 + 512 + 2 * pr;
@@ -91,6 +104,7 @@ __global__ void __launch_bounds__(256) mla_epilogue_kernel(const EpiParams p) {
       q16[o + 1] = bf16_bits(y1);
     }
   }
+  if (g != 0) return;
   // ---- latent insert
   const int64_t slot = p.slot_mapping[b];
   if (slot < 0) return;
@@ -100,8 +114,8 @@ __global__ void __launch_bounds__(256) mla_epilogue_kernel(const EpiParams p) {
     return;
   }
   uint8_t* ent = p.cache + blk * p.block_stride + (slot % p.block_size) * p.entry_stride;
-  const uint16_t* kc = p.kv_c + b * p.kv_s0;
-  const uint16_t* kr = p.k_pe + b * p.kp_s0;
+  const uint16_t* __restrict__ kc = p.kv_c + b * p.kv_s0;
+  const uint16_t* __restrict__ kr = p.k_pe + b * p.kp_s0;
   if (tid < 32) {   // rope part, one pair per lane
     float y0 = bf16_at(kr + 2 * tid), y1 = bf16_at(kr + 2 * tid + 1);
     if (cs) rope_pair(y0, y1, cs[tid], cs[32 + tid], y0, y1);
@@ -116,31 +130,30 @@ __global__ void __launch_bounds__(256) mla_epilogue_kernel(const EpiParams p) {
       reinterpret_cast<uint16_t*>(ent + 528)[2 * tid + 1] = bf16_bits(y1);
     }
   }
+  // NoPE part: warp w owns the 128-wide tile w, 4 values per lane
+  const int w = tid >> 5, lane = tid & 31;
+  float x[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) x[i] = bf16_at(kc + 128 * w + 4 * lane + i);
   if (F == 0) {
-    for (int d = tid; d < 512; d += blockDim.x) reinterpret_cast<uint16_t*>(ent)[d] = kc[d];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) reinterpret_cast<uint16_t*>(ent)[128 * w + 4 * lane + i] = kc[128 * w + 4 * lane + i];
   } else if (F == 1) {
-    for (int d = tid; d < 512; d += blockDim.x) ent[d] = e4m3_sat(bf16_at(kc + d) * cinv);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ent[128 * w + 4 * lane + i] = e4m3_sat(x[i] * cinv);
   } else {
-    // warps 0..3: one 128-wide tile each, 4 values per lane
-    const int w = tid >> 5, lane = tid & 31;
-    if (w < 4) {
-      float x[4];
-      float amax = 0.f;
+    float amax = 0.f;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        x[i] = bf16_at(kc + 128 * w + 4 * lane + i);
-        amax = fmaxf(amax, fabsf(x[i]));
-      }
+    for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(x[i]));
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-      const int k = ds_tile_exponent(amax);
-      const float inv = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);   // 2^-k, exact
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const int k = ds_tile_exponent(amax);
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);   // 2^-k, exact
 #pragma unroll
-      for (int i = 0; i < 4; ++i) ent[128 * w + 4 * lane + i] = e4m3_sat(x[i] * inv);
-      if (lane == 0) {
-        const float s = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
-        *reinterpret_cast<float*>(ent + 512 + 4 * w) = s;
-      }
+    for (int i = 0; i < 4; ++i) ent[128 * w + 4 * lane + i] = e4m3_sat(x[i] * inv);
+    if (lane == 0) {
+      const float s = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+      *reinterpret_cast<float*>(ent + 512 + 4 * w) = s;
     }
   }
 }
@@ -218,12 +231,13 @@ __global__ void mla_gather_kernel(const GatherParams p) {
 
 // ------------------------------------------------------------------------------------------
 cudaError_t launch_epilogue(int fmt, const EpiParams& p, int B, cudaStream_t stream) {
+  const dim3 grid(B, (p.H + 3) / 4);
   if (fmt == 0)
-    mla_epilogue_kernel<0><<<B, 256, 0, stream>>>(p);
+    mla_epilogue_kernel<0><<<grid, 128, 0, stream>>>(p);
   else if (fmt == 1)
-    mla_epilogue_kernel<1><<<B, 256, 0, stream>>>(p);
+    mla_epilogue_kernel<1><<<grid, 128, 0, stream>>>(p);
   else
-    mla_epilogue_kernel<2><<<B, 256, 0, stream>>>(p);
+    mla_epilogue_kernel<2><<<grid, 128, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
