@@ -1,6 +1,8 @@
 // mla_api.cu -- the C ABI declared in include/mla.h: argument checks, split-K planning,
 // workspace carving and kernel launches.  Host code only; every step of the computation
 // runs in the library's kernels.
+#include <cuda.h>
+
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -102,6 +104,74 @@ size_t workspace_bytes_for(int64_t n_rows, int H, const SplitPlan& sp) {
 
 int grid_for(int64_t items, int sms) {
   return static_cast<int>(items < sms ? items : sms);
+}
+
+// ---- tensor maps for the TMA page kernel (encoded through the runtime's driver entry point,
+// cached per (cache pointer, geometry); a map is only host memory passed by value)
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct TmapEntry {
+  const void* base = nullptr;
+  int64_t nb = 0, bstride = 0, estride = 0;
+  int bs = 0, fmt = -1, rows = 0;
+  CUtensorMap map;
+};
+TmapEntry g_tmaps[8];
+int g_tmap_next = 0;
+std::mutex g_tmap_mu;
+
+// Rows per TMA box for a block size, or 0 when the page kernel does not serve it: the box
+// rows must divide the 128-key tile (block_size 16..128 a power of two) or be a whole
+// 128-row slice of a larger block.
+int tma_rows_for(int block_size) {
+  if (block_size >= 128) return (block_size % 128 == 0) ? 128 : 0;
+  if (block_size >= 16 && (128 % block_size) == 0) return block_size;
+  return 0;
+}
+
+int tmap_for(const void* base, int fmt, int64_t nb, int64_t bstride, int64_t estride, int bs, int rows,
+             CUtensorMap* out) {
+  std::lock_guard<std::mutex> lk(g_tmap_mu);
+  for (auto& e : g_tmaps)
+    if (e.base == base && e.fmt == fmt && e.nb == nb && e.bstride == bstride && e.estride == estride && e.bs == bs &&
+        e.rows == rows) {
+      *out = e.map;
+      return MLA_OK;
+    }
+  static EncodeTiledFn enc = nullptr;
+  if (!enc) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    enc = reinterpret_cast<EncodeTiledFn>(fn);
+  }
+  TmapEntry& e = g_tmaps[g_tmap_next];
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(entry_bytes(static_cast<mla_cache_format>(fmt))),
+                              static_cast<cuuint64_t>(bs), static_cast<cuuint64_t>(nb)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(estride), static_cast<cuuint64_t>(bstride)};
+  const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(rows), 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = enc(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    e.base = nullptr;
+    return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  }
+  e.base = base;
+  e.fmt = fmt;
+  e.nb = nb;
+  e.bstride = bstride;
+  e.estride = estride;
+  e.bs = bs;
+  e.rows = rows;
+  g_tmap_next = (g_tmap_next + 1) % 8;
+  *out = e.map;
+  return MLA_OK;
 }
 
 }  // namespace
@@ -347,9 +417,20 @@ extern "C" int mla_paged_decode(const void* q, int64_t q_s0, int64_t q_s1, const
   }
   p.err = d->err;
   const int grid = grid_for(items, d->sms);
+  // bf16 caches whose blocks tile the 128-key tile go through the TMA page kernel
+  const int tma_rows = (fmt == MLA_CACHE_BF16) ? tma_rows_for(block_size) : 0;
+  CUtensorMap tmap;
+  if (tma_rows) {
+    if (int rc = tmap_for(kv_cache, fmt, num_blocks, block_stride_bytes, entry_stride_bytes, block_size, tma_rows,
+                          &tmap))
+      return rc;
+    p.tma_rows = tma_rows;
+  }
   cudaError_t e;
   prof_begin(stream);
-  if (fmt == MLA_CACHE_BF16)
+  if (tma_rows)
+    e = launch_attn_tma_bf16(p, &tmap, grid, stream);
+  else if (fmt == MLA_CACHE_BF16)
     e = launch_attn_paged_bf16(p, grid, stream);
   else if (fmt == MLA_CACHE_FP8)
     e = launch_attn_paged_fp8(p, grid, stream);

@@ -78,7 +78,7 @@ template <> struct Fmt<kBF16> {
   static constexpr int kRec = 1152, kRecPad = 1168, kPiece = 16, kStages = 3, kNP = 1;
 };
 template <> struct Fmt<kFP8> {
-  static constexpr int kRec = 576, kRecPad = 592, kPiece = 32, kStages = 3, kNP = 1;
+  static constexpr int kRec = 576, kRecPad = 592, kPiece = 32, kStages = 2, kNP = 1;
 };
 template <> struct Fmt<kDS> {
   static constexpr int kRec = 656, kRecPad = 656, kPiece = 32, kStages = 2, kNP = 4;
@@ -93,7 +93,8 @@ template <int F> struct Smem {
   static constexpr int kScale = kStage + Fmt<F>::kStages * kStageBytes;   // [128][4] fp32
   static constexpr int kValid = kScale + kTile * 16;               // [128] u8
   static constexpr int kRed = kValid + kTile;                      // [2][4][16] + [4][16] fp32
-  static constexpr int kBar = kRed + 3 * 4 * 16 * 4;               // mbarriers (8-byte aligned)
+  static constexpr int kAddr = kRed + 3 * 4 * 16 * 4;              // [2][128] entry addresses
+  static constexpr int kBar = kAddr + 2 * kTile * 8;               // mbarriers (8-byte aligned)
   static constexpr int kNumBars = 2 * Fmt<F>::kStages + 5;
   static constexpr int kMisc = kBar + kNumBars * 8;                // meta[kStages], tmem addr, abort
   static constexpr int kTotal = kMisc + 64;
@@ -123,6 +124,7 @@ struct AttnParams {
   int q_len;
   int64_t chunk;          // keys per split (multiple of kTile)
   int n_splits;
+  int tma_rows;           // TMA page kernel: rows per box (divides 128)
   // items
   int n_rows, n_items;
   // scales
@@ -252,20 +254,25 @@ __device__ __forceinline__ uint32_t pack2(float a, float b, bool as_bf16) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
+// L2 prefetch of an entry, one instruction per 128-byte line (the bulk-copy engine is kept
+// for the copies themselves).
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+  const uint8_t* c = static_cast<const uint8_t*>(p);
+  for (uint32_t off = 0; off < bytes; off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(c + off));
 }
 
 // One converter thread turns 64 consecutive e4m3 bytes of its staged entry into one 64-wide
 // f16 block row of the key tile (8 swizzled 16-byte chunks); `sw` holds the row's swizzled
-// chunk offsets.
+// chunk offsets.  All loads are issued before any store.
 __device__ __forceinline__ void cvt_block_e4m3(const uint8_t* src, uint8_t* dst_row, const uint32_t (&sw)[8],
                                                bool valid) {
+  uint4 raw[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) raw[i] = valid ? *reinterpret_cast<const uint4*>(src + 16 * i) : make_uint4(0, 0, 0, 0);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    uint4 raw = valid ? *reinterpret_cast<const uint4*>(src + 16 * i) : make_uint4(0, 0, 0, 0);
-    uint4 lo = e4m3x8_to_f16x8(make_uint2(raw.x, raw.y));
-    uint4 hi = e4m3x8_to_f16x8(make_uint2(raw.z, raw.w));
+    const uint4 lo = e4m3x8_to_f16x8(make_uint2(raw[i].x, raw[i].y));
+    const uint4 hi = e4m3x8_to_f16x8(make_uint2(raw[i].z, raw[i].w));
     *reinterpret_cast<uint4*>(dst_row + sw[2 * i]) = lo;
     *reinterpret_cast<uint4*>(dst_row + sw[2 * i + 1]) = hi;
   }
@@ -274,11 +281,11 @@ __device__ __forceinline__ void cvt_block_e4m3(const uint8_t* src, uint8_t* dst_
 // Same for 64 16-bit values copied as they are.
 __device__ __forceinline__ void copy_block_16b(const uint8_t* src, uint8_t* dst_row, const uint32_t (&sw)[8],
                                                bool valid) {
+  uint4 v[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    uint4 v = valid ? *reinterpret_cast<const uint4*>(src + 16 * i) : make_uint4(0, 0, 0, 0);
-    *reinterpret_cast<uint4*>(dst_row + sw[i]) = v;
-  }
+  for (int i = 0; i < 8; ++i) v[i] = valid ? *reinterpret_cast<const uint4*>(src + 16 * i) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) *reinterpret_cast<uint4*>(dst_row + sw[i]) = v[i];
 }
 
 // Converter warp cw (0..3) writes blocks 2cw and 2cw+1 of key-tile row `row` from the staged
@@ -356,8 +363,8 @@ __device__ __forceinline__ int butterfly16_head(int lane) {
 
 // ------------------------------------------------------------------------------------------
 // The kernel.  Warp roles:
-//   0      producer: per-entry 1-D bulk copies into the staging ring, L2 prefetch two tiles
-//          ahead;
+//   0      producer: per-entry 1-D bulk copies into the staging ring; entry addresses and an L2
+//          prefetch one tile ahead;
 //   1      MMA issuer (one thread) and TMEM owner;
 //   2..5   softmax + epilogue: thread = TMEM lane = key row of the tile (logits) and output
 //          column d (O^T readout);
@@ -415,49 +422,88 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
+    // Entry addresses of a tile are resolved one tile ahead (four independent index / block-
+    // table loads per lane, in flight while the current tile's copies are issued) into a
+    // two-slot ring in shared memory, and prefetched into L2 from there.
+    const uint8_t** addr_ring = reinterpret_cast<const uint8_t**>(smem + SM::kAddr);
     int st = 0;
     uint32_t eph = 0;
     uint32_t errbits = 0;
     bool armed[NST] = {};
     uint32_t armed_par[NST] = {};
     bool ok = true;
-    auto prefetch_tile = [&](const ItemInfo& it, int t) {
-      const int nk = tile_keys(it.n, t);
-      for (int k = lane; k < nk; k += 32) {
-        uint32_t e = 0;
-        const uint8_t* src = key_entry<kSparse>(p, it, static_cast<int64_t>(t) * kTile + k, e);
-        if (src) prefetch_l2(src, FT::kRec);
+    struct Cursor {
+      int item, t, ntiles;
+      ItemInfo it;
+    };
+    auto first_from = [&](int item) {
+      Cursor c{item, 0, 0, ItemInfo{}};
+      for (; c.item < p.n_items; c.item += gridDim.x) {
+        c.it = decode_item<kSparse>(p, c.item);
+        c.ntiles = static_cast<int>((c.it.n + kTile - 1) / kTile);
+        if (c.ntiles > 0) return c;
+      }
+      return c;
+    };
+    auto advance = [&](const Cursor& c) {
+      if (c.t + 1 < c.ntiles) {
+        Cursor n = c;
+        n.t += 1;
+        return n;
+      }
+      return first_from(c.item + gridDim.x);
+    };
+    auto tile_addrs = [&](const Cursor& c, const uint8_t* (&a)[4]) {
+      const int nk = tile_keys(c.it.n, c.t);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int k = lane + 32 * i;
+        a[i] = (k < nk) ? key_entry<kSparse>(p, c.it, static_cast<int64_t>(c.t) * kTile + k, errbits) : nullptr;
       }
     };
-    for (int item = blockIdx.x; item < p.n_items && ok; item += gridDim.x) {
-      const ItemInfo it = decode_item<kSparse>(p, item);
-      const int ntiles = static_cast<int>((it.n + kTile - 1) / kTile);
-      for (int t = 0; t < ntiles && t < 2; ++t) prefetch_tile(it, t);
-      for (int t = 0; t < ntiles && ok; ++t) {
-        if (t + 2 < ntiles) prefetch_tile(it, t + 2);
-        const int nk = tile_keys(it.n, t);
-        const int npieces = (nk + FT::kPiece - 1) / FT::kPiece;
-        for (int pc = 0; pc < npieces; ++pc) {
-          if (lane == 0) TL(0, 1);
-          if (!mbar_wait(&empty[st], eph ^ 1u, abort_flag)) { ok = false; break; }
-          if (lane == 0) TL(0, 2);
-          const int kin = pc * FT::kPiece + lane;
-          const uint8_t* src = nullptr;
-          if (lane < FT::kPiece && kin < nk)
-            src = key_entry<kSparse>(p, it, static_cast<int64_t>(t) * kTile + kin, errbits);
-          const uint32_t mask = __ballot_sync(0xFFFFFFFFu, src != nullptr);
-          if (lane == 0) {
-            meta[st] = mask;
-            mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(__popc(mask)) * FT::kRec);
-          }
-          __syncwarp();
-          if (src) bulk_g2s(stage + st * SM::kStageBytes + lane * FT::kRecPad, src, FT::kRec, &full[st]);
-          if (lane == 0) TL(0, 3);
-          armed[st] = true;
-          armed_par[st] = eph;
-          if (++st == NST) { st = 0; eph ^= 1u; }
-        }
+    auto publish = [&](const uint8_t* (&a)[4], int slot_) {
+      const uint8_t** ring = addr_ring + slot_ * kTile;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        ring[lane + 32 * i] = a[i];
+        if (a[i]) prefetch_l2(a[i], FT::kRec);
       }
+    };
+    Cursor cur = first_from(blockIdx.x);
+    int slot = 0;
+    if (cur.item < p.n_items) {
+      const uint8_t* a[4];
+      tile_addrs(cur, a);
+      publish(a, 0);
+      __syncwarp();
+    }
+    while (ok && cur.item < p.n_items) {
+      const Cursor nxt = advance(cur);
+      const uint8_t* an[4] = {nullptr, nullptr, nullptr, nullptr};
+      if (nxt.item < p.n_items) tile_addrs(nxt, an);
+      const int nk = tile_keys(cur.it.n, cur.t);
+      const int npieces = (nk + FT::kPiece - 1) / FT::kPiece;
+      const uint8_t* const* ring = addr_ring + slot * kTile;
+      for (int pc = 0; pc < npieces; ++pc) {
+        if (!mbar_wait(&empty[st], eph ^ 1u, abort_flag)) { ok = false; break; }
+        const int kin = pc * FT::kPiece + lane;
+        const uint8_t* src = (lane < FT::kPiece && kin < nk) ? ring[kin] : nullptr;
+        const uint32_t mask = __ballot_sync(0xFFFFFFFFu, src != nullptr);
+        if (lane == 0) {
+          meta[st] = mask;
+          mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(__popc(mask)) * FT::kRec);
+        }
+        __syncwarp();
+        if (src) bulk_g2s(stage + st * SM::kStageBytes + lane * FT::kRecPad, src, FT::kRec, &full[st]);
+        armed[st] = true;
+        armed_par[st] = eph;
+        if (++st == NST) { st = 0; eph ^= 1u; }
+      }
+      if (!ok) break;
+      slot ^= 1;
+      if (nxt.item < p.n_items) publish(an, slot);
+      __syncwarp();
+      cur = nxt;
     }
     volatile int no_abort = 0;     // never leave bulk copies in flight behind us
     for (int s = 0; s < NST; ++s)
@@ -468,6 +514,12 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t kv_a = smem_u32(kv), q_a = smem_u32(qs), p_a = smem_u32(ps);
+      // descriptors differ only in their start-address field (16-byte units; shared addresses
+      // stay below 256 KB, so adding to the 14-bit field never carries out of it)
+      const uint64_t dK = smem_desc(kv_a, 16, 1024, kSwizzle128B);
+      const uint64_t dQ = smem_desc(q_a, 16, 1024, kSwizzle128B);
+      const uint64_t dV = smem_desc(kv_a, kBlkBytes, 1024, kSwizzle128B);
+      const uint64_t dP = smem_desc(p_a, 256, 128, kSwizzleNone);
       constexpr uint32_t kIdQkNope = idesc_f16(128, kRows, F == kBF16, F == kBF16, 0, 0);
       constexpr uint32_t kIdQkRope = idesc_f16(128, kRows, 1, 1, 0, 0);
       constexpr uint32_t kIdPv = idesc_f16(128, kRows, F == kBF16, F == kBF16, 1, 1);
@@ -487,20 +539,19 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
               for (int kk = 0; kk < 8; ++kk) {
                 const int b = 2 * j + (kk >> 2);
                 const uint32_t ko = (kk & 3) * 32;
-                mma_f16_ss(tmem + 16 * j, smem_desc(kv_a + b * kBlkBytes + ko, 16, 1024, kSwizzle128B),
-                           smem_desc(q_a + b * kQBlkBytes + ko, 16, 1024, kSwizzle128B), kIdQkNope, kk > 0);
+                mma_f16_ss(tmem + 16 * j, dK + ((b * kBlkBytes + ko) >> 4), dQ + ((b * kQBlkBytes + ko) >> 4),
+                           kIdQkNope, kk > 0);
               }
             for (int kk = 0; kk < 4; ++kk) {
               const uint32_t ko = kk * 32;
-              mma_f16_ss(tmem + 64, smem_desc(kv_a + 8 * kBlkBytes + ko, 16, 1024, kSwizzle128B),
-                         smem_desc(q_a + 8 * kQBlkBytes + ko, 16, 1024, kSwizzle128B), kIdQkRope, kk > 0);
+              mma_f16_ss(tmem + 64, dK + ((8 * kBlkBytes + ko) >> 4), dQ + ((8 * kQBlkBytes + ko) >> 4), kIdQkRope,
+                         kk > 0);
             }
           } else {
             for (int ks = 0; ks < 36; ++ks) {
               const int b = ks >> 2;
               const uint32_t ko = (ks & 3) * 32;
-              mma_f16_ss(tmem, smem_desc(kv_a + b * kBlkBytes + ko, 16, 1024, kSwizzle128B),
-                         smem_desc(q_a + b * kQBlkBytes + ko, 16, 1024, kSwizzle128B), kIdQkNope, ks > 0);
+              mma_f16_ss(tmem, dK + ((b * kBlkBytes + ko) >> 4), dQ + ((b * kQBlkBytes + ko) >> 4), kIdQkNope, ks > 0);
             }
           }
           mma_commit(s_full);
@@ -511,8 +562,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
           tc_fence_after();
           for (int j = 0; j < 4; ++j)
             for (int kk = 0; kk < 8; ++kk) {
-              const uint64_t a = smem_desc(kv_a + 2 * j * kBlkBytes + kk * 2048, kBlkBytes, 1024, kSwizzle128B);
-              const uint64_t b = smem_desc(p_a + (F == kDS ? j * 4096 : 0) + kk * 512, 256, 128, kSwizzleNone);
+              const uint64_t a = dV + ((2 * j * kBlkBytes + kk * 2048) >> 4);
+              const uint64_t b = dP + (((F == kDS ? j * 4096 : 0) + kk * 512) >> 4);
               mma_f16_ss(tmem + kOCol + 16 * j, a, b, kIdPv, (t > 0 || kk > 0) ? 1u : 0u);
             }
           mma_commit(o_done);

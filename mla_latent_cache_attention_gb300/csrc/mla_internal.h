@@ -63,5 +63,8 @@ cudaError_t launch_attn_sparse_ds(const AttnParams& p, int grid, cudaStream_t st
 cudaError_t launch_attn_paged_bf16(const AttnParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_attn_paged_fp8(const AttnParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_attn_paged_ds(const AttnParams& p, int grid, cudaStream_t stream);
+// Paged bf16 decode with TMA page loads; `tmap` points to a CUtensorMap (3-D, uint8,
+// [num_blocks][block_size][1152 B], 128-byte swizzle, box 128 B x tma_rows x 1).
+cudaError_t launch_attn_tma_bf16(const AttnParams& p, const void* tmap, int grid, cudaStream_t stream);
 
 }  // namespace mla
