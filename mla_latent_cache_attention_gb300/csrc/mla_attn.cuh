@@ -40,24 +40,25 @@ enum : int { kBF16 = 0, kFP8 = 1, kDS = 2 };
 
 #ifdef MLA_TIMELINE
 // Debug timeline (never in the product build): per CTA (first 4) and role, a log of
-// (event id, %globaltimer) pairs.
+// (event id, %globaltimer) pairs.  Store-only: the marking thread counts in a register.
 constexpr int kTlCtas = 4, kTlRoles = 4, kTlEvents = 512;
 __device__ unsigned long long g_tl[kTlCtas][kTlRoles][kTlEvents][2];
 __device__ int g_tl_n[kTlCtas][kTlRoles];
-__device__ __forceinline__ void tl_mark(int role, int ev) {
-  if (blockIdx.x < kTlCtas) {
-    int& n = g_tl_n[blockIdx.x][role];
-    if (n < kTlEvents) {
-      g_tl[blockIdx.x][role][n][0] = ev;
-      g_tl[blockIdx.x][role][n][1] = globaltimer();
-      ++n;
-    }
+__device__ __forceinline__ void tl_mark(int role, int ev, int& n) {
+  if (blockIdx.x < kTlCtas && n < kTlEvents) {
+    g_tl[blockIdx.x][role][n][0] = ev;
+    g_tl[blockIdx.x][role][n][1] = globaltimer();
+    ++n;
+    g_tl_n[blockIdx.x][role] = n;
   }
 }
-#define TL(role, ev) tl_mark(role, ev)
+#define TL(role, ev) tl_mark(role, ev, tl_n)
+#define TL_DECL int tl_n = 0
 #else
 #define TL(role, ev) ((void)0)
+#define TL_DECL ((void)0)
 #endif
+
 
 constexpr int kTile = 128;               // keys per tile (MMA M, TMEM lanes)
 constexpr int kRows = 16;                // heads per CTA (MMA N)
@@ -397,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
   volatile int* abort_flag = reinterpret_cast<volatile int*>(meta + NST + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  TL_DECL;
 
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {

@@ -119,6 +119,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int BR = p.tma_rows;
   const int NPG = kTile / BR;      // pages per tile (BR divides 128)
+  TL_DECL;
 
   if (tid == 0) {
     for (int g = 0; g < 5; ++g) mbar_init(&kv_full[g], 1);
@@ -162,6 +163,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         tmeta[2 * (g & 1) + 1] = static_cast<uint32_t>(tile_keys(cur.it.n, cur.t));
       }
       // groups in the order their buffers free up: block 8 (after QK), then pairs 0..3 (after PV j)
+      if (lane == 0) TL(0, 1);
       for (int gi = 0; gi < 5 && ok; ++gi) {
         const int grp = (gi == 0) ? 4 : gi - 1;
         if (g > 0) {
@@ -190,6 +192,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         }
         armed = true;
         armed_par = static_cast<uint32_t>(g & 1);
+        if (lane == 0) TL(0, 10 + grp);
       }
       if (!ok) break;
       // L2 prefetch of the next tile
@@ -228,9 +231,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         if (!mbar_wait(q_full, ph_q, abort_flag)) { ok = false; break; }
         ph_q ^= 1u;
         for (int t = 0; t < ntiles && ok; ++t) {
+          TL(2, 1);
 #pragma unroll
           for (int grp = 0; grp < 5; ++grp) {
             if (!mbar_wait(&kv_full[grp], ph_kv, abort_flag)) { ok = false; break; }
+            TL(2, 10 + grp);
             tc_fence_after();
             const int b0 = (grp == 4) ? 8 : 2 * grp;
             const int nks = (grp == 4) ? 4 : 8;
@@ -245,7 +250,9 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           if (!ok) break;
           ph_kv ^= 1u;
           mma_commit(s_full);
+          TL(2, 2);
           if (!mbar_wait(p_full, ph_p, abort_flag)) { ok = false; break; }
+          TL(2, 3);
           ph_p ^= 1u;
           tc_fence_after();
 #pragma unroll
@@ -258,6 +265,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             }
             mma_commit(&pair_free[j]);
           }
+          TL(2, 4);
         }
       }
       mma_commit(mma_final);
@@ -302,6 +310,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         w = w && mbar_wait(s_full, ph_s, abort_flag);
         ph_s ^= 1u;
         tc_fence_after();
+        if (st_tid == 0) TL(3, 1);
         const uint32_t pmask = tmeta[2 * (g & 1)];
         const int nk = static_cast<int>(tmeta[2 * (g & 1) + 1]);
         const bool valid = (myrow < nk) && ((pmask >> (myrow / BR)) & 1u);
@@ -351,6 +360,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
             m_run[r] = mnew;
           }
         }
+        if (st_tid == 0) TL(3, 2);
         if (t > 0) {
           w = mbar_wait(&pair_free[3], ph_o, abort_flag);    // PV of the previous tile complete
           ph_o ^= 1u;
@@ -387,9 +397,11 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
         ok = named_bar_and(1, 128, w);
         if (!ok) break;
         if (st_tid == 0) mbar_arrive(p_full);
+        if (st_tid == 0) TL(3, 3);
       }
       if (!ok) break;
       bool w = true;
+      if (st_tid == 0) TL(3, 5);
       if (ntiles > 0) {
         w = mbar_wait(&pair_free[3], ph_o, abort_flag);
         ph_o ^= 1u;
@@ -446,6 +458,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1)
           p.part_lse[(static_cast<int64_t>(it.split) * p.n_rows + it.row) * p.H + h0 + myrow] = lv;
         }
       }
+      if (st_tid == 0) TL(3, 6);
       tc_fence_before();
       named_bar_sync(1, 128);
     }
