@@ -11,6 +11,7 @@
 #include "mla.h"
 #include "mla_attn.cuh"
 #include "mla_internal.h"
+#include "mla_paged_tma.cuh"
 
 namespace mla {
 namespace {
@@ -79,15 +80,15 @@ struct SplitPlan {
   int64_t chunk;
 };
 
-// Split-K plan of the paged decode.  The split count depends on the number of (row, head
-// group) units, max_context and the SM count only -- never on seq_lens -- as the pages'
-// decode core fixes its split count from the deployment's longest sequence.  Aim for about
-// eight work items per SM, with at least 8 key tiles (1024 keys) per split.
-SplitPlan plan_splits(int64_t n_rows, int n_hgroups, int max_context, int sms) {
+// Split-K plan of the paged decode.  The split count depends on the number of (request,
+// column group) units, max_context and the SM count only -- never on seq_lens -- as the
+// pages' decode core fixes its split count from the deployment's longest sequence.  Aim for
+// about eight work items per SM, with at least 4 key tiles (512 keys) per split; the kernels
+// hand items out longest first, which evens out the tail.
+SplitPlan plan_splits(int64_t units, int max_context, int sms) {
   const int64_t max_tiles = max_context > 0 ? (max_context + kTile - 1) / kTile : 1;
-  const int64_t base = n_rows * n_hgroups;
-  int64_t splits = base > 0 ? (8LL * sms + base - 1) / base : 1;
-  const int64_t cap = max_tiles / 8 > 1 ? max_tiles / 8 : 1;
+  int64_t splits = units > 0 ? (8LL * sms + units - 1) / units : 1;
+  const int64_t cap = max_tiles / 4 > 1 ? max_tiles / 4 : 1;
   if (splits > cap) splits = cap;
   if (splits < 1) splits = 1;
   const int64_t tiles_per = (max_tiles + splits - 1) / splits;
@@ -95,30 +96,41 @@ SplitPlan plan_splits(int64_t n_rows, int n_hgroups, int max_context, int sms) {
   return SplitPlan{static_cast<int>(splits), tiles_per * kTile};
 }
 
+// Planning units: requests x groups of up to 64 query columns.
+int64_t plan_units(int64_t B, int q_len, int H) {
+  return B * ((static_cast<int64_t>(q_len) * H + 63) / 64);
+}
+
+// Partials [S][rows][H][512] fp32, their LSEs, and one scheduler word.
 size_t workspace_bytes_for(int64_t n_rows, int H, const SplitPlan& sp) {
   if (sp.n_splits <= 1) return 0;
   const size_t po = static_cast<size_t>(sp.n_splits) * n_rows * H * kLora * sizeof(float);
   const size_t pl = static_cast<size_t>(sp.n_splits) * n_rows * H * sizeof(float);
-  return ((po + 255) & ~size_t(255)) + ((pl + 255) & ~size_t(255));
+  return ((po + 255) & ~size_t(255)) + ((pl + 255) & ~size_t(255)) + 256;
 }
 
 int grid_for(int64_t items, int sms) {
   return static_cast<int>(items < sms ? items : sms);
 }
 
-// ---- tensor maps for the TMA page kernel (encoded through the runtime's driver entry point,
-// cached per (cache pointer, geometry); a map is only host memory passed by value)
+// ---- tensor maps for the TMA page kernel (encoded through the runtime's driver entry point
+// and cached by their full description; a map is only host memory passed by value)
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+struct TmapKey {
+  const void* base;
+  uint64_t dims[3], strides[2];
+  uint32_t box[3];
+  bool operator==(const TmapKey& o) const { return memcmp(this, &o, sizeof *this) == 0; }
+};
 struct TmapEntry {
-  const void* base = nullptr;
-  int64_t nb = 0, bstride = 0, estride = 0;
-  int bs = 0, fmt = -1, rows = 0;
+  bool used = false;
+  TmapKey key;
   CUtensorMap map;
 };
-TmapEntry g_tmaps[8];
+TmapEntry g_tmaps[16];
 int g_tmap_next = 0;
 std::mutex g_tmap_mu;
 
@@ -131,12 +143,17 @@ int tma_rows_for(int block_size) {
   return 0;
 }
 
-int tmap_for(const void* base, int fmt, int64_t nb, int64_t bstride, int64_t estride, int bs, int rows,
-             CUtensorMap* out) {
+// 3-D uint8 tensor map with 128-byte swizzle: dims {x bytes, y, z}, strides {y, z} in bytes.
+int tmap_3d(const void* base, const uint64_t (&dims)[3], const uint64_t (&strides)[2], const uint32_t (&box)[3],
+            CUtensorMap* out) {
+  TmapKey key{};
+  key.base = base;
+  for (int i = 0; i < 3; ++i) key.dims[i] = dims[i], key.box[i] = box[i];
+  key.strides[0] = strides[0];
+  key.strides[1] = strides[1];
   std::lock_guard<std::mutex> lk(g_tmap_mu);
   for (auto& e : g_tmaps)
-    if (e.base == base && e.fmt == fmt && e.nb == nb && e.bstride == bstride && e.estride == estride && e.bs == bs &&
-        e.rows == rows) {
+    if (e.used && e.key == key) {
       *out = e.map;
       return MLA_OK;
     }
@@ -150,28 +167,51 @@ int tmap_for(const void* base, int fmt, int64_t nb, int64_t bstride, int64_t est
     enc = reinterpret_cast<EncodeTiledFn>(fn);
   }
   TmapEntry& e = g_tmaps[g_tmap_next];
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(entry_bytes(static_cast<mla_cache_format>(fmt))),
-                              static_cast<cuuint64_t>(bs), static_cast<cuuint64_t>(nb)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(estride), static_cast<cuuint64_t>(bstride)};
-  const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(rows), 1};
+  const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+  const cuuint64_t st[2] = {strides[0], strides[1]};
+  const cuuint32_t bx[3] = {box[0], box[1], box[2]};
   const cuuint32_t es[3] = {1, 1, 1};
-  const CUresult r = enc(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = enc(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), d, st, bx, es,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
-    e.base = nullptr;
+    e.used = false;
     return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
   }
-  e.base = base;
-  e.fmt = fmt;
-  e.nb = nb;
-  e.bstride = bstride;
-  e.estride = estride;
-  e.bs = bs;
-  e.rows = rows;
-  g_tmap_next = (g_tmap_next + 1) % 8;
+  e.used = true;
+  e.key = key;
+  g_tmap_next = (g_tmap_next + 1) % 16;
   *out = e.map;
   return MLA_OK;
+}
+
+// Column grouping of the page kernel: NQ query columns per item (16, 32 or 64; at most 32 for
+// bf16, whose 144 KB key tiles leave less room for the query), G groups per request and the
+// query box (heads x tokens) that loads one group.  Returns false when no grouping fits.
+struct ColPlan {
+  int nq, G, box_h, box_q;
+};
+bool plan_columns(int fmt, int H, int q_len, ColPlan* cp) {
+  const int nqmax = fmt == MLA_CACHE_BF16 ? 32 : 64;
+  const int cols = H * q_len;
+  if (cols <= nqmax) {
+    const int nq = cols <= 16 ? 16 : cols <= 32 ? 32 : 64;
+    if (H > 256 || q_len > 256) return false;
+    *cp = ColPlan{nq, 1, H, q_len};
+    return true;
+  }
+  for (int nq = nqmax; nq >= 16; nq /= 2) {
+    if (H % nq == 0) {
+      *cp = ColPlan{nq, cols / nq, nq, 1};
+      return true;
+    }
+    if (nq % H == 0) {
+      const int tq = nq / H;
+      *cp = ColPlan{nq, (q_len + tq - 1) / tq, H, tq};
+      return true;
+    }
+  }
+  return false;
 }
 
 }  // namespace
@@ -341,7 +381,7 @@ extern "C" size_t mla_paged_decode_workspace_size(int32_t B, int32_t q_len, int3
     sms = d->sms;
   }
   const int64_t n_rows = static_cast<int64_t>(B) * q_len;
-  const SplitPlan sp = plan_splits(n_rows, (H + kRows - 1) / kRows, max_context, sms);
+  const SplitPlan sp = plan_splits(plan_units(B, q_len, H), max_context, sms);
   return workspace_bytes_for(n_rows, H, sp);
 }
 
@@ -374,80 +414,139 @@ extern "C" int mla_paged_decode(const void* q, int64_t q_s0, int64_t q_s1, const
   if (int rc = dev_info(&d)) return rc;
   const int64_t n_rows = static_cast<int64_t>(B) * q_len;
   const int n_hgroups = (H + kRows - 1) / kRows;
-  const SplitPlan sp = plan_splits(n_rows, n_hgroups, max_context, d->sms);
+  const SplitPlan sp = plan_splits(plan_units(B, q_len, H), max_context, d->sms);
   const size_t need = workspace_bytes_for(n_rows, H, sp);
   if (need > 0) {
     if (!workspace || workspace_bytes < need)
       return fail(MLA_ERR_INVALID, "workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
     if (!aligned(workspace, 256)) return fail(MLA_ERR_INVALID, "workspace must be 256-byte aligned");
   }
-  const int64_t items = n_rows * n_hgroups * sp.n_splits;
-  if (items >= (int64_t(1) << 31)) return fail(MLA_ERR_UNSUPPORTED, "too many work items");
-  AttnParams p{};
-  const int qe = fmt == MLA_CACHE_FP8 ? 1 : 2;
-  p.q = static_cast<const uint8_t*>(q);
-  p.q_s0b = q_s0 * qe;
-  p.q_s1b = q_s1 * qe;
-  p.H = H;
-  p.n_hgroups = n_hgroups;
-  p.cache = static_cast<const uint8_t*>(kv_cache);
-  p.num_blocks = num_blocks;
-  p.block_stride = block_stride_bytes;
-  p.entry_stride = entry_stride_bytes;
-  p.block_size = block_size;
-  p.block_table = block_table;
-  p.bt_stride = bt_stride;
-  p.seq_lens = seq_lens;
-  p.q_len = q_len;
-  p.chunk = sp.chunk;
-  p.n_splits = sp.n_splits;
-  p.n_rows = static_cast<int>(n_rows);
-  p.n_items = static_cast<int>(items);
-  const float sigma = fmt == MLA_CACHE_FP8 ? softmax_scale * q_scale * k_scale : softmax_scale;
-  p.sig2 = sigma * 1.4426950408889634f;
-  p.out_scale = fmt == MLA_CACHE_FP8 ? k_scale : 1.f;
-  p.out = static_cast<uint8_t*>(out);
-  p.o_s0b = o_s0 * 2;
-  p.o_s1b = o_s1 * 2;
-  p.lse = lse;
+  float* part_o = nullptr;
+  float* part_lse = nullptr;
+  uint32_t* sched = nullptr;
   if (sp.n_splits > 1) {
     const size_t po = static_cast<size_t>(sp.n_splits) * n_rows * H * kLora * sizeof(float);
-    p.part_o = static_cast<float*>(workspace);
-    p.part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ((po + 255) & ~size_t(255)));
+    const size_t pl = static_cast<size_t>(sp.n_splits) * n_rows * H * sizeof(float);
+    part_o = static_cast<float*>(workspace);
+    part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ((po + 255) & ~size_t(255)));
+    sched = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(workspace) + ((po + 255) & ~size_t(255)) +
+                                        ((pl + 255) & ~size_t(255)));
   }
-  p.err = d->err;
-  const int grid = grid_for(items, d->sms);
-  // bf16 caches whose blocks tile the 128-key tile go through the TMA page kernel
-  const int tma_rows = (fmt == MLA_CACHE_BF16) ? tma_rows_for(block_size) : 0;
-  CUtensorMap tmap;
-  if (tma_rows) {
-    if (int rc = tmap_for(kv_cache, fmt, num_blocks, block_stride_bytes, entry_stride_bytes, block_size, tma_rows,
-                          &tmap))
-      return rc;
-    p.tma_rows = tma_rows;
-  }
+  const float sigma = fmt == MLA_CACHE_FP8 ? softmax_scale * q_scale * k_scale : softmax_scale;
+  const float out_scale = fmt == MLA_CACHE_FP8 ? k_scale : 1.f;
+  const int qe = fmt == MLA_CACHE_FP8 ? 1 : 2;
+
+  // The TMA page kernel serves bf16 and plain-fp8 caches whose blocks tile the 128-key tile,
+  // with a query whose rows and heads are 16-byte aligned.
+  const int tma_rows = (fmt != MLA_CACHE_FP8_DS_MLA) ? tma_rows_for(block_size) : 0;
+  ColPlan cp{};
+  const bool use_tma = tma_rows > 0 && plan_columns(static_cast<int>(fmt), H, q_len, &cp) && aligned(q, 16) &&
+                       (q_s0 * qe) % 16 == 0 && (q_s1 * qe) % 16 == 0 && num_blocks < (int64_t(1) << 31) &&
+                       max_context < (1 << 30);
   cudaError_t e;
-  prof_begin(stream);
-  if (tma_rows)
-    e = launch_attn_tma_bf16(p, &tmap, grid, stream);
-  else if (fmt == MLA_CACHE_BF16)
-    e = launch_attn_paged_bf16(p, grid, stream);
-  else if (fmt == MLA_CACHE_FP8)
-    e = launch_attn_paged_fp8(p, grid, stream);
-  else
-    e = launch_attn_paged_ds(p, grid, stream);
-  prof_end(stream);
+  if (use_tma) {
+    const int64_t items = static_cast<int64_t>(sp.n_splits) * B * cp.G;
+    if (items >= (int64_t(1) << 31)) return fail(MLA_ERR_UNSUPPORTED, "too many work items");
+    CUtensorMap tkv, tq;
+    const uint64_t kd[3] = {static_cast<uint64_t>(entry_bytes(fmt)), static_cast<uint64_t>(block_size),
+                            static_cast<uint64_t>(num_blocks)};
+    const uint64_t ks[2] = {static_cast<uint64_t>(entry_stride_bytes), static_cast<uint64_t>(block_stride_bytes)};
+    const uint32_t kb[3] = {128, static_cast<uint32_t>(tma_rows), 1};
+    if (int rc = tmap_3d(kv_cache, kd, ks, kb, &tkv)) return rc;
+    const uint64_t qd[3] = {static_cast<uint64_t>(576 * qe), static_cast<uint64_t>(H), static_cast<uint64_t>(n_rows)};
+    const uint64_t qs[2] = {static_cast<uint64_t>(q_s1 * qe), static_cast<uint64_t>(q_s0 * qe)};
+    const uint32_t qb[3] = {128, static_cast<uint32_t>(cp.box_h), static_cast<uint32_t>(cp.box_q)};
+    if (int rc = tmap_3d(q, qd, qs, qb, &tq)) return rc;
+    PagedParams p{};
+    p.H = H;
+    p.q_len = q_len;
+    p.B = B;
+    p.G = cp.G;
+    p.cols = H * q_len;
+    p.qbox_h = cp.box_h;
+    p.qbox_q = cp.box_q;
+    p.block_table = block_table;
+    p.bt_stride = bt_stride;
+    p.seq_lens = seq_lens;
+    p.num_blocks = static_cast<int>(num_blocks);
+    p.block_size = block_size;
+    p.BR = tma_rows;
+    p.chunk = static_cast<int>(sp.chunk);
+    p.n_splits = sp.n_splits;
+    p.n_items = static_cast<int>(items);
+    p.n_rows = static_cast<int>(n_rows);
+    p.sig2 = sigma * 1.4426950408889634f;
+    p.out_scale = out_scale;
+    p.out = static_cast<uint8_t*>(out);
+    p.o_s0b = o_s0 * 2;
+    p.o_s1b = o_s1 * 2;
+    p.lse = lse;
+    p.part_o = part_o;
+    p.part_lse = part_lse;
+    p.sched = sched;
+    p.err = d->err;
+    if (sched && cudaMemsetAsync(sched, 0, sizeof(uint32_t), stream) != cudaSuccess)
+      return fail(MLA_ERR_CUDA, "scheduler reset failed");
+    const int grid = grid_for(items, d->sms);
+    prof_begin(stream);
+    e = fmt == MLA_CACHE_BF16 ? launch_paged_tma_bf16(cp.nq, p, &tkv, &tq, grid, stream)
+                              : launch_paged_tma_fp8(cp.nq, p, &tkv, &tq, grid, stream);
+    prof_end(stream);
+  } else {
+    const int64_t items = n_rows * n_hgroups * sp.n_splits;
+    if (items >= (int64_t(1) << 31)) return fail(MLA_ERR_UNSUPPORTED, "too many work items");
+    AttnParams p{};
+    p.q = static_cast<const uint8_t*>(q);
+    p.q_s0b = q_s0 * qe;
+    p.q_s1b = q_s1 * qe;
+    p.H = H;
+    p.n_hgroups = n_hgroups;
+    p.cache = static_cast<const uint8_t*>(kv_cache);
+    p.num_blocks = num_blocks;
+    p.block_stride = block_stride_bytes;
+    p.entry_stride = entry_stride_bytes;
+    p.block_size = block_size;
+    p.block_table = block_table;
+    p.bt_stride = bt_stride;
+    p.seq_lens = seq_lens;
+    p.q_len = q_len;
+    p.chunk = sp.chunk;
+    p.n_splits = sp.n_splits;
+    p.n_rows = static_cast<int>(n_rows);
+    p.n_items = static_cast<int>(items);
+    p.sig2 = sigma * 1.4426950408889634f;
+    p.out_scale = out_scale;
+    p.out = static_cast<uint8_t*>(out);
+    p.o_s0b = o_s0 * 2;
+    p.o_s1b = o_s1 * 2;
+    p.lse = lse;
+    p.part_o = part_o;
+    p.part_lse = part_lse;
+    p.err = d->err;
+    const int grid = grid_for(items, d->sms);
+    prof_begin(stream);
+    if (fmt == MLA_CACHE_BF16)
+      e = launch_attn_paged_bf16(p, grid, stream);
+    else if (fmt == MLA_CACHE_FP8)
+      e = launch_attn_paged_fp8(p, grid, stream);
+    else
+      e = launch_attn_paged_ds(p, grid, stream);
+    prof_end(stream);
+  }
   if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "decode attention launch failed: %s", cudaGetErrorString(e));
   if (sp.n_splits > 1) {
     MergeParams m{};
-    m.part_o = p.part_o;
-    m.part_lse = p.part_lse;
+    m.part_o = part_o;
+    m.part_lse = part_lse;
     m.S = sp.n_splits;
     m.n_rows = static_cast<int>(n_rows);
     m.H = H;
-    m.out = p.out;
-    m.o_s0b = p.o_s0b;
-    m.o_s1b = p.o_s1b;
+    m.seq_lens = seq_lens;
+    m.q_len = q_len;
+    m.chunk = sp.chunk;
+    m.out = static_cast<uint8_t*>(out);
+    m.o_s0b = o_s0 * 2;
+    m.o_s1b = o_s1 * 2;
     m.lse = lse;
     if (launch_merge(m, stream) != cudaSuccess)
       return fail(MLA_ERR_CUDA, "merge launch failed: %s", cudaGetErrorString(cudaGetLastError()));

@@ -35,6 +35,9 @@ struct MergeParams {
   const float* part_o;     // [S][n_rows][H][512]
   const float* part_lse;   // [S][n_rows][H]
   int S, n_rows, H;
+  const int32_t* seq_lens; // row r reads only the ceil(L / chunk) splits of its request r / q_len
+  int q_len;
+  int64_t chunk;
   uint8_t* out;            // bf16 rows
   int64_t o_s0b, o_s1b;
   float* lse;              // [n_rows, H] or null
@@ -63,8 +66,14 @@ cudaError_t launch_attn_sparse_ds(const AttnParams& p, int grid, cudaStream_t st
 cudaError_t launch_attn_paged_bf16(const AttnParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_attn_paged_fp8(const AttnParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_attn_paged_ds(const AttnParams& p, int grid, cudaStream_t stream);
-// Paged bf16 decode with TMA page loads; `tmap` points to a CUtensorMap (3-D, uint8,
-// [num_blocks][block_size][1152 B], 128-byte swizzle, box 128 B x tma_rows x 1).
-cudaError_t launch_attn_tma_bf16(const AttnParams& p, const void* tmap, int grid, cudaStream_t stream);
+// Paged decode with TMA page loads (ring pipeline), `nq` query columns per item.  `tkv` and
+// `tq` point to CUtensorMaps: the cache as [num_blocks][block_size][entry bytes] (uint8,
+// 128-byte swizzle, box 128 B x BR x 1) and the query as [rows][H][row bytes] (box 128 B x
+// qbox_h x qbox_q).
+struct PagedParams;
+cudaError_t launch_paged_tma_bf16(int nq, const PagedParams& p, const void* tkv, const void* tq, int grid,
+                                  cudaStream_t stream);
+cudaError_t launch_paged_tma_fp8(int nq, const PagedParams& p, const void* tkv, const void* tq, int grid,
+                                 cudaStream_t stream);
 
 }  // namespace mla

@@ -1,0 +1,51 @@
+// Paged decode kernel instantiations for the fp8 cache (TMA page loads, ring pipeline).
+#include "mla_internal.h"
+#include "mla_paged_tma.cuh"
+
+namespace mla {
+namespace {
+
+template <int NQ>
+cudaError_t launch_nq(const PagedParams& p, const void* tkv, const void* tq, int grid, cudaStream_t stream) {
+  using C = PagedCfg<kFP8, NQ>;
+  static bool configured[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!configured[dev]) {
+    e = cudaFuncSetAttribute(mla_paged_tma_kernel<kFP8, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
+    if (e != cudaSuccess) return e;
+    configured[dev] = true;
+  }
+  mla_paged_tma_kernel<kFP8, NQ><<<grid, C::kThreads, C::kAlloc, stream>>>(
+      p, *static_cast<const CUtensorMap*>(tkv), *static_cast<const CUtensorMap*>(tq));
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_paged_tma_fp8(int nq, const PagedParams& p, const void* tkv, const void* tq, int grid,
+                                 cudaStream_t stream) {
+  switch (nq) {
+    case 16:
+      return launch_nq<16>(p, tkv, tq, grid, stream);
+    case 32:
+      return launch_nq<32>(p, tkv, tq, grid, stream);
+    case 64:
+      return launch_nq<64>(p, tkv, tq, grid, stream);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace mla
+
+#ifdef MLA_TIMELINE
+extern "C" __attribute__((visibility("default"))) int mla_debug_timeline_fp8(void* events, void* counts) {
+  cudaMemcpyFromSymbol(events, mla::g_tl, sizeof(mla::g_tl));
+  cudaMemcpyFromSymbol(counts, mla::g_tl_n, sizeof(mla::g_tl_n));
+  const int zero[mla::kTlCtas][mla::kTlRoles] = {};
+  return cudaMemcpyToSymbol(mla::g_tl_n, zero, sizeof(zero)) == cudaSuccess ? 0 : -3;
+}
+#endif

@@ -166,13 +166,18 @@ __global__ void __launch_bounds__(128) mla_epilogue_kernel(const EpiParams p) {
 __global__ void __launch_bounds__(128) mla_merge_kernel(const MergeParams p) {
   const int64_t rh = blockIdx.x;
   const int64_t stride = static_cast<int64_t>(p.n_rows) * p.H;
-  float m = -CUDART_INF_F;
-  for (int s = 0; s < p.S; ++s) m = fmaxf(m, p.part_lse[s * stride + rh]);
   const int row = static_cast<int>(rh / p.H), h = static_cast<int>(rh % p.H);
+  int S = p.S;
+  if (p.seq_lens) {     // splits past the request's length hold nothing
+    const int64_t L = max(p.seq_lens[row / p.q_len], 0);
+    S = static_cast<int>(min(static_cast<int64_t>(S), (L + p.chunk - 1) / p.chunk));
+  }
+  float m = -CUDART_INF_F;
+  for (int s = 0; s < S; ++s) m = fmaxf(m, p.part_lse[s * stride + rh]);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float wsum = 0.f;
   if (m != -CUDART_INF_F) {
-    for (int s = 0; s < p.S; ++s) {
+    for (int s = 0; s < S; ++s) {
       const float ls = p.part_lse[s * stride + rh];
       if (ls == -CUDART_INF_F) continue;
       const float w = expf(ls - m);

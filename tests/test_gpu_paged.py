@@ -77,6 +77,19 @@ def test_block_sizes_and_heads(m, fmt, bs, H):
     assert_lse_close(l, rl, f"bs={bs} H={H}")
 
 
+@pytest.mark.parametrize("fmt,H,q_len", [(synth.BF16, 16, 3), (synth.FP8, 16, 5), (synth.FP8, 128, 1),
+                                         (synth.BF16, 128, 2), (synth.FP8, 8, 3), (synth.BF16, 48, 1)])
+def test_query_column_groups(m, fmt, H, q_len):
+    # query columns (token, head) split into groups: within a token, several tokens per group
+    # (with a ragged last group), and a request that fits one group
+    kw = dict(q_scale=0.05, k_scale=0.05) if fmt == synth.FP8 else {}
+    case = synth.paged_case(700 + H + q_len + fmt, fmt, B=3, q_len=q_len, H=H, L_lo=5, L_hi=1500, block_size=64,
+                            max_context=16384, **kw)
+    o, l, ro, rl = run(m, case)
+    assert_attn_close(o, ro, f"H={H} q_len={q_len}")
+    assert_lse_close(l, rl, f"H={H} q_len={q_len}")
+
+
 def test_padded_entry_pitch(m):
     case = synth.paged_case(601, synth.DS_MLA, B=4, q_len=1, H=16, L_lo=100, L_hi=700, block_size=64,
                             entry_pad=16)
