@@ -36,6 +36,24 @@
 
 #include "mla_attn.cuh"
 
+// Pipeline choices (measured on GB300; the defaults are the fastest found):
+//   MLA_OVERLAP_FP8  fp8 issues QK(t+1) before PV(t)
+//   MLA_LOOKAHEAD    tiles between a page-table lookup and the tile's loads
+//   MLA_L2PF         also prefetch that tile into L2 when its pages are known
+//   MLA_SLOT_COMMITS release each ring slot by its own commit (else by PV of its tile)
+#ifndef MLA_OVERLAP_FP8
+#define MLA_OVERLAP_FP8 1
+#endif
+#ifndef MLA_LOOKAHEAD
+#define MLA_LOOKAHEAD 2
+#endif
+#ifndef MLA_L2PF
+#define MLA_L2PF 1
+#endif
+#ifndef MLA_SLOT_COMMITS
+#define MLA_SLOT_COMMITS 1
+#endif
+
 namespace mla {
 
 struct PagedParams {
@@ -75,7 +93,10 @@ struct PagedCfg {
   static constexpr int kSW = NQ == 64 ? 8 : 4;           // softmax warps
   static constexpr int kNC = NQ * 4 / kSW;               // columns per softmax thread
   static constexpr int kThreads = 64 + 32 * kSW;
-  static constexpr bool kOverlap = F == kFP8;
+  static constexpr bool kOverlap = (F == kFP8) && MLA_OVERLAP_FP8;
+  static constexpr int kPfDist = MLA_LOOKAHEAD;           // tiles between a page lookup and its use
+  static constexpr bool kL2Pf = MLA_L2PF;
+  static constexpr bool kSlotCommits = MLA_SLOT_COMMITS;
   static constexpr int kQBytes = kNBQ * NQ * 128;
   static constexpr int kPBytes = F == kBF16 ? kTile * NQ * 2 : 2 * kTile * NQ;
   static constexpr int kRedBytes = 3 * NQ * 4 * 4;       // max partials [2][NQ][4], sum partials [NQ][4]
@@ -94,7 +115,7 @@ struct PagedCfg {
   static constexpr int kRed = kP + kPBytes;
   static constexpr int kItems = kRed + kRedBytes;
   static constexpr int kBar = kItems + kItemDepth * 32;
-  static constexpr int kNumBars = 2 * kR + 9 + 2 * kItemDepth;
+  static constexpr int kNumBars = 2 * kR + 8 + 2 * kItemDepth;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kTotal = kMisc + 16;
   static constexpr int kAlloc = kTotal + 1024;
@@ -109,6 +130,27 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, in
       "[%5];" ::"r"(smem_u32(dst)),
       "l"(tm), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* tm, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tm), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
+// Bounded wait by lane 0 of the warp only (fewer shared-memory polls); the verdict and the
+// acquired view reach the other lanes through the warp barrier.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  bool w = true;
+  if ((threadIdx.x & 31) == 0) w = mbar_wait(bar, parity, abort_flag);
+  w = __shfl_sync(0xFFFFFFFFu, w ? 1 : 0, 0) != 0;
+  __syncwarp();
+  return w;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // D(tmem) (+)= A x B with e4m3 operands (kind::f8f6f4), fp32 accumulate.
@@ -194,16 +236,19 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
   float* red = reinterpret_cast<float*>(smem + C::kRed);
   WorkItem* items = reinterpret_cast<WorkItem*>(smem + C::kItems);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
-  uint64_t* full = bars;
-  uint64_t* empty = bars + R;
-  uint64_t* s_full = bars + 2 * R;        // [2]
-  uint64_t* p_full = bars + 2 * R + 2;
-  uint64_t* pv_done = bars + 2 * R + 3;
-  uint64_t* q_full = bars + 2 * R + 4;
-  uint64_t* q_empty = bars + 2 * R + 5;
-  uint64_t* fin = bars + 2 * R + 6;
-  uint64_t* item_full = bars + 2 * R + 9;
+  // Every tcgen05.commit costs the tensor pipe a drain, so the MMA side commits twice per tile
+  // only: s_full[t & 1] after QK(t) and pv_done[t & 1] after PV(t).  A ring slot is free once
+  // PV of the tile that last used it is done, and the query tile once QK of the item's last
+  // tile is.
+  uint64_t* full = bars;                  // [R] TMA landed
+  uint64_t* s_full = bars + R;            // [2]
+  uint64_t* pv_done = bars + R + 2;       // [2]
+  uint64_t* p_full = bars + R + 4;
+  uint64_t* q_full = bars + R + 5;
+  uint64_t* fin = bars + R + 6;
+  uint64_t* item_full = bars + R + 8;
   uint64_t* item_empty = item_full + kItemDepth;
+  uint64_t* empty = item_empty + kItemDepth;  // [R] slot consumed (per-slot release)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
 
@@ -219,12 +264,12 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&pv_done[i], 1);
+    }
     mbar_init(p_full, 1);
-    mbar_init(pv_done, 1);
     mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
     mbar_init(fin, 1);
     for (int k = 0; k < kItemDepth; ++k) {
       mbar_init(&item_full[k], 1);
@@ -247,20 +292,22 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
     const int NPG = kTile / p.BR;
     uint32_t errbits = 0;
     int64_t pos = 0;   // ring positions issued
-    int nitem = 0, nq = 0;
+    int nitem = 0, nq = 0, stride_k = 0;
+    int gq = -1;       // global index of the last tile of the previous item with tiles
+    int gt_next = 0;   // global index of the next tile
+    int t_waited = -1; // last tile whose PV the producer waited for
     bool ok = true;
-    int ticket = 0;
-    if (lane == 0) ticket = p.sched ? static_cast<int>(atomicAdd(p.sched, 1u)) : static_cast<int>(blockIdx.x);
-    ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
-    int stride_k = 1;
-    while (ok) {
-      const int item = ticket;
-      if (item >= p.n_items) break;
+    // work items: decode a queue ticket (empty splits skipped: the merge ignores them)
+    auto take_ticket = [&]() -> int {
+      int item = 0;
       if (lane == 0)
-        ticket = p.sched ? static_cast<int>(atomicAdd(p.sched, 1u)) : static_cast<int>(blockIdx.x + stride_k * gridDim.x);
-      ticket = __shfl_sync(0xFFFFFFFFu, ticket, 0);
+        item = p.sched ? static_cast<int>(atomicAdd(p.sched, 1u)) : static_cast<int>(blockIdx.x + stride_k * gridDim.x);
       ++stride_k;
-      WorkItem it;
+      return __shfl_sync(0xFFFFFFFFu, item, 0);
+    };
+    auto decode = [&](int item, WorkItem& it) -> bool {     // false: empty split
+      it.b = -1;
+      if (item >= p.n_items) return true;
       const int bg = p.B * p.G;
       it.s = item / bg;
       it.b = (item % bg) / p.G;
@@ -270,65 +317,122 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
       it.n = min(max(it.L - it.k0, 0), p.chunk);
       it.ntiles = (it.n + kTile - 1) / kTile;
       it.pad = 0;
-      if (it.n == 0 && p.n_splits > 1) continue;     // an empty split: the merge skips it
+      return it.n > 0 || p.n_splits == 1;
+    };
+    auto next_item = [&](int ticket) -> WorkItem {
+      WorkItem it{};
+      while (!decode(ticket, it)) ticket = take_ticket();
+      return it;
+    };
+    // block_table entry of page q of tile t of an item (-1: past the item), issued early and
+    // checked late so that its latency hides behind the copies in flight
+    auto page_raw = [&](const WorkItem& it, int t, int q) -> int {
+      if (it.b < 0 || t >= it.ntiles) return -2;
+      const int kp = it.k0 + t * kTile + q * p.BR;
+      if (kp >= it.k0 + it.n) return -1;
+      return p.block_table[static_cast<int64_t>(it.b) * p.bt_stride + kp / p.block_size];
+    };
+    auto page_fix = [&](const WorkItem& it, int t, int q, int raw, int& y) -> int {
+      y = 0;
+      if (raw == -1 || raw == -2) return p.num_blocks;
+      if (raw < 0 || raw >= p.num_blocks) {
+        errbits |= 2u;
+        return p.num_blocks;
+      }
+      y = (it.k0 + t * kTile + q * p.BR) % p.block_size;
+      return raw;
+    };
+    constexpr int D = C::kPfDist;
+    // resolved pages of the next D tiles in processing order (lane q < NPG: page q)
+    int fb[D], fy[D];
+    bool fv[D];
+#pragma unroll
+    for (int i = 0; i < D; ++i) fv[i] = false, fb[i] = 0, fy[i] = 0;
+    // the next item is claimed only when the current one is D tiles from its end, so that
+    // the queue hands the tail out evenly
+    WorkItem cur = next_item(take_ticket());
+    WorkItem nxt{};
+    bool have_nxt = false;
+    while (ok && cur.b >= 0) {
       {
         const int k = nitem % kItemDepth;
-        if (nitem >= kItemDepth && !mbar_wait(&item_empty[k], ((nitem / kItemDepth) - 1) & 1, abort_flag)) {
+        if (nitem >= kItemDepth && !warp_wait(&item_empty[k], ((nitem / kItemDepth) - 1) & 1, abort_flag)) {
           ok = false;
           break;
         }
         if (lane == 0) {
-          items[k] = it;
+          items[k] = cur;
           mbar_arrive(&item_full[k]);
         }
         ++nitem;
       }
-      if (it.ntiles == 0) continue;
-      // query columns of the item: box (128 B x qbox_h heads x qbox_q tokens) per block
-      if (nq > 0 && !mbar_wait(q_empty, (nq - 1) & 1, abort_flag)) {
-        ok = false;
-        break;
-      }
-      if (lane == 0) {
-        const int cg0 = it.g * NQ;
-        const int h0 = cg0 % p.H, r0 = it.b * p.q_len + cg0 / p.H;
-        mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(C::kNBQ * 128 * p.qbox_h * p.qbox_q));
-#pragma unroll 1
-        for (int blk = 0; blk < C::kNBQ; ++blk) {
-          const int x = (F == kFP8 && blk == 4) ? 448 : 128 * blk;
-          tma_load_3d(qs + blk * NQ * 128, &tm_q, x, h0, r0, q_full);
+      if (lane == 0) TL(0, 5);
+      if (cur.ntiles > 0) {
+        // query columns of the item: box (128 B x qbox_h heads x qbox_q tokens) per block
+        if (gq >= 0 && !warp_wait(&s_full[gq & 1], static_cast<uint32_t>(gq >> 1) & 1u, abort_flag)) {
+          ok = false;
+          break;
         }
-      }
-      ++nq;
-      for (int t = 0; t < it.ntiles && ok; ++t) {
-        // page ids of the tile (lane q < NPG holds page q); out-of-range -> zero-filled box
-        int blk = p.num_blocks, y = 0;
-        if (lane < NPG) {
-          const int kp = it.k0 + t * kTile + lane * p.BR;
-          if (kp < it.k0 + it.n) {
-            const int id = p.block_table[static_cast<int64_t>(it.b) * p.bt_stride + kp / p.block_size];
-            if (id >= 0 && id < p.num_blocks) {
-              blk = id;
-              y = kp % p.block_size;
-            } else {
-              errbits |= 2u;
-            }
+        if (lane == 0) {
+          const int cg0 = cur.g * NQ;
+          const int h0 = cg0 % p.H, r0 = cur.b * p.q_len + cg0 / p.H;
+          mbar_arrive_expect_tx(q_full, static_cast<uint32_t>(C::kNBQ * 128 * p.qbox_h * p.qbox_q));
+#pragma unroll 1
+          for (int blk = 0; blk < C::kNBQ; ++blk) {
+            const int x = (F == kFP8 && blk == 4) ? 448 : 128 * blk;
+            tma_load_3d(qs + blk * NQ * 128, &tm_q, x, h0, r0, q_full);
           }
         }
+        ++nq;
+      }
+      for (int t = 0; t < cur.ntiles && ok; ++t) {
+        if (!have_nxt && t + D >= cur.ntiles) {
+          nxt = next_item(take_ticket());
+          have_nxt = true;
+        }
+        // pages of this tile: from the lookahead queue, else looked up now
+        int blk, y;
+        if (fv[0]) {
+          blk = fb[0];
+          y = fy[0];
+        } else {
+          const int raw = lane < NPG ? page_raw(cur, t, lane) : -2;
+          blk = page_fix(cur, t, lane, raw, y);
+        }
+#pragma unroll
+        for (int i = 0; i + 1 < D; ++i) fb[i] = fb[i + 1], fy[i] = fy[i + 1], fv[i] = fv[i + 1];
+        // the tile D ahead (this item or the next): table entries requested now
+        const int ta = t + D;
+        const bool in_cur = ta < cur.ntiles;
+        const WorkItem& ia = in_cur ? cur : nxt;
+        const int tta = in_cur ? ta : ta - cur.ntiles;
+        const bool av = in_cur || (nxt.b >= 0 && tta < nxt.ntiles);
+        const int raw_a = (av && lane < NPG) ? page_raw(ia, tta, lane) : -2;
         if (lane == 0) TL(0, 1);
 #pragma unroll 1
         for (int b = 0; b < NB; ++b, ++pos) {
           const int slot = static_cast<int>(pos % R);
-          const int use = static_cast<int>(pos / R);
-          if (use > 0 && !mbar_wait(&empty[slot], (use - 1) & 1, abort_flag)) {
-            ok = false;
-            break;
+          if (C::kSlotCommits && pos >= R) {
+            if (!warp_wait(&empty[slot], static_cast<uint32_t>(pos / R - 1) & 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+          } else if (pos >= R) {
+            const int tu = static_cast<int>((pos - R) / NB);     // tile that last used the slot
+            if (tu != t_waited) {
+              if (!warp_wait(&pv_done[tu & 1], static_cast<uint32_t>(tu >> 1) & 1u, abort_flag)) {
+                ok = false;
+                break;
+              }
+              t_waited = tu;
+            }
           }
           if (F == kBF16 && b == 9) {
             if (lane == 0) mbar_arrive(&full[slot]);
             continue;
           }
           if (lane == 0) mbar_arrive_expect_tx(&full[slot], kSlotBytes);
+          if (lane == 0 && (b == 0 || b == NB - 1)) TL(0, (b == 0 ? 1000 : 3000) + static_cast<int>((pos / NB) % 1000));
           __syncwarp();
           const int x = (F == kFP8 && b == 4) ? 448 : 128 * b;
           for (int q = 0; q < NPG; ++q) {
@@ -337,12 +441,32 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
             if (lane == 0) tma_load_3d(ring + slot * kSlotBytes + q * p.BR * 128, &tm_kv, x, yy, z, &full[slot]);
           }
         }
+        // finish the lookahead: queue its pages (and prefetch them into L2)
+        {
+          int ya = 0;
+          const int ba = page_fix(ia, tta, lane, raw_a, ya);
+          fb[D - 1] = ba;
+          fy[D - 1] = ya;
+          fv[D - 1] = av;
+          for (int q = 0; q < NPG && av && C::kL2Pf; ++q) {
+            const int z = __shfl_sync(0xFFFFFFFFu, ba, q);
+            const int yy = __shfl_sync(0xFFFFFFFFu, ya, q);
+            if (z < p.num_blocks && lane < C::kNBQ) tma_prefetch_3d(&tm_kv, (F == kFP8 && lane == 4) ? 448 : 128 * lane, yy, z);
+          }
+        }
       }
+      if (cur.ntiles > 0) {
+        gt_next += cur.ntiles;
+        gq = gt_next - 1;
+      }
+      if (!have_nxt) nxt = next_item(take_ticket());
+      cur = nxt;
+      have_nxt = false;
     }
     // end marker
     if (ok) {
       const int k = nitem % kItemDepth;
-      if (nitem < kItemDepth || mbar_wait(&item_empty[k], ((nitem / kItemDepth) - 1) & 1, abort_flag)) {
+      if (nitem < kItemDepth || warp_wait(&item_empty[k], ((nitem / kItemDepth) - 1) & 1, abort_flag)) {
         if (lane == 0) {
           WorkItem e{};
           e.b = -1;
@@ -352,7 +476,7 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
       }
     }
     // never leave copies in flight behind us
-    {
+    if (lane == 0) {
       volatile int no_abort = 0;
       const int64_t first = pos > R ? pos - R : 0;
       for (int64_t q = first; q < pos; ++q) {
@@ -361,6 +485,7 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
       }
       if (nq > 0) mbar_wait(q_full, (nq - 1) & 1, &no_abort);
     }
+    __syncwarp();
     errbits = __reduce_or_sync(0xFFFFFFFFu, errbits);
     if (lane == 0 && errbits) set_device_error(p.err, errbits);
   } else if (warp == 1) {
@@ -381,16 +506,57 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
       bool ok = true;
       int nit = 0, nq = 0, g = 0;
       // QK of global tile gt into S buffer gt & 1; returns false on a failed wait
+      auto issue_pv = [&](int gt, bool first) -> bool {
+        if (!mbar_wait(p_full, static_cast<uint32_t>(gt) & 1u, abort_flag)) return false;
+        tc_fence_after();
+        TL(2, 3);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t dO = tmem + C::kTmemO + j * NQ;
+          if (F == kBF16) {
+            const uint64_t aV = dV0 + ((slot_of(gt, 2 * j) * kSlotBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_f16_ss(dO, aV + ((kk * 2048) >> 4), dP0 + ((kk * NQ * 32) >> 4), kIdPv, (!first || kk > 0) ? 1u : 0u);
+            if (C::kSlotCommits) {
+              mma_commit(&empty[slot_of(gt, 2 * j)]);
+              mma_commit(&empty[slot_of(gt, 2 * j + 1)]);
+            }
+          } else {
+            const uint64_t aV = dV0 + ((slot_of(gt, j) * kSlotBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t pb = dP0 + ((kk * NQ * 32) >> 4);
+              mma_f8_ss(dO, aV + ((kk * 4096) >> 4), pb, kIdPv, (!first || kk > 0) ? 1u : 0u);
+              mma_f8_ss(dO, aV + ((kk * 4096) >> 4), pb + ((kTile * NQ) >> 4), kIdPv, 1u);
+            }
+            if (C::kSlotCommits) mma_commit(&empty[slot_of(gt, j)]);
+          }
+        }
+        mma_commit(&pv_done[gt & 1]);
+        TL(2, 4);
+        return true;
+      };
+      // PV of tile pv_gt may be issued in the middle of a QK whose blocks are still landing
+      // (the two write different accumulators)
+      int pv_gt = -1;
+      bool pv_first = false;
       auto issue_qk = [&](int gt, bool last) -> bool {
         const uint32_t dS = tmem + C::kTmemS + (gt & 1) * NQ;
         TL(2, 1);
 #pragma unroll 1
         for (int b = 0; b < NB; ++b) {
           const int slot = slot_of(gt, b);
+          if (pv_gt >= 0 && !mbar_test_wait(&full[slot], use_of(gt, b)) &&
+              mbar_test_wait(p_full, static_cast<uint32_t>(pv_gt) & 1u)) {
+            if (!issue_pv(pv_gt, pv_first)) return false;
+            pv_gt = -1;
+          }
           if (!mbar_wait(&full[slot], use_of(gt, b), abort_flag)) return false;
+          if (b == 0 || b == NB - 1) TL(2, (b == 0 ? 1000 : 2000) + gt % 1000);
           tc_fence_after();
           if (F == kBF16 && b == 9) {
-            mbar_arrive(&empty[slot]);
+            if (C::kSlotCommits) mbar_arrive(&empty[slot]);
             continue;
           }
           const uint64_t aK = dK0 + ((slot * kSlotBytes) >> 4);
@@ -408,38 +574,8 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
           }
         }
         mma_commit(&s_full[gt & 1]);
-        mma_commit(&empty[slot_of(gt, C::kRope)]);
-        if (last) mma_commit(q_empty);
+        if (C::kSlotCommits) mma_commit(&empty[slot_of(gt, C::kRope)]);
         TL(2, 2);
-        return true;
-      };
-      auto issue_pv = [&](int gt, bool first) -> bool {
-        if (!mbar_wait(p_full, static_cast<uint32_t>(gt) & 1u, abort_flag)) return false;
-        tc_fence_after();
-        TL(2, 3);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t dO = tmem + C::kTmemO + j * NQ;
-          if (F == kBF16) {
-            const uint64_t aV = dV0 + ((slot_of(gt, 2 * j) * kSlotBytes) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_f16_ss(dO, aV + ((kk * 2048) >> 4), dP0 + ((kk * NQ * 32) >> 4), kIdPv, (!first || kk > 0) ? 1u : 0u);
-            mma_commit(&empty[slot_of(gt, 2 * j)]);
-            mma_commit(&empty[slot_of(gt, 2 * j + 1)]);
-          } else {
-            const uint64_t aV = dV0 + ((slot_of(gt, j) * kSlotBytes) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t pb = dP0 + ((kk * NQ * 32) >> 4);
-              mma_f8_ss(dO, aV + ((kk * 4096) >> 4), pb, kIdPv, (!first || kk > 0) ? 1u : 0u);
-              mma_f8_ss(dO, aV + ((kk * 4096) >> 4), pb + ((kTile * NQ) >> 4), kIdPv, 1u);
-            }
-            mma_commit(&empty[slot_of(gt, j)]);
-          }
-        }
-        mma_commit(pv_done);
-        TL(2, 4);
         return true;
       };
       while (ok) {
@@ -456,8 +592,11 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
         if (C::kOverlap) {
           ok = issue_qk(g, it.ntiles == 1);
           for (int t = 1; t < it.ntiles && ok; ++t) {
+            pv_gt = g + t - 1;
+            pv_first = (t == 1);
             ok = issue_qk(g + t, t == it.ntiles - 1);
-            ok = ok && issue_pv(g + t - 1, t == 1);
+            if (ok && pv_gt >= 0) ok = issue_pv(pv_gt, pv_first);
+            pv_gt = -1;
           }
           ok = ok && issue_pv(g + it.ntiles - 1, it.ntiles == 1);
         } else {
@@ -475,6 +614,10 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ softmax + epilogue
+    // Online softmax with a lazily moved reference max m (per column): p = 2^(s - m + kPExp)
+    // stays below 2^(kTau + kPExp) as long as no logit exceeds m by more than kTau; only a
+    // tile that does (a vote over all softmax threads) computes its exact column maxima,
+    // moves m up to them and rescales O and the row sums by 2^(m_old - m_new).
     constexpr int NT = 32 * C::kSW;
     const int sw = warp - 2;
     const int quad = warp & 3;                  // TMEM lane quadrant of this warp
@@ -484,27 +627,29 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     float* red_m = red;                         // [2][NQ][4]
     float* red_l = red + 2 * NQ * 4;            // [NQ][4]
-    constexpr float kPScale = F == kFP8 ? 8.f : 0.f;   // fp8: p carried as 256 p (log2 256 = 8)
+    constexpr float kTau = F == kFP8 ? 4.f : 8.f;
+    // row sums: per thread and column when registers allow (6 warps), else per warp and
+    // column (lane % NC), reduced over the warp each tile
+    constexpr bool kLReg = C::kThreads <= 192;
+    constexpr int NL = kLReg ? NC : 1;
+    constexpr float kPExp = F == kFP8 ? 4.f : 0.f;   // fp8: p carried as 2^4 p, at most 2^8 (e4m3 max 448)
     int nit = 0, g = 0;
     bool ok = true;
     while (ok) {
       const int k = nit % kItemDepth;
-      bool w = mbar_wait(&item_full[k], (nit / kItemDepth) & 1, abort_flag);
+      bool w = warp_wait(&item_full[k], (nit / kItemDepth) & 1, abort_flag);
       const WorkItem it = items[k];
       ++nit;
       if (!named_bar_and(1, NT, w)) break;
       if (it.b < 0) break;
-      float m_run[NC];
+      float m_ref[NC], l_part[NL];
 #pragma unroll
-      for (int c = 0; c < NC; ++c) m_run[c] = -CUDART_INF_F;
-      float l_lane = 0.f;                         // this warp's keys' sum of p, column (lane % NC)
+      for (int c = 0; c < NC; ++c) m_ref[c] = -CUDART_INF_F;
+#pragma unroll
+      for (int c = 0; c < NL; ++c) l_part[c] = 0.f;
       const int cgb = it.g * NQ + c0;           // global column of this thread's column 0
-      for (int t = 0; t < it.ntiles; ++t) {
-        const int gt = g + t;
-        w = mbar_wait(&s_full[gt & 1], static_cast<uint32_t>(gt >> 1) & 1u, abort_flag);
-        tc_fence_after();
-        if (stid == 0) TL(3, 1);
-        float s[NC];
+      // logits of this thread's key for its columns, scaled and masked
+      auto load_s = [&](float (&s)[NC], int gt, int t) {
         tmem_ld_n<NC>(tl + C::kTmemS + (gt & 1) * NQ + c0, s);
         tmem_ld_wait();
         const int kpos = it.k0 + t * kTile + row;
@@ -518,6 +663,15 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
           for (int c = 0; c < NC; ++c)
             if ((cgb + c) / p.H < dq) s[c] = -CUDART_INF_F;
         }
+      };
+      for (int t = 0; t < it.ntiles; ++t) {
+        const int gt = g + t;
+        w = warp_wait(&s_full[gt & 1], static_cast<uint32_t>(gt >> 1) & 1u, abort_flag);
+        tc_fence_after();
+        if (stid == 0) TL(3, 1);
+        float s[NC];
+        load_s(s, gt, t);
+        const bool rv = it.k0 + t * kTile + row < it.k0 + it.n;
         // rows past the item never reach PV with stale contents
         if (!rv && c0 == 0) {
 #pragma unroll 1
@@ -528,47 +682,71 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
             for (int i = 0; i < 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
           }
         }
-        float* rb = red_m + (gt & 1) * NQ * 4;
-        {
-          float v[NC];
+        bool need = false;
 #pragma unroll
-          for (int c = 0; c < NC; ++c) v[c] = s[c];
-          const float wm = warp_col_reduce<NC, true>(v, lane);
-          if (NC == 32 || lane < 16) rb[(c0 + (lane % NC)) * 4 + quad] = wm;
+        for (int c = 0; c < NC; ++c) need |= (s[c] > m_ref[c] + kTau) || (m_ref[c] == -CUDART_INF_F && s[c] > -CUDART_INF_F);
+        if (stid == 0) TL(3, 10);
+        // one barrier decides: nothing to do (common), or move the reference (or abort)
+        const bool rare = named_bar_or(1, NT, need || !w);
+        bool pv_waited = false;
+        if (rare) {
+          ok = named_bar_and(1, NT, w);
+          if (!ok) break;
+          float* rb = red_m + (gt & 1) * NQ * 4;
+          {
+            const float wm = warp_col_reduce<NC, true>(s, lane);
+            if (NC == 32 || lane < 16) rb[(c0 + (lane % NC)) * 4 + quad] = wm;
+          }
+          named_bar_sync(1, NT);
+          float mt_l;
+          {
+            const float4 q4 = reinterpret_cast<const float4*>(rb)[c0 + (lane % NC)];
+            mt_l = fmaxf(fmaxf(q4.x, q4.y), fmaxf(q4.z, q4.w));
+          }
+          bool resc = false;
+          float alpha[NC];
+          float alpha_lane = 1.f;
+#pragma unroll
+          for (int c = 0; c < NC; ++c) {
+            const float mo = m_ref[c];
+            const float mn = fmaxf(mo, __shfl_sync(0xFFFFFFFFu, mt_l, c));
+            alpha[c] = (mo == -CUDART_INF_F) ? 0.f : ex2(mo - mn);
+            resc |= (mn != mo);
+            m_ref[c] = mn;
+            if (kLReg) l_part[kLReg ? c : 0] *= alpha[c];
+            alpha_lane = (c == (lane % NC)) ? alpha[c] : alpha_lane;
+          }
+          if (!kLReg) l_part[0] *= alpha_lane;
+          // O of the previous tiles moves to the new reference once PV of the last tile is done
+          if (t > 0) {
+            w = warp_wait(&pv_done[(gt - 1) & 1], static_cast<uint32_t>((gt - 1) >> 1) & 1u, abort_flag);
+            tc_fence_after();
+            pv_waited = true;
+            if (w && resc) {
+#pragma unroll 1
+              for (int j = 0; j < 4; ++j) {
+                float o[NC];
+                tmem_ld_n<NC>(tl + C::kTmemO + j * NQ + c0, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < NC; ++c) o[c] *= alpha[c];
+                tmem_st_n<NC>(tl + C::kTmemO + j * NQ + c0, o);
+              }
+              tmem_st_wait();
+            }
+          }
+          load_s(s, gt, t);
         }
-        ok = named_bar_and(1, NT, w);
-        if (!ok) break;
-        bool changed = false;
-        float alpha[NC];
-        float alpha_lane = 0.f;
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-          const float4 q4 = reinterpret_cast<const float4*>(rb)[c0 + c];
-          const float mt = fmaxf(fmaxf(q4.x, q4.y), fmaxf(q4.z, q4.w));
-          const float mnew = fmaxf(m_run[c], mt);
-          const float mu = (mnew == -CUDART_INF_F) ? 0.f : mnew;
-          alpha[c] = exp2f(m_run[c] - mu);
-          s[c] = exp2f(s[c] - mu + kPScale);     // p (fp8: 256 p)
-          if (c == (lane % NC)) alpha_lane = alpha[c];
-          changed |= (mnew != m_run[c]);
-          m_run[c] = mnew;
+          const float mu = (m_ref[c] == -CUDART_INF_F) ? 0.f : m_ref[c];
+          s[c] = ex2(s[c] - mu + kPExp);
+          if (kLReg) l_part[kLReg ? c : 0] += s[c];
         }
         if (stid == 0) TL(3, 2);
-        if (t > 0) {
-          w = mbar_wait(pv_done, static_cast<uint32_t>(gt - 1) & 1u, abort_flag);   // PV of the previous tile
+        if (t > 0 && !pv_waited) {
+          w = warp_wait(&pv_done[(gt - 1) & 1], static_cast<uint32_t>((gt - 1) >> 1) & 1u, abort_flag);   // PV of the previous tile
           tc_fence_after();
-          if (w && changed) {
-#pragma unroll 1
-            for (int j = 0; j < 4; ++j) {
-              float o[NC];
-              tmem_ld_n<NC>(tl + C::kTmemO + j * NQ + c0, o);
-              tmem_ld_wait();
-#pragma unroll
-              for (int c = 0; c < NC; ++c) o[c] *= alpha[c];
-              tmem_st_n<NC>(tl + C::kTmemO + j * NQ + c0, o);
-            }
-            tmem_st_wait();
-          }
         }
         if (F == kBF16) {
           // MN-major no-swizzle: 8 keys x 8 columns core matrices, 8-key groups NQ*16 bytes apart
@@ -606,32 +784,47 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
         if (!ok) break;
         if (stid == 0) mbar_arrive(p_full);
         if (stid == 0) TL(3, 3);
-        // row sums of the tile while PV runs
-        l_lane = l_lane * alpha_lane + warp_col_reduce<NC, false>(s, lane);
+        if (!kLReg) l_part[0] += warp_col_reduce<NC, false>(s, lane);   // while PV runs
       }
       if (!ok) break;
       // ---- epilogue: O / l and the LSE of every column of the item
+      if (stid == 0) TL(3, 5);
       w = true;
       if (it.ntiles > 0) {
-        w = mbar_wait(pv_done, static_cast<uint32_t>(g + it.ntiles - 1) & 1u, abort_flag);
+        w = warp_wait(&pv_done[(g + it.ntiles - 1) & 1], static_cast<uint32_t>((g + it.ntiles - 1) >> 1) & 1u, abort_flag);
         tc_fence_after();
       }
       g += it.ntiles;
-      if (NC == 32 || lane < 16) red_l[(c0 + (lane % NC)) * 4 + quad] = l_lane;
+      {
+        float lw;
+        if constexpr (kLReg) lw = warp_col_reduce<NC, false>(l_part, lane);
+        else lw = l_part[0];
+        if (NC == 32 || lane < 16) red_l[(c0 + (lane % NC)) * 4 + quad] = lw;
+      }
       ok = named_bar_and(1, NT, w);
       if (!ok) break;
-      float inv[NC];
-      float lse_mine = -CUDART_INF_F;
-#pragma unroll
-      for (int c = 0; c < NC; ++c) {
-        const float4 q4 = reinterpret_cast<const float4*>(red_l)[c0 + c];
+      // column (lane % NC): total row sum, 1 / l and the LSE; then 1 / l to every lane
+      const int cl = lane % NC;
+      float inv_l, lse_l;
+      {
+        const float4 q4 = reinterpret_cast<const float4*>(red_l)[c0 + cl];
         const float l = (q4.x + q4.y) + (q4.z + q4.w);
+        float m_l = m_ref[0];
+#pragma unroll
+        for (int c = 1; c < NC; ++c) m_l = (c == cl) ? m_ref[c] : m_l;
         const bool live = l > 0.f;
-        inv[c] = live ? p.out_scale / l : 0.f;
-        const float lse = live ? (m_run[c] + log2f(l) - kPScale) * 0.69314718055994531f : -CUDART_INF_F;
-        if (c == row) lse_mine = lse;
+        inv_l = live ? __fdividef(p.out_scale, l) : 0.f;
+        lse_l = live ? (m_l + __log2f(l) - kPExp) * 0.69314718055994531f : -CUDART_INF_F;
       }
+      float inv[NC];
+#pragma unroll
+      for (int c = 0; c < NC; ++c) inv[c] = __shfl_sync(0xFFFFFFFFu, inv_l, c);
       const bool final_out = (p.n_splits == 1);
+      // (row, head) of column cg: row = b * q_len + cg / H, head = cg % H, so the flat index
+      // row * H + head is b * q_len * H + cg
+      const int64_t flat0 = static_cast<int64_t>(it.b) * p.q_len * p.H + cgb;
+      const int ncol = min(NC, p.cols - cgb);
+      const int qi0 = cgb / p.H, h0 = cgb % p.H;
 #pragma unroll 1
       for (int j = 0; j < 4; ++j) {
         float o[NC];
@@ -643,32 +836,36 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
           for (int c = 0; c < NC; ++c) o[c] = 0.f;
         }
         const int d = 128 * j + row;
+        if (final_out) {
+          int qi = qi0, h = h0;
+          uint8_t* base = p.out + static_cast<int64_t>(it.b) * p.q_len * p.o_s0b + 2 * d;
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-          const int cg = cgb + c;
-          if (cg < p.cols) {
-            const int orow = it.b * p.q_len + cg / p.H, h = cg % p.H;
-            const float val = o[c] * inv[c];
-            if (final_out) {
-              *reinterpret_cast<__nv_bfloat16*>(p.out + orow * p.o_s0b + h * p.o_s1b + 2 * d) = __float2bfloat16_rn(val);
-            } else {
-              p.part_o[((static_cast<int64_t>(it.s) * p.n_rows + orow) * p.H + h) * kLora + d] = val;
+          for (int c = 0; c < NC; ++c) {
+            if (c < ncol)
+              *reinterpret_cast<__nv_bfloat16*>(base + qi * p.o_s0b + h * p.o_s1b) = __float2bfloat16_rn(o[c] * inv[c]);
+            if (++h == p.H) {
+              h = 0;
+              ++qi;
             }
           }
+        } else {
+          float* dst = p.part_o + ((static_cast<int64_t>(it.s) * p.n_rows * p.H + flat0) * kLora + d);
+#pragma unroll
+          for (int c = 0; c < NC; ++c)
+            if (c < ncol) dst[static_cast<int64_t>(c) * kLora] = o[c] * inv[c];
         }
       }
-      if (row < NC && cgb + row < p.cols) {
-        const int cg = cgb + row;
-        const int orow = it.b * p.q_len + cg / p.H, h = cg % p.H;
+      if (row < 32 && (NC == 32 || lane < 16) && cl < ncol) {
         if (final_out) {
-          if (p.lse) p.lse[static_cast<int64_t>(orow) * p.H + h] = lse_mine;
+          if (p.lse) p.lse[flat0 + cl] = lse_l;
         } else {
-          p.part_lse[(static_cast<int64_t>(it.s) * p.n_rows + orow) * p.H + h] = lse_mine;
+          p.part_lse[static_cast<int64_t>(it.s) * p.n_rows * p.H + flat0 + cl] = lse_l;
         }
       }
       tc_fence_before();
       named_bar_sync(1, NT);
       if (stid == 0) mbar_arrive(&item_empty[k]);
+      if (stid == 0) TL(3, 6);
     }
   }
 

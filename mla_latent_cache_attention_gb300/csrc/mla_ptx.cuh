@@ -52,6 +52,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity.  `abort_flag` (shared) is polled so that
 // one role's failure releases the others.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
@@ -98,6 +110,18 @@ __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bo
   asm volatile(
       "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %2, 0;\n"
       " bar.red.and.pred po, %1, %3, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
+      : "=r"(r)
+      : "r"(id), "r"(v ? 1u : 0u), "r"(nthreads)
+      : "memory");
+  return r != 0;
+}
+
+// Named barrier that ORs a predicate over the participating threads.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t nthreads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred pi, po;\n setp.ne.u32 pi, %2, 0;\n"
+      " bar.red.or.pred po, %1, %3, pi;\n selp.u32 %0, 1, 0, po;\n}\n"
       : "=r"(r)
       : "r"(id), "r"(v ? 1u : 0u), "r"(nthreads)
       : "memory");
