@@ -4,6 +4,7 @@
 #include <cuda.h>
 
 #include <cstdarg>
+#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -11,6 +12,7 @@
 #include "mla.h"
 #include "mla_attn.cuh"
 #include "mla_internal.h"
+#include "mla_ds.cuh"
 #include "mla_paged_tma.cuh"
 
 namespace mla {
@@ -109,6 +111,16 @@ size_t workspace_bytes_for(int64_t n_rows, int H, const SplitPlan& sp) {
   return ((po + 255) & ~size_t(255)) + ((pl + 255) & ~size_t(255)) + 256;
 }
 
+// The sparse forward runs the staged-converter kernel unless MLA_SPARSE_GATHER=1 selects the
+// vector-load gather kernel (faster on some index patterns, slower on the uniform top-k one).
+bool sparse_gather_kernel() {
+  static const int v = [] {
+    const char* e = getenv("MLA_SPARSE_GATHER");
+    return (e && e[0] == '1') ? 1 : 0;
+  }();
+  return v == 1;
+}
+
 int grid_for(int64_t items, int sms) {
   return static_cast<int>(items < sms ? items : sms);
 }
@@ -123,6 +135,7 @@ struct TmapKey {
   const void* base;
   uint64_t dims[3], strides[2];
   uint32_t box[3];
+  bool swz;
   bool operator==(const TmapKey& o) const { return memcmp(this, &o, sizeof *this) == 0; }
 };
 struct TmapEntry {
@@ -143,11 +156,13 @@ int tma_rows_for(int block_size) {
   return 0;
 }
 
-// 3-D uint8 tensor map with 128-byte swizzle: dims {x bytes, y, z}, strides {y, z} in bytes.
+// 3-D uint8 tensor map (128-byte swizzle, or none): dims {x bytes, y, z}, strides {y, z} in
+// bytes.
 int tmap_3d(const void* base, const uint64_t (&dims)[3], const uint64_t (&strides)[2], const uint32_t (&box)[3],
-            CUtensorMap* out) {
+            CUtensorMap* out, bool swizzle = true) {
   TmapKey key{};
   key.base = base;
+  key.swz = swizzle;
   for (int i = 0; i < 3; ++i) key.dims[i] = dims[i], key.box[i] = box[i];
   key.strides[0] = strides[0];
   key.strides[1] = strides[1];
@@ -172,8 +187,8 @@ int tmap_3d(const void* base, const uint64_t (&dims)[3], const uint64_t (&stride
   const cuuint32_t bx[3] = {box[0], box[1], box[2]};
   const cuuint32_t es[3] = {1, 1, 1};
   const CUresult r = enc(&e.map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), d, st, bx, es,
-                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     e.used = false;
     return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
@@ -338,32 +353,65 @@ extern "C" int mla_sparse_fwd(const void* q, int64_t q_s0, int64_t q_s1, const v
   if (lse && !aligned(lse, 4)) return fail(MLA_ERR_INVALID, "lse must be 4-byte aligned");
   DevInfo* d = nullptr;
   if (int rc = dev_info(&d)) return rc;
-  AttnParams p{};
+  DsParams p{};
   p.q = static_cast<const uint8_t*>(q);
   p.q_s0b = q_s0 * 2;
   p.q_s1b = q_s1 * 2;
   p.H = H;
-  p.n_hgroups = (H + kRows - 1) / kRows;
+  p.q_len = 1;
+  p.B = T;
+  p.G = (H + 15) / 16;
+  p.cols = H;
   p.records = static_cast<const uint8_t*>(kv_records);
   p.rec_stride = record_stride_bytes;
   p.num_records = num_records;
   p.indptr = kv_indptr;
   p.indices = kv_indices;
   p.has_invalid = has_invalid ? 1 : 0;
-  p.q_len = 1;
-  p.n_splits = 1;
   p.chunk = 0;
+  p.n_splits = 1;
   p.n_rows = T;
-  p.n_items = T * p.n_hgroups;
+  const int64_t items = static_cast<int64_t>(T) * p.G;
+  if (items >= (int64_t(1) << 31)) return fail(MLA_ERR_UNSUPPORTED, "too many work items");
+  p.n_items = static_cast<int>(items);
   p.sig2 = softmax_scale * 1.4426950408889634f;
-  p.out_scale = 1.f;
   p.out = static_cast<uint8_t*>(out);
   p.o_s0b = o_s0 * 2;
   p.o_s1b = o_s1 * 2;
   p.lse = lse;
+  p.sched = nullptr;
   p.err = d->err;
   prof_begin(stream);
-  const cudaError_t e = launch_attn_sparse_ds(p, grid_for(p.n_items, d->sms), stream);
+  cudaError_t e;
+  if (sparse_gather_kernel()) {
+    e = launch_ds_sparse(p, grid_for(items, d->sms), stream);
+  } else {
+    AttnParams a{};
+    a.q = p.q;
+    a.q_s0b = p.q_s0b;
+    a.q_s1b = p.q_s1b;
+    a.H = H;
+    a.n_hgroups = (H + kRows - 1) / kRows;
+    a.records = p.records;
+    a.rec_stride = p.rec_stride;
+    a.num_records = p.num_records;
+    a.indptr = p.indptr;
+    a.indices = p.indices;
+    a.has_invalid = p.has_invalid;
+    a.q_len = 1;
+    a.n_splits = 1;
+    a.chunk = 0;
+    a.n_rows = T;
+    a.n_items = T * a.n_hgroups;
+    a.sig2 = p.sig2;
+    a.out_scale = 1.f;
+    a.out = p.out;
+    a.o_s0b = p.o_s0b;
+    a.o_s1b = p.o_s1b;
+    a.lse = lse;
+    a.err = d->err;
+    e = launch_attn_sparse_ds(a, grid_for(a.n_items, d->sms), stream);
+  }
   prof_end(stream);
   if (e != cudaSuccess)
     return fail(MLA_ERR_CUDA, "sparse attention launch failed: %s", cudaGetErrorString(cudaGetLastError()));
@@ -436,11 +484,77 @@ extern "C" int mla_paged_decode(const void* q, int64_t q_s0, int64_t q_s1, const
   const float out_scale = fmt == MLA_CACHE_FP8 ? k_scale : 1.f;
   const int qe = fmt == MLA_CACHE_FP8 ? 1 : 2;
 
-  // The TMA page kernel serves bf16 and plain-fp8 caches whose blocks tile the 128-key tile,
-  // with a query whose rows and heads are 16-byte aligned.
-  const int tma_rows = (fmt != MLA_CACHE_FP8_DS_MLA) ? tma_rows_for(block_size) : 0;
+  // The TMA page kernels serve caches whose blocks tile the 128-key tile, with a query whose
+  // rows and heads are 16-byte aligned.
+  const int tma_rows = tma_rows_for(block_size);
+  if (fmt == MLA_CACHE_FP8_DS_MLA && tma_rows > 0 && aligned(q, 16) && (q_s0 * 2) % 16 == 0 && (q_s1 * 2) % 16 == 0 &&
+      num_blocks < (int64_t(1) << 31) && max_context < (1 << 30)) {
+    const int G = (q_len * H + 15) / 16;
+    const int64_t items = static_cast<int64_t>(sp.n_splits) * B * G;
+    if (items >= (int64_t(1) << 31)) return fail(MLA_ERR_UNSUPPORTED, "too many work items");
+    CUtensorMap tkv, tsc;
+    const uint64_t kd[3] = {656, static_cast<uint64_t>(block_size), static_cast<uint64_t>(num_blocks)};
+    const uint64_t ks[2] = {static_cast<uint64_t>(entry_stride_bytes), static_cast<uint64_t>(block_stride_bytes)};
+    const uint32_t kb[3] = {128, static_cast<uint32_t>(tma_rows), 1};
+    const uint32_t sb[3] = {16, static_cast<uint32_t>(tma_rows), 1};
+    if (int rc = tmap_3d(kv_cache, kd, ks, kb, &tkv)) return rc;
+    if (int rc = tmap_3d(kv_cache, kd, ks, sb, &tsc, false)) return rc;
+    DsParams p{};
+    p.q = static_cast<const uint8_t*>(q);
+    p.q_s0b = q_s0 * 2;
+    p.q_s1b = q_s1 * 2;
+    p.H = H;
+    p.q_len = q_len;
+    p.B = B;
+    p.G = G;
+    p.cols = H * q_len;
+    p.block_table = block_table;
+    p.bt_stride = bt_stride;
+    p.seq_lens = seq_lens;
+    p.num_blocks = static_cast<int>(num_blocks);
+    p.block_size = block_size;
+    p.BR = tma_rows;
+    p.chunk = static_cast<int>(sp.chunk);
+    p.n_splits = sp.n_splits;
+    p.n_items = static_cast<int>(items);
+    p.n_rows = static_cast<int>(n_rows);
+    p.sig2 = softmax_scale * 1.4426950408889634f;
+    p.out = static_cast<uint8_t*>(out);
+    p.o_s0b = o_s0 * 2;
+    p.o_s1b = o_s1 * 2;
+    p.lse = lse;
+    p.part_o = part_o;
+    p.part_lse = part_lse;
+    p.sched = sched;
+    p.err = d->err;
+    if (sched && cudaMemsetAsync(sched, 0, sizeof(uint32_t), stream) != cudaSuccess)
+      return fail(MLA_ERR_CUDA, "scheduler reset failed");
+    prof_begin(stream);
+    const cudaError_t e = launch_ds_paged(p, &tkv, &tsc, grid_for(items, d->sms), stream);
+    prof_end(stream);
+    if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "decode attention launch failed: %s", cudaGetErrorString(e));
+    if (sp.n_splits > 1) {
+      MergeParams m{};
+      m.part_o = part_o;
+      m.part_lse = part_lse;
+      m.S = sp.n_splits;
+      m.n_rows = static_cast<int>(n_rows);
+      m.H = H;
+      m.seq_lens = seq_lens;
+      m.q_len = q_len;
+      m.chunk = sp.chunk;
+      m.out = static_cast<uint8_t*>(out);
+      m.o_s0b = o_s0 * 2;
+      m.o_s1b = o_s1 * 2;
+      m.lse = lse;
+      if (launch_merge(m, stream) != cudaSuccess)
+        return fail(MLA_ERR_CUDA, "merge launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+    }
+    return ok();
+  }
+  const bool tma_fmt = fmt != MLA_CACHE_FP8_DS_MLA;
   ColPlan cp{};
-  const bool use_tma = tma_rows > 0 && plan_columns(static_cast<int>(fmt), H, q_len, &cp) && aligned(q, 16) &&
+  const bool use_tma = tma_fmt && tma_rows > 0 && plan_columns(static_cast<int>(fmt), H, q_len, &cp) && aligned(q, 16) &&
                        (q_s0 * qe) % 16 == 0 && (q_s1 * qe) % 16 == 0 && num_blocks < (int64_t(1) << 31) &&
                        max_context < (1 << 30);
   cudaError_t e;

@@ -491,12 +491,20 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
         const int kin = pc * FT::kPiece + lane;
         const uint8_t* src = (lane < FT::kPiece && kin < nk) ? ring[kin] : nullptr;
         const uint32_t mask = __ballot_sync(0xFFFFFFFFu, src != nullptr);
+        // entries that sit back to back at the staging pitch (a page of an unpadded cache)
+        // arrive with one copy instead of one per entry
+        const int cnt = min(FT::kPiece, nk - pc * FT::kPiece);
+        const uint8_t* src0 = reinterpret_cast<const uint8_t*>(
+            __shfl_sync(0xFFFFFFFFu, static_cast<unsigned long long>(reinterpret_cast<uintptr_t>(src)), 0));
+        const bool contig = (FT::kRecPad == FT::kRec) && mask == ((cnt >= 32) ? 0xFFFFFFFFu : ((1u << cnt) - 1u)) &&
+                            __all_sync(0xFFFFFFFFu, lane >= cnt || src == src0 + static_cast<int64_t>(lane) * FT::kRec);
         if (lane == 0) {
           meta[st] = mask;
           mbar_arrive_expect_tx(&full[st], static_cast<uint32_t>(__popc(mask)) * FT::kRec);
+          if (contig) bulk_g2s(stage + st * SM::kStageBytes, src0, static_cast<uint32_t>(cnt) * FT::kRec, &full[st]);
         }
         __syncwarp();
-        if (src) bulk_g2s(stage + st * SM::kStageBytes + lane * FT::kRecPad, src, FT::kRec, &full[st]);
+        if (!contig && src) bulk_g2s(stage + st * SM::kStageBytes + lane * FT::kRecPad, src, FT::kRec, &full[st]);
         armed[st] = true;
         armed_par[st] = eph;
         if (++st == NST) { st = 0; eph ^= 1u; }

@@ -1,0 +1,779 @@
+// mla_ds.cuh -- MLA over the 656-byte fp8_ds_mla record: the sparse (CSR-indexed) forward and
+// the paged decode / spec-verify.
+//
+// What it computes ("FlashMLA: Multi-head Latent Attention decode kernels", sparse attention
+// over the fp8_ds_mla cache; "vLLM MLA backend", the fp8_ds_mla record): a record holds 512
+// e4m3 codes of kv_c_normed in four 128-wide tiles with one fp32 scale each, then 64 bf16 of
+// k_pe.  The key is k = [s_j * code_j (j = 0..3) | k_pe], the value its first 512 entries; the
+// logit of query q is softmax_scale * q . k.
+//
+// How (GB300 design, exact up to fp32 accumulation):
+//   * QK on the tensor cores directly on the e4m3 codes (kind::f8f6f4): the bf16 query of
+//     every column c is split into two e4m3 terms hi + lo of 2^e_c q (an e4m3 holds 4
+//     significant bits, a bf16 8, so hi + lo carries q exactly wherever 2^e_c |q| >= 2^-2),
+//     stacked as 2 x 16 columns of the B operand.  Each key tile j accumulates separately
+//     (S_j, 32 TMEM columns) and the softmax forms s = 2^-e_c sum_j s_j (S_j,hi + S_j,lo) +
+//     S_rope, so the per-key scale is applied in fp32.  k_pe . q_pe runs as a bf16 MMA.
+//   * PV on the e4m3 codes as well: O_j^T = V_j^T P_j with P_j = p * s_j * r_j, one P per value
+//     tile so that each key's scale multiplies its own term, as four e5m2 terms (stacked along
+//     N, 16 columns each; e4m3 codes x e5m2 weights).  Each term rounds what the earlier ones
+//     left, so P_j holds to about 2^-12 relative, and e5m2 reaches down to 2^-16, which keeps
+//     the many small weights of a long row (whose values reach 448 times the scale) from
+//     being lost under an e4m3 floor of 2^-9.  r_j is a power of two kept per item so
+//     that s_j r_j <= 1; when a later key needs a smaller r_j, O_j is rescaled by the (exact)
+//     ratio.
+//   * Online softmax with a lazily moved reference max, as in the page kernel.
+//   * Paged source: TMA page boxes (four code tiles, k_pe, and the scales through a second,
+//     unswizzled map) into a two-tile ring.  Sparse source: eight gather warps load each
+//     record with 16-byte vector loads (a record is 41 of them) and store it in the same
+//     layout; masked or out-of-range indices store zeros and a row flag.
+//
+// Warps: 0 scheduler (+ TMA producer for pages), 1 MMA issuer, 2..5 softmax + query
+// preparation + epilogue, 6..13 gather (sparse only).
+#pragma once
+#include "mla_paged_tma.cuh"
+
+namespace mla {
+
+struct DsParams {
+  const uint8_t* q;               // bf16 [rows][H][>=576]
+  int64_t q_s0b, q_s1b;
+  int H, q_len, B, G, cols;       // B requests (sparse: query rows), G groups of 16 columns
+  // sparse source
+  const uint8_t* records;
+  int64_t rec_stride, num_records;
+  const int32_t* indptr;
+  const int32_t* indices;
+  int has_invalid;
+  // paged source
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const int32_t* seq_lens;
+  int num_blocks, block_size, BR;
+  int chunk, n_splits, n_items, n_rows;
+  float sig2;                     // softmax scale * log2(e)
+  uint8_t* out;
+  int64_t o_s0b, o_s1b;
+  float* lse;
+  float* part_o;
+  float* part_lse;
+  uint32_t* sched;
+  uint32_t* err;
+};
+
+template <bool kSparse>
+struct DsCfg {
+  static constexpr int NQ = 16, NB = 5, R = 10;        // a tile is 5 ring slots; the ring holds two
+  static constexpr int kGatherWarps = kSparse ? 8 : 0;
+  static constexpr int kThreads = 192 + 32 * kGatherWarps;
+  static constexpr int kRing = 0;
+  static constexpr int kScale = kRing + R * kSlotBytes;          // [2][128] float4
+  static constexpr int kQ = kScale + 2 * kTile * 16;              // 4 x (32 rows x 128 B) hi/lo + 16 x 128 B rope
+  static constexpr int kQRope = kQ + 4 * 32 * 128;
+  static constexpr int kP = kQRope + NQ * 128;                    // 4 x (128 keys x 64 B)
+  static constexpr int kRed = kP + 4 * kTile * 64;                // [2][16][4] max, [16][4] sum, [4][4] scale max
+  static constexpr int kColF = kRed + (3 * NQ * 4 + 16) * 4;      // [16] 2^-e_c
+  static constexpr int kValid = kColF + NQ * 4;                   // [2][128] row flags (sparse)
+  static constexpr int kItems = kValid + 2 * kTile;
+  static constexpr int kBar = kItems + kItemDepth * 32;
+  static constexpr int kNumBars = R + 8 + 2 * kItemDepth;
+  static constexpr int kMisc = kBar + kNumBars * 8;
+  static constexpr int kTotal = kMisc + 16;
+  static constexpr int kAlloc = kTotal + 1024;
+  static_assert(kAlloc <= kSmemLimit, "shared memory budget");
+  static constexpr int kS = 0;                                    // S (144 columns): S_j at 32 j, rope at 128
+  static constexpr int kTmemO = 160;                              // O_j at kTmemO + 64 j (4 terms x 16 columns)
+  static constexpr int kTmemCols = 512;
+};
+
+__device__ __forceinline__ uint32_t e5m2x2_sat(float a, float b) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E5M2));
+}
+__device__ __forceinline__ float2 e5m2x2_to_float2(uint32_t v) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E5M2);
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }   // e in [-126, 127]
+
+// 2^e with e the largest integer such that a * 2^e <= 448 (a > 0 finite), clamped to the
+// normal range.
+__device__ __forceinline__ int e4m3_fit_exponent(float a) {
+  if (!(a > 0.f)) return 0;
+  int e = 8 - (static_cast<int>((__float_as_uint(a) >> 23) & 0xFF) - 127);   // a * 2^e in [256, 512)
+  e = max(min(e, 126), -126);
+  while (e > -126 && a * pow2i(e) > 448.f) --e;
+  while (e < 126 && a * pow2i(e + 1) <= 448.f) ++e;
+  return e;
+}
+
+template <bool kSparse>
+__global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
+    mla_ds_kernel(const __grid_constant__ DsParams p, const __grid_constant__ CUtensorMap tm_kv,
+                  const __grid_constant__ CUtensorMap tm_sc) {
+  using C = DsCfg<kSparse>;
+  constexpr int R = C::R, NB = C::NB, NQ = C::NQ;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem + C::kRing;
+  float4* scl = reinterpret_cast<float4*>(smem + C::kScale);      // [2][128]
+  uint8_t* qs = smem + C::kQ;
+  uint8_t* qr = smem + C::kQRope;
+  uint8_t* ps = smem + C::kP;
+  float* red = reinterpret_cast<float*>(smem + C::kRed);
+  float* colf = reinterpret_cast<float*>(smem + C::kColF);
+  uint8_t* vrow = smem + C::kValid;                                 // [2][128]
+  WorkItem* items = reinterpret_cast<WorkItem*>(smem + C::kItems);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
+  uint64_t* full = bars;                  // [R] slot data landed (TMA bytes / gather warps)
+  uint64_t* s_full = bars + R;            // [2]
+  uint64_t* pv_done = bars + R + 2;       // [2]
+  uint64_t* p_full = bars + R + 4;
+  uint64_t* q_full = bars + R + 5;
+  uint64_t* fin = bars + R + 6;
+  uint64_t* s_free = bars + R + 7;        // the softmax has read S
+  uint64_t* item_full = bars + R + 8;
+  uint64_t* item_empty = item_full + kItemDepth;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  TL_DECL;
+
+  if (tid == 0) {
+    for (int i = 0; i < R; ++i) mbar_init(&full[i], kSparse ? C::kGatherWarps : 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&pv_done[i], 1);
+    }
+    mbar_init(p_full, 1);
+    mbar_init(q_full, 1);
+    mbar_init(fin, 1);
+    mbar_init(s_free, 1);
+    for (int k = 0; k < kItemDepth; ++k) {
+      mbar_init(&item_full[k], 1);
+      mbar_init(&item_empty[k], 2 + C::kGatherWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  // items: (split s, request / row b, column group g)
+  auto decode = [&](int item, WorkItem& it) -> bool {     // false: an empty split (skipped)
+    it.b = -1;
+    if (item >= p.n_items) return true;
+    const int bg = p.B * p.G;
+    it.s = item / bg;
+    it.b = (item % bg) / p.G;
+    it.g = item % p.G;
+    it.pad = 0;
+    if (kSparse) {
+      const int b0 = p.indptr[it.b], b1 = p.indptr[it.b + 1];
+      it.k0 = b0;
+      it.n = max(b1 - b0, 0);
+      it.L = it.k0 + it.n;
+    } else {
+      it.L = max(p.seq_lens[it.b], 0);
+      it.k0 = it.s * p.chunk;
+      it.n = min(max(it.L - it.k0, 0), p.chunk);
+    }
+    it.ntiles = (it.n + kTile - 1) / kTile;
+    return it.n > 0 || p.n_splits == 1;
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ scheduler / page producer
+    uint32_t errbits = 0;
+    int nitem = 0, stride_k = 0, gt_next = 0;
+    bool ok = true;
+    auto take_ticket = [&]() -> int {
+      int item = 0;
+      if (lane == 0)
+        item = p.sched ? static_cast<int>(atomicAdd(p.sched, 1u)) : static_cast<int>(blockIdx.x + stride_k * gridDim.x);
+      ++stride_k;
+      return __shfl_sync(0xFFFFFFFFu, item, 0);
+    };
+    auto next_item = [&]() -> WorkItem {
+      WorkItem it{};
+      while (!decode(take_ticket(), it)) {
+      }
+      return it;
+    };
+    const int NPG = kTile / max(p.BR, 1);
+    int64_t pos = 0;
+    int t_waited = -1;
+    WorkItem cur = next_item();
+    while (ok && cur.b >= 0) {
+      {
+        const int k = nitem % kItemDepth;
+        if (nitem >= kItemDepth && !warp_wait(&item_empty[k], ((nitem / kItemDepth) - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        if (lane == 0) {
+          items[k] = cur;
+          mbar_arrive(&item_full[k]);
+        }
+        ++nitem;
+      }
+      if (!kSparse) {
+        for (int t = 0; t < cur.ntiles && ok; ++t) {
+          const int gt = gt_next + t;
+          int blk = p.num_blocks, y = 0;
+          if (lane < NPG) {
+            const int kp = cur.k0 + t * kTile + lane * p.BR;
+            if (kp < cur.k0 + cur.n) {
+              const int id = p.block_table[static_cast<int64_t>(cur.b) * p.bt_stride + kp / p.block_size];
+              if (id >= 0 && id < p.num_blocks) {
+                blk = id;
+                y = kp % p.block_size;
+              } else {
+                errbits |= 2u;
+              }
+            }
+          }
+          // the two-tile ring: tile gt reuses the slots of tile gt - 2
+          if (gt >= 2 && gt - 2 != t_waited) {
+            if (!warp_wait(&pv_done[gt & 1], static_cast<uint32_t>((gt - 2) >> 1) & 1u, abort_flag)) {
+              ok = false;
+              break;
+            }
+            t_waited = gt - 2;
+          }
+#pragma unroll 1
+          for (int b = 0; b < NB; ++b, ++pos) {
+            const int slot = static_cast<int>(pos % R);
+            const uint32_t bytes = kSlotBytes + (b == NB - 1 ? static_cast<uint32_t>(kTile * 16) : 0u);
+            if (lane == 0) mbar_arrive_expect_tx(&full[slot], bytes);
+            __syncwarp();
+            const int x = (b == NB - 1) ? 528 : 128 * b;
+            for (int q = 0; q < NPG; ++q) {
+              const int z = __shfl_sync(0xFFFFFFFFu, blk, q);
+              const int yy = __shfl_sync(0xFFFFFFFFu, y, q);
+              if (lane == 0) {
+                tma_load_3d(ring + slot * kSlotBytes + q * p.BR * 128, &tm_kv, x, yy, z, &full[slot]);
+                if (b == NB - 1)
+                  tma_load_3d(reinterpret_cast<uint8_t*>(scl + (gt & 1) * kTile) + q * p.BR * 16, &tm_sc, 512, yy, z,
+                              &full[slot]);
+              }
+            }
+          }
+        }
+      }
+      gt_next += cur.ntiles;
+      if (ok) cur = next_item();
+    }
+    if (ok) {
+      const int k = nitem % kItemDepth;
+      if (nitem < kItemDepth || warp_wait(&item_empty[k], ((nitem / kItemDepth) - 1) & 1, abort_flag)) {
+        if (lane == 0) {
+          WorkItem e{};
+          e.b = -1;
+          items[k] = e;
+          mbar_arrive(&item_full[k]);
+        }
+      }
+    }
+    if (!kSparse && lane == 0) {     // never leave copies in flight behind us
+      volatile int no_abort = 0;
+      const int64_t first = pos > R ? pos - R : 0;
+      for (int64_t q = first; q < pos; ++q) mbar_wait(&full[q % R], static_cast<uint32_t>(q / R) & 1u, &no_abort);
+    }
+    __syncwarp();
+    errbits = __reduce_or_sync(0xFFFFFFFFu, errbits);
+    if (lane == 0 && errbits) set_device_error(p.err, errbits);
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t ring_a = smem_u32(ring), q_a = smem_u32(qs), qr_a = smem_u32(qr), p_a = smem_u32(ps);
+      const uint64_t dK0 = smem_desc(ring_a, 16, 1024, kSwizzle128B);
+      const uint64_t dQ0 = smem_desc(q_a, 16, 1024, kSwizzle128B);
+      const uint64_t dQr = smem_desc(qr_a, 16, 1024, kSwizzle128B);
+      const uint64_t dV0 = smem_desc(ring_a, kSlotBytes, 1024, kSwizzle128B);
+      const uint64_t dP0 = smem_desc(p_a, 512, 128, kSwizzleNone);
+      constexpr uint32_t kIdNope = idesc_e4m3(128, 32, 0, 0);
+      constexpr uint32_t kIdRope = idesc_f16(128, 16, 1, 1, 0, 0);
+      constexpr uint32_t kIdPv = idesc_e4m3(128, 64, 1, 1) | (1u << 10);   // B (weights) in e5m2
+      auto slot_of = [&](int gt, int b) -> int { return (gt & 1) * NB + b; };
+      auto issue_qk = [&](int gt) -> bool {
+        // one S buffer: the softmax of the previous tile must have read it
+        if (gt > 0 && !mbar_wait(s_free, static_cast<uint32_t>(gt - 1) & 1u, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t dS = tmem + C::kS;
+#pragma unroll 1
+        for (int b = 0; b < NB; ++b) {
+          const int slot = slot_of(gt, b);
+          if (!mbar_wait(&full[slot], static_cast<uint32_t>(gt >> 1) & 1u, abort_flag)) return false;
+          tc_fence_after();
+          const uint64_t aK = dK0 + ((slot * kSlotBytes) >> 4);
+          if (b < 4) {
+            const uint64_t bQ = dQ0 + ((b * 32 * 128) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f8_ss(dS + 32 * b, aK + ((kk * 32) >> 4), bQ + ((kk * 32) >> 4), kIdNope, kk > 0 ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ss(dS + 128, aK + ((kk * 32) >> 4), dQr + ((kk * 32) >> 4), kIdRope, kk > 0 ? 1u : 0u);
+          }
+        }
+        mma_commit(&s_full[0]);
+        return true;
+      };
+      auto issue_pv = [&](int gt, bool first) -> bool {
+        if (!mbar_wait(p_full, static_cast<uint32_t>(gt) & 1u, abort_flag)) return false;
+        tc_fence_after();
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint64_t aV = dV0 + ((slot_of(gt, j) * kSlotBytes) >> 4);
+          const uint64_t bP = dP0 + ((j * kTile * 64) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f8_ss(tmem + C::kTmemO + 64 * j, aV + ((kk * 4096) >> 4), bP + ((kk * 2048) >> 4), kIdPv,
+                      (!first || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&pv_done[gt & 1]);
+        return true;
+      };
+      bool ok = true;
+      int nit = 0, nq = 0, g = 0;
+      while (ok) {
+        const int k = nit % kItemDepth;
+        if (!mbar_wait(&item_full[k], (nit / kItemDepth) & 1, abort_flag)) break;
+        const WorkItem it = items[k];
+        mbar_arrive(&item_empty[k]);
+        ++nit;
+        if (it.b < 0) break;
+        if (it.ntiles == 0) continue;
+        if (!mbar_wait(q_full, nq & 1, abort_flag)) break;
+        ++nq;
+        tc_fence_after();
+        ok = issue_qk(g);
+        for (int t = 1; t < it.ntiles && ok; ++t) {
+          ok = issue_qk(g + t);
+          ok = ok && issue_pv(g + t - 1, t == 1);
+        }
+        ok = ok && issue_pv(g + it.ntiles - 1, it.ntiles == 1);
+        g += it.ntiles;
+      }
+      mma_commit(fin);
+      volatile int no_abort = 0;
+      mbar_wait(fin, 0, &no_abort);
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ------------------------------------------------------------------ softmax, query, epilogue
+    constexpr int NT = 128;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;
+    const int stid = tid - 64;
+    const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    float* red_m = red;                 // [2][16][4]
+    float* red_l = red + 2 * NQ * 4;    // [16][4]
+    float* red_s = red + 3 * NQ * 4;    // [4 warps][4 tiles] scale maxima
+    constexpr float kTau = 4.f, kPExp = 4.f;
+    int nit = 0, g = 0;
+    bool ok = true;
+    while (ok) {
+      const int k = nit % kItemDepth;
+      bool w = warp_wait(&item_full[k], (nit / kItemDepth) & 1, abort_flag);
+      const WorkItem it = items[k];
+      ++nit;
+      if (!named_bar_and(1, NT, w)) break;
+      if (it.b < 0) break;
+      const int cgb = it.g * NQ;     // first global column of the item
+      if (it.ntiles > 0) {
+        // query: thread (c = stid / 8, part = stid % 8) handles elements 64 part .. +63 of
+        // column c; hi / lo e4m3 of 2^e_c q into rows c / 16 + c, k_pe as it is
+        const int c = stid >> 3, part = stid & 7;
+        const int cg = cgb + c;
+        const bool live = cg < p.cols;
+        const uint8_t* qrow = live ? p.q + (static_cast<int64_t>(it.b) * p.q_len + cg / p.H) * p.q_s0b + (cg % p.H) * p.q_s1b
+                                   : nullptr;
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = live ? *reinterpret_cast<const uint4*>(qrow + part * 128 + 16 * i) : make_uint4(0, 0, 0, 0);
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t wv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            amax = fmaxf(amax, fabsf(__uint_as_float(wv[u] << 16)));
+            amax = fmaxf(amax, fabsf(__uint_as_float(wv[u] & 0xFFFF0000u)));
+          }
+        }
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+        const int e = e4m3_fit_exponent(amax);
+        const float sc = pow2i(e);
+        if (part == 0) colf[c] = pow2i(-e);
+        // 64 elements -> 64 hi bytes + 64 lo bytes at block part / 2, byte (part & 1) * 64
+        const int blk = part >> 1;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {     // 16 elements per 16-byte output chunk
+          uint32_t hw[4], lw[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint4 a = v[2 * i + (u >> 1)];
+            const uint32_t w0 = (u & 1) ? a.z : a.x, w1 = (u & 1) ? a.w : a.y;
+            const float x0 = __uint_as_float(w0 << 16) * sc, x1 = __uint_as_float(w0 & 0xFFFF0000u) * sc;
+            const float x2 = __uint_as_float(w1 << 16) * sc, x3 = __uint_as_float(w1 & 0xFFFF0000u) * sc;
+            const uint32_t h01 = e4m3x2_sat(x0, x1), h23 = e4m3x2_sat(x2, x3);
+            const float2 f01 = e4m3x2_to_float2(h01), f23 = e4m3x2_to_float2(h23);
+            hw[u] = h01 | (h23 << 16);
+            lw[u] = e4m3x2_sat(x0 - f01.x, x1 - f01.y) | (e4m3x2_sat(x2 - f23.x, x3 - f23.y) << 16);
+          }
+          const int chunk = (part & 1) * 4 + i;
+          uint8_t* base = qs + blk * (32 * 128);
+          *reinterpret_cast<uint4*>(base + sw128(c, chunk)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+          *reinterpret_cast<uint4*>(base + sw128(16 + c, chunk)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+        }
+        // k_pe part: 128 bytes per column, one 16-byte chunk per thread
+        const uint4 rv = live ? *reinterpret_cast<const uint4*>(qrow + 1024 + 16 * part) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(qr + sw128(c, part)) = rv;
+        fence_proxy_async_smem();
+        named_bar_sync(1, NT);
+        if (stid == 0) mbar_arrive(q_full);
+      }
+      float m_ref[NQ], l_part[NQ];
+#pragma unroll
+      for (int c = 0; c < NQ; ++c) {
+        m_ref[c] = -CUDART_INF_F;
+        l_part[c] = 0.f;
+      }
+      float rj[4] = {0.f, 0.f, 0.f, 0.f};   // per value tile: P_j = p s_j r_j (0: not set yet)
+      for (int t = 0; t < it.ntiles; ++t) {
+        const int gt = g + t;
+        w = warp_wait(&s_full[0], static_cast<uint32_t>(gt) & 1u, abort_flag);
+        tc_fence_after();
+        const float4 s4 = scl[(gt & 1) * kTile + row];
+        const float sj[4] = {s4.x, s4.y, s4.z, s4.w};
+        const int kpos = it.k0 + t * kTile + row;
+        bool rv = kpos < it.k0 + it.n;
+        if (kSparse) rv = rv && vrow[(gt & 1) * kTile + row] != 0;
+        float s[NQ];
+        {
+          const uint32_t sb = tl + C::kS;
+#pragma unroll
+          for (int c = 0; c < NQ; ++c) s[c] = 0.f;
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float hl[32];
+            tmem_ld_n<32>(sb + 32 * j, hl);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < NQ; ++c) s[c] = fmaf(sj[j], hl[c] + hl[16 + c], s[c]);
+          }
+          float sr[16];
+          tmem_ld16(sb + 128, sr);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < NQ; ++c) s[c] = rv ? p.sig2 * fmaf(colf[c], s[c], sr[c]) : -CUDART_INF_F;
+        }
+        if (!kSparse) {
+          const int dq = kpos - it.L + p.q_len;
+          if (rv && dq > 0) {
+#pragma unroll
+            for (int c = 0; c < NQ; ++c)
+              if ((cgb + c) / p.H < dq) s[c] = -CUDART_INF_F;
+          }
+        }
+        bool need = false;
+#pragma unroll
+        for (int c = 0; c < NQ; ++c) need |= (s[c] > m_ref[c] + kTau) | ((m_ref[c] == -CUDART_INF_F) & (s[c] > -CUDART_INF_F));
+#pragma unroll
+        for (int j = 0; j < 4; ++j) need |= rv && (sj[j] * rj[j] > 1.f || rj[j] == 0.f);
+        tc_fence_before();
+        const bool rare = named_bar_or(1, NT, need || !w);
+        if (stid == 0) mbar_arrive(s_free);     // S is in registers: the next QK may overwrite it
+        bool pv_waited = false;
+        if (rare) {
+          ok = named_bar_and(1, NT, w);
+          if (!ok) break;
+          float* rb = red_m + (gt & 1) * NQ * 4;
+          {
+            float v[NQ];
+#pragma unroll
+            for (int c = 0; c < NQ; ++c) v[c] = s[c];
+            const float wm = warp_col_reduce<NQ, true>(v, lane);
+            if (lane < 16) rb[lane * 4 + quad] = wm;
+            float sm[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              sm[j] = rv ? sj[j] : 0.f;
+#pragma unroll
+              for (int o = 16; o >= 1; o >>= 1) sm[j] = fmaxf(sm[j], __shfl_xor_sync(0xFFFFFFFFu, sm[j], o));
+            }
+            if (lane == 0) *reinterpret_cast<float4*>(red_s + quad * 4) = make_float4(sm[0], sm[1], sm[2], sm[3]);
+          }
+          named_bar_sync(1, NT);
+          float mt_l;
+          {
+            const float4 q4 = reinterpret_cast<const float4*>(rb)[lane % NQ];
+            mt_l = fmaxf(fmaxf(q4.x, q4.y), fmaxf(q4.z, q4.w));
+          }
+          bool resc = false;
+          float alpha[NQ];
+#pragma unroll
+          for (int c = 0; c < NQ; ++c) {
+            const float mo = m_ref[c];
+            const float mn = fmaxf(mo, __shfl_sync(0xFFFFFFFFu, mt_l, c));
+            alpha[c] = (mo == -CUDART_INF_F) ? 0.f : ex2(mo - mn);
+            resc |= (mn != mo);
+            m_ref[c] = mn;
+            l_part[c] *= alpha[c];
+          }
+          // value-tile references: r_j = 2^-ceil(log2 max s_j) once a larger scale shows up
+          float ratio[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            float mx = 0.f;
+#pragma unroll
+            for (int wq = 0; wq < 4; ++wq) mx = fmaxf(mx, red_s[wq * 4 + j]);
+            ratio[j] = 1.f;
+            if (mx > 0.f && (rj[j] == 0.f || mx * rj[j] > 1.f)) {
+              const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFF) - 127;
+              int e = -(ex + ((__float_as_uint(mx) & 0x7FFFFFu) ? 1 : 0));   // 2^e * mx <= 1
+              e = max(min(e, 126), -126);
+              const float rn = pow2i(e);
+              ratio[j] = (rj[j] == 0.f) ? 0.f : rn / rj[j];
+              resc |= (rj[j] != 0.f);
+              rj[j] = rn;
+            }
+          }
+          if (t > 0) {
+            w = warp_wait(&pv_done[(gt - 1) & 1], static_cast<uint32_t>((gt - 1) >> 1) & 1u, abort_flag);
+            tc_fence_after();
+            pv_waited = true;
+            if (w && resc) {
+#pragma unroll 1
+              for (int jq = 0; jq < 16; ++jq) {     // value tile jq / 4, term jq % 4
+                float o[16];
+                tmem_ld16(tl + C::kTmemO + 16 * jq, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 16; ++c) o[c] *= alpha[c] * ratio[jq >> 2];
+                tmem_st16(tl + C::kTmemO + 16 * jq, o);
+              }
+              tmem_st_wait();
+            }
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < NQ; ++c) {
+          const float mu = (m_ref[c] == -CUDART_INF_F) ? 0.f : m_ref[c];
+          s[c] = ex2(s[c] - mu + kPExp);
+          l_part[c] += s[c];
+        }
+        if (t > 0 && !pv_waited) {
+          w = warp_wait(&pv_done[(gt - 1) & 1], static_cast<uint32_t>((gt - 1) >> 1) & 1u, abort_flag);
+          tc_fence_after();
+        }
+        // P_j = p s_j r_j as four e5m2 terms (4 x 16 columns), 8 keys x 16 B core matrices
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float f = rv ? sj[j] * rj[j] : 0.f;
+          uint8_t* pj = ps + j * (kTile * 64) + (row >> 3) * 512 + (row & 7) * 16;
+          float a[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) a[c] = s[c] * f;
+#pragma unroll
+          for (int term = 0; term < 4; ++term) {
+            uint32_t wv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const uint32_t c01 = e5m2x2_sat(a[4 * u], a[4 * u + 1]), c23 = e5m2x2_sat(a[4 * u + 2], a[4 * u + 3]);
+              wv[u] = c01 | (c23 << 16);
+              if (term < 3) {
+                const float2 f01 = e5m2x2_to_float2(c01), f23 = e5m2x2_to_float2(c23);
+                a[4 * u] -= f01.x, a[4 * u + 1] -= f01.y, a[4 * u + 2] -= f23.x, a[4 * u + 3] -= f23.y;
+              }
+            }
+            *reinterpret_cast<uint4*>(pj + 128 * term) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+          }
+        }
+        // rows past the item or masked: their codes never reach PV (stale slot contents)
+        if (!rv) {
+#pragma unroll 1
+          for (int j = 0; j < 4; ++j) {
+            uint4* dst = reinterpret_cast<uint4*>(ring + ((gt & 1) * NB + j) * kSlotBytes + row * 128);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        ok = named_bar_and(1, NT, w);
+        if (!ok) break;
+        if (stid == 0) mbar_arrive(p_full);
+      }
+      if (!ok) break;
+      // ---- epilogue
+      w = true;
+      if (it.ntiles > 0) {
+        w = warp_wait(&pv_done[(g + it.ntiles - 1) & 1], static_cast<uint32_t>((g + it.ntiles - 1) >> 1) & 1u,
+                      abort_flag);
+        tc_fence_after();
+      }
+      g += it.ntiles;
+      {
+        const float lw = warp_col_reduce<NQ, false>(l_part, lane);
+        if (lane < 16) red_l[lane * 4 + quad] = lw;
+      }
+      ok = named_bar_and(1, NT, w);
+      if (!ok) break;
+      const int cl = lane % NQ;
+      float inv_l, lse_l;
+      {
+        const float4 q4 = reinterpret_cast<const float4*>(red_l)[cl];
+        const float l = (q4.x + q4.y) + (q4.z + q4.w);
+        float m_l = m_ref[0];
+#pragma unroll
+        for (int c = 1; c < NQ; ++c) m_l = (c == cl) ? m_ref[c] : m_l;
+        const bool live = l > 0.f;
+        inv_l = live ? __fdividef(1.f, l) : 0.f;
+        lse_l = live ? (m_l + __log2f(l) - kPExp) * 0.69314718055994531f : -CUDART_INF_F;
+      }
+      float inv[NQ];
+#pragma unroll
+      for (int c = 0; c < NQ; ++c) inv[c] = __shfl_sync(0xFFFFFFFFu, inv_l, c);
+      const bool final_out = (p.n_splits == 1);
+      const int64_t flat0 = static_cast<int64_t>(it.b) * p.q_len * p.H + cgb;
+      const int ncol = min(NQ, p.cols - cgb);
+      const int qi0 = cgb / p.H, h0 = cgb % p.H;
+#pragma unroll 1
+      for (int j = 0; j < 4; ++j) {
+        float o[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) o[c] = 0.f;
+        if (it.ntiles > 0) {
+#pragma unroll
+          for (int term = 0; term < 4; ++term) {
+            float ot[16];
+            tmem_ld16(tl + C::kTmemO + 64 * j + 16 * term, ot);
+            tmem_ld_wait();
+#pragma unroll
+            for (int c = 0; c < 16; ++c) o[c] += ot[c];
+          }
+        }
+        const float ur = (rj[j] > 0.f) ? 1.f / rj[j] : 0.f;     // exact: a power of two
+        const int d = 128 * j + row;
+        if (final_out) {
+          int qi = qi0, h = h0;
+          uint8_t* base = p.out + static_cast<int64_t>(it.b) * p.q_len * p.o_s0b + 2 * d;
+#pragma unroll
+          for (int c = 0; c < NQ; ++c) {
+            if (c < ncol)
+              *reinterpret_cast<__nv_bfloat16*>(base + qi * p.o_s0b + h * p.o_s1b) =
+                  __float2bfloat16_rn(o[c] * ur * inv[c]);
+            if (++h == p.H) {
+              h = 0;
+              ++qi;
+            }
+          }
+        } else {
+          float* dst = p.part_o + ((static_cast<int64_t>(it.s) * p.n_rows * p.H + flat0) * kLora + d);
+#pragma unroll
+          for (int c = 0; c < NQ; ++c)
+            if (c < ncol) dst[static_cast<int64_t>(c) * kLora] = o[c] * ur * inv[c];
+        }
+      }
+      if (row < 16 && cl < ncol) {
+        if (final_out) {
+          if (p.lse) p.lse[flat0 + cl] = lse_l;
+        } else {
+          p.part_lse[static_cast<int64_t>(it.s) * p.n_rows * p.H + flat0 + cl] = lse_l;
+        }
+      }
+      tc_fence_before();
+      named_bar_sync(1, NT);
+      if (stid == 0) mbar_arrive(&item_empty[k]);
+    }
+  } else {
+    // ------------------------------------------------------------------ gather (sparse)
+    // thread gi (0..255): record r = gi / 2 of the tile, half h = gi % 2 of its 41 16-byte
+    // chunks (0..31 codes, 32 scales, 33..40 k_pe)
+    const int gi = tid - 192;
+    const int r = gi >> 1, h = gi & 1;
+    const int c_lo = h ? 21 : 0, c_hi = h ? 41 : 21;
+    uint32_t errbits = 0;
+    int nit = 0, g = 0;
+    bool ok = true;
+    while (ok) {
+      const int k = nit % kItemDepth;
+      if (!warp_wait(&item_full[k], (nit / kItemDepth) & 1, abort_flag)) break;
+      const WorkItem it = items[k];
+      ++nit;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&item_empty[k]);
+      if (it.b < 0) break;
+      for (int t = 0; t < it.ntiles && ok; ++t) {
+        const int gt = g + t;
+        const int e = t * kTile + r;
+        bool valid = false;
+        const uint8_t* src = nullptr;
+        if (e < it.n) {
+          const int idx = p.indices[it.k0 + e];
+          if (idx >= 0 && idx < p.num_records) {
+            valid = true;
+            src = p.records + static_cast<int64_t>(idx) * p.rec_stride;
+          } else if (idx >= p.num_records || !p.has_invalid) {
+            errbits |= 1u;
+          }
+        }
+        uint4 v[21];
+#pragma unroll
+        for (int i = 0; i < 21; ++i) {
+          const int c = c_lo + i;
+          v[i] = (valid && c < c_hi) ? *reinterpret_cast<const uint4*>(src + 16 * c) : make_uint4(0, 0, 0, 0);
+        }
+        // tile gt reuses the slots of tile gt - 2
+        if (gt >= 2 && !warp_wait(&pv_done[gt & 1], static_cast<uint32_t>((gt - 2) >> 1) & 1u, abort_flag)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int i = 0; i < 21; ++i) {
+          const int c = c_lo + i;
+          if (c >= c_hi) continue;
+          if (c < 32) {
+            const int j = c >> 3, cc = c & 7;
+            *reinterpret_cast<uint4*>(ring + ((gt & 1) * NB + j) * kSlotBytes + sw128(r, cc)) = v[i];
+          } else if (c == 32) {
+            *reinterpret_cast<uint4*>(scl + (gt & 1) * kTile + r) = v[i];
+          } else {
+            *reinterpret_cast<uint4*>(ring + ((gt & 1) * NB + 4) * kSlotBytes + sw128(r, c - 33)) = v[i];
+          }
+        }
+        if (h == 0) vrow[(gt & 1) * kTile + r] = valid ? 1 : 0;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0)
+          for (int b = 0; b < NB; ++b) mbar_arrive(&full[(gt & 1) * NB + b]);
+      }
+      g += it.ntiles;
+    }
+    errbits = __reduce_or_sync(0xFFFFFFFFu, errbits);
+    if (lane == 0 && errbits) set_device_error(p.err, errbits);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0 && *abort_flag == 2) set_device_error(p.err, 16u);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::kTmemCols);
+  }
+}
+
+}  // namespace mla

@@ -71,6 +71,12 @@ cudaError_t launch_attn_paged_ds(const AttnParams& p, int grid, cudaStream_t str
 // 128-byte swizzle, box 128 B x BR x 1) and the query as [rows][H][row bytes] (box 128 B x
 // qbox_h x qbox_q).
 struct PagedParams;
+struct DsParams;
+// fp8_ds_mla attention: sparse records gathered by vector loads; paged records by TMA boxes
+// (`tkv` as above over the 656-byte record, `tsc` the same geometry unswizzled with 16-byte
+// boxes for the scales).
+cudaError_t launch_ds_sparse(const DsParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_ds_paged(const DsParams& p, const void* tkv, const void* tsc, int grid, cudaStream_t stream);
 cudaError_t launch_paged_tma_bf16(int nq, const PagedParams& p, const void* tkv, const void* tq, int grid,
                                   cudaStream_t stream);
 cudaError_t launch_paged_tma_fp8(int nq, const PagedParams& p, const void* tkv, const void* tq, int grid,
