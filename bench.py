@@ -30,6 +30,13 @@ sys.path.insert(0, ROOT)
 
 METRIC = "MLA attention achieved HBM GB/s (% of GB300 peak); query-rows/s at 1 GPU"
 WORKLOADS = ("decode_bf16_epilogue", "sparse_prefill", "fp8_spec_verify", "ds_mla_h96_decode")
+# the attention kernel each workload times (the profiling hook brackets exactly its launch)
+KERNELS = {
+    "decode_bf16_epilogue": "mla_paged_tma_kernel<bf16, 16 columns>",
+    "sparse_prefill": "mla_attn_kernel<fp8_ds_mla, sparse> (staged converters)",
+    "fp8_spec_verify": "mla_paged_tma_kernel<fp8, 64 columns>",
+    "ds_mla_h96_decode": "mla_ds_kernel<paged>",
+}
 
 
 def peaks():
@@ -46,21 +53,24 @@ def peaks():
 class Work:
     """Host inputs of one workload plus its byte / row accounting."""
 
-    def __init__(self, name: str):
+    def __init__(self, name: str, batch: int = 0):
         from mla_latent_cache_attention_gb300 import synth
         self.name = name
         self.synth = synth
+        # batch > 0 keeps the workload's geometry with fewer requests (profiling captures that
+        # must stay small); bench lines use the full workload
+        kw = dict(B=batch) if batch > 0 else {}
         if name == "decode_bf16_epilogue":
-            self.case, self.epi = synth.config1()
+            self.case, self.epi = synth.config1(**kw)
             self.kind = "paged"
         elif name == "sparse_prefill":
-            self.case = synth.config2()
+            self.case = synth.config2(**(dict(T=batch) if batch > 0 else {}))
             self.kind = "sparse"
         elif name == "fp8_spec_verify":
-            self.case = synth.config3()
+            self.case = synth.config3(**kw)
             self.kind = "paged"
         elif name == "ds_mla_h96_decode":
-            self.case = synth.config4()
+            self.case = synth.config4(**kw)
             self.kind = "paged"
         else:
             raise SystemExit(f"unknown workload {name}")
@@ -238,7 +248,7 @@ def run_native(args, rank, world, dist):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     m.lib()
-    w = Work(args.workload)
+    w = Work(args.workload, args.batch)
     r = GpuRunner(w, dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):
@@ -306,7 +316,7 @@ def run_native(args, rank, world, dist):
         "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": prof, "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": "mla_attn_kernel (attention only; epilogue and merge outside)",
+                     "kernel": KERNELS[args.workload] + " (attention only; epilogue and merge outside)",
                      "kernel_ms": round(attn_avg, 5), "bytes_per_launch": w.attn_bytes},
         "e2e": {"value": round(world * w.step_bytes * K / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(r.h2d), "d2h_bytes_per_step": int(r.d2h)},
@@ -379,7 +389,7 @@ def cpu_baseline(w: Work, budget_s: float = 15.0):
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    w = Work(args.workload)
+    w = Work(args.workload, args.batch)
     budget = max(1.0, args.cpu_seconds / max(1, args.steps))
     vals, rows, secs = [], 0, 0.0
     for _ in range(args.warmup if args.warmup < 1 else 1):
@@ -409,6 +419,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default="decode_bf16_epilogue", choices=WORKLOADS)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="requests (query rows for sparse_prefill) instead of the workload's own; for small profiling captures")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()

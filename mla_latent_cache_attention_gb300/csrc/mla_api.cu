@@ -150,9 +150,9 @@ std::mutex g_tmap_mu;
 // Rows per TMA box for a block size, or 0 when the page kernel does not serve it: the box
 // rows must divide the 128-key tile (block_size 16..128 a power of two) or be a whole
 // 128-row slice of a larger block.
-int tma_rows_for(int block_size) {
-  if (block_size >= 128) return (block_size % 128 == 0) ? 128 : 0;
-  if (block_size >= 16 && (128 % block_size) == 0) return block_size;
+int tma_rows_for(int block_size, int keys_per_tile = 128) {
+  if (block_size >= keys_per_tile) return (block_size % keys_per_tile == 0) ? keys_per_tile : 0;
+  if (block_size >= 16 && (keys_per_tile % block_size) == 0) return block_size;
   return 0;
 }
 
@@ -324,6 +324,7 @@ extern "C" int mla_q_concat_cache_insert(const void* ql_nope, int64_t ql_s0, int
   p.cos_sin = cos_sin_cache;
   p.max_position = max_position;
   p.H = H;
+  p.vec16 = aligned(ql_nope, 16) && aligned(mqa_q, 16) && ql_s0 % 8 == 0 && ql_s1 % 8 == 0;
   p.err = d->err;
   if (launch_epilogue(static_cast<int>(fmt), p, B, stream) != cudaSuccess)
     return fail(MLA_ERR_CUDA, "epilogue launch failed: %s", cudaGetErrorString(cudaGetLastError()));
@@ -553,8 +554,11 @@ extern "C" int mla_paged_decode(const void* q, int64_t q_s0, int64_t q_s1, const
     return ok();
   }
   const bool tma_fmt = fmt != MLA_CACHE_FP8_DS_MLA;
+  // keys per tile of the page kernel (a template choice; 128 for both formats, measured
+  // faster than 64-key tiles for bf16 despite the deeper ring those allow)
+  const int tma_rows_p = tma_rows_for(block_size, 128);
   ColPlan cp{};
-  const bool use_tma = tma_fmt && tma_rows > 0 && plan_columns(static_cast<int>(fmt), H, q_len, &cp) && aligned(q, 16) &&
+  const bool use_tma = tma_fmt && tma_rows_p > 0 && plan_columns(static_cast<int>(fmt), H, q_len, &cp) && aligned(q, 16) &&
                        (q_s0 * qe) % 16 == 0 && (q_s1 * qe) % 16 == 0 && num_blocks < (int64_t(1) << 31) &&
                        max_context < (1 << 30);
   cudaError_t e;
@@ -565,7 +569,7 @@ extern "C" int mla_paged_decode(const void* q, int64_t q_s0, int64_t q_s1, const
     const uint64_t kd[3] = {static_cast<uint64_t>(entry_bytes(fmt)), static_cast<uint64_t>(block_size),
                             static_cast<uint64_t>(num_blocks)};
     const uint64_t ks[2] = {static_cast<uint64_t>(entry_stride_bytes), static_cast<uint64_t>(block_stride_bytes)};
-    const uint32_t kb[3] = {128, static_cast<uint32_t>(tma_rows), 1};
+    const uint32_t kb[3] = {128, static_cast<uint32_t>(tma_rows_p), 1};
     if (int rc = tmap_3d(kv_cache, kd, ks, kb, &tkv)) return rc;
     const uint64_t qd[3] = {static_cast<uint64_t>(576 * qe), static_cast<uint64_t>(H), static_cast<uint64_t>(n_rows)};
     const uint64_t qs[2] = {static_cast<uint64_t>(q_s1 * qe), static_cast<uint64_t>(q_s0 * qe)};
@@ -584,7 +588,7 @@ extern "C" int mla_paged_decode(const void* q, int64_t q_s0, int64_t q_s1, const
     p.seq_lens = seq_lens;
     p.num_blocks = static_cast<int>(num_blocks);
     p.block_size = block_size;
-    p.BR = tma_rows;
+    p.BR = tma_rows_p;
     p.chunk = static_cast<int>(sp.chunk);
     p.n_splits = sp.n_splits;
     p.n_items = static_cast<int>(items);

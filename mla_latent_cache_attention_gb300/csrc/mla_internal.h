@@ -28,6 +28,7 @@ struct EpiParams {
   const float* cos_sin;
   int64_t max_position;
   int H;
+  int vec16;               // ql_nope rows and mqa_q 16-byte aligned (vector copies)
   uint32_t* err;
 };
 

@@ -83,26 +83,29 @@ struct WorkItem {
 constexpr int kItemDepth = 4;
 constexpr int kSlotBytes = kTile * 128;
 
-template <int F, int NQ>
+template <int F, int NQ, int KM>
 struct PagedCfg {
   static_assert(F == kBF16 || F == kFP8, "format");
   static_assert(NQ == 16 || NQ == 32 || NQ == 64, "columns per item");
+  static_assert(KM == 64 || KM == 128, "keys per tile");
+  static constexpr int kM = KM;                           // keys per tile (QK MMA M)
+  static constexpr int kSlot = KM * 128;                  // one ring slot: KM rows of 128 B
   static constexpr int kNB = F == kBF16 ? 10 : 5;        // ring positions per tile (bf16: 9 blocks + 1 pad)
   static constexpr int kNBQ = F == kBF16 ? 9 : 5;        // query blocks
   static constexpr int kRope = F == kBF16 ? 8 : 4;       // block used by QK only
   static constexpr int kSW = NQ == 64 ? 8 : 4;           // softmax warps
   static constexpr int kNC = NQ * 4 / kSW;               // columns per softmax thread
   static constexpr int kThreads = 64 + 32 * kSW;
-  static constexpr bool kOverlap = (F == kFP8) && MLA_OVERLAP_FP8;
+  static constexpr bool kOverlap = (F == kFP8 || KM == 64) && MLA_OVERLAP_FP8;
   static constexpr int kPfDist = MLA_LOOKAHEAD;           // tiles between a page lookup and its use
   static constexpr bool kL2Pf = MLA_L2PF;
   static constexpr bool kSlotCommits = MLA_SLOT_COMMITS;
   static constexpr int kQBytes = kNBQ * NQ * 128;
-  static constexpr int kPBytes = F == kBF16 ? kTile * NQ * 2 : 2 * kTile * NQ;
+  static constexpr int kPBytes = F == kBF16 ? KM * NQ * 2 : 2 * KM * NQ;
   static constexpr int kRedBytes = 3 * NQ * 4 * 4;       // max partials [2][NQ][4], sum partials [NQ][4]
   static constexpr int kFixed = kQBytes + kPBytes + kRedBytes + kItemDepth * 32 + 8 * (9 + 2 * kItemDepth) + 64;
   static constexpr int ring_slots() {
-    int r = (kSmemLimit - 1024 - kFixed) / (kSlotBytes + 16);
+    int r = (kSmemLimit - 1024 - kFixed) / (kSlot + 16);
     if (F == kBF16 && (r & 1)) --r;                      // V pairs never wrap the ring
     return r;
   }
@@ -110,7 +113,7 @@ struct PagedCfg {
   static_assert(kR >= 2 * kNB || (!kOverlap && kR >= kNB), "ring too small");
   static_assert(!kOverlap || kR >= 2 * kNB, "overlap needs two tiles in the ring");
   static constexpr int kRing = 0;
-  static constexpr int kQ = kRing + kR * kSlotBytes;
+  static constexpr int kQ = kRing + kR * kSlot;
   static constexpr int kP = kQ + kQBytes;
   static constexpr int kRed = kP + kPBytes;
   static constexpr int kItems = kRed + kRedBytes;
@@ -222,11 +225,11 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t v) {
   return __half22float2(*reinterpret_cast<const __half2*>(&h));
 }
 
-template <int F, int NQ>
-__global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
+template <int F, int NQ, int KM>
+__global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
     mla_paged_tma_kernel(const __grid_constant__ PagedParams p, const __grid_constant__ CUtensorMap tm_kv,
                          const __grid_constant__ CUtensorMap tm_q) {
-  using C = PagedCfg<F, NQ>;
+  using C = PagedCfg<F, NQ, KM>;
   constexpr int R = C::kR, NB = C::kNB, NC = C::kNC;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -289,7 +292,7 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer
-    const int NPG = kTile / p.BR;
+    const int NPG = KM / p.BR;
     uint32_t errbits = 0;
     int64_t pos = 0;   // ring positions issued
     int nitem = 0, nq = 0, stride_k = 0;
@@ -315,7 +318,7 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
       it.L = max(p.seq_lens[it.b], 0);
       it.k0 = it.s * p.chunk;
       it.n = min(max(it.L - it.k0, 0), p.chunk);
-      it.ntiles = (it.n + kTile - 1) / kTile;
+      it.ntiles = (it.n + KM - 1) / KM;
       it.pad = 0;
       return it.n > 0 || p.n_splits == 1;
     };
@@ -328,7 +331,7 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
     // checked late so that its latency hides behind the copies in flight
     auto page_raw = [&](const WorkItem& it, int t, int q) -> int {
       if (it.b < 0 || t >= it.ntiles) return -2;
-      const int kp = it.k0 + t * kTile + q * p.BR;
+      const int kp = it.k0 + t * KM + q * p.BR;
       if (kp >= it.k0 + it.n) return -1;
       return p.block_table[static_cast<int64_t>(it.b) * p.bt_stride + kp / p.block_size];
     };
@@ -339,7 +342,7 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
         errbits |= 2u;
         return p.num_blocks;
       }
-      y = (it.k0 + t * kTile + q * p.BR) % p.block_size;
+      y = (it.k0 + t * KM + q * p.BR) % p.block_size;
       return raw;
     };
     constexpr int D = C::kPfDist;
@@ -431,14 +434,14 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
             if (lane == 0) mbar_arrive(&full[slot]);
             continue;
           }
-          if (lane == 0) mbar_arrive_expect_tx(&full[slot], kSlotBytes);
+          if (lane == 0) mbar_arrive_expect_tx(&full[slot], C::kSlot);
           if (lane == 0 && (b == 0 || b == NB - 1)) TL(0, (b == 0 ? 1000 : 3000) + static_cast<int>((pos / NB) % 1000));
           __syncwarp();
           const int x = (F == kFP8 && b == 4) ? 448 : 128 * b;
           for (int q = 0; q < NPG; ++q) {
             const int z = __shfl_sync(0xFFFFFFFFu, blk, q);
             const int yy = __shfl_sync(0xFFFFFFFFu, y, q);
-            if (lane == 0) tma_load_3d(ring + slot * kSlotBytes + q * p.BR * 128, &tm_kv, x, yy, z, &full[slot]);
+            if (lane == 0) tma_load_3d(ring + slot * C::kSlot + q * p.BR * 128, &tm_kv, x, yy, z, &full[slot]);
           }
         }
         // finish the lookahead: queue its pages (and prefetch them into L2)
@@ -494,10 +497,10 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
       const uint32_t ring_a = smem_u32(ring), q_a = smem_u32(qs), p_a = smem_u32(ps);
       const uint64_t dK0 = smem_desc(ring_a, 16, 1024, kSwizzle128B);
       const uint64_t dQ0 = smem_desc(q_a, 16, 1024, kSwizzle128B);
-      const uint64_t dV0 = smem_desc(ring_a, kSlotBytes, 1024, kSwizzle128B);
+      const uint64_t dV0 = smem_desc(ring_a, C::kSlot, 1024, kSwizzle128B);
       constexpr uint32_t kPLbo = F == kBF16 ? NQ * 16 : NQ * 8;   // 8-key groups of P
       const uint64_t dP0 = smem_desc(p_a, kPLbo, 128, kSwizzleNone);
-      constexpr uint32_t kIdQk = F == kBF16 ? idesc_f16(128, NQ, 1, 1, 0, 0) : idesc_e4m3(128, NQ, 0, 0);
+      constexpr uint32_t kIdQk = F == kBF16 ? idesc_f16(KM, NQ, 1, 1, 0, 0) : idesc_e4m3(KM, NQ, 0, 0);
       constexpr uint32_t kIdPv = F == kBF16 ? idesc_f16(128, NQ, 1, 1, 1, 1) : idesc_e4m3(128, NQ, 1, 1);
       auto slot_of = [&](int gt, int b) -> int { return static_cast<int>((static_cast<int64_t>(gt) * NB + b) % R); };
       auto use_of = [&](int gt, int b) -> uint32_t {
@@ -514,21 +517,21 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
         for (int j = 0; j < 4; ++j) {
           const uint32_t dO = tmem + C::kTmemO + j * NQ;
           if (F == kBF16) {
-            const uint64_t aV = dV0 + ((slot_of(gt, 2 * j) * kSlotBytes) >> 4);
+            const uint64_t aV = dV0 + ((slot_of(gt, 2 * j) * C::kSlot) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
+            for (int kk = 0; kk < KM / 16; ++kk)
               mma_f16_ss(dO, aV + ((kk * 2048) >> 4), dP0 + ((kk * NQ * 32) >> 4), kIdPv, (!first || kk > 0) ? 1u : 0u);
             if (C::kSlotCommits) {
               mma_commit(&empty[slot_of(gt, 2 * j)]);
               mma_commit(&empty[slot_of(gt, 2 * j + 1)]);
             }
           } else {
-            const uint64_t aV = dV0 + ((slot_of(gt, j) * kSlotBytes) >> 4);
+            const uint64_t aV = dV0 + ((slot_of(gt, j) * C::kSlot) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
+            for (int kk = 0; kk < KM / 32; ++kk) {
               const uint64_t pb = dP0 + ((kk * NQ * 32) >> 4);
               mma_f8_ss(dO, aV + ((kk * 4096) >> 4), pb, kIdPv, (!first || kk > 0) ? 1u : 0u);
-              mma_f8_ss(dO, aV + ((kk * 4096) >> 4), pb + ((kTile * NQ) >> 4), kIdPv, 1u);
+              mma_f8_ss(dO, aV + ((kk * 4096) >> 4), pb + ((KM * NQ) >> 4), kIdPv, 1u);
             }
             if (C::kSlotCommits) mma_commit(&empty[slot_of(gt, j)]);
           }
@@ -559,7 +562,7 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
             if (C::kSlotCommits) mbar_arrive(&empty[slot]);
             continue;
           }
-          const uint64_t aK = dK0 + ((slot * kSlotBytes) >> 4);
+          const uint64_t aK = dK0 + ((slot * C::kSlot) >> 4);
           const uint64_t bQ = dQ0 + ((b * NQ * 128) >> 4);
           if (F == kBF16) {
 #pragma unroll
@@ -622,7 +625,11 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
     const int sw = warp - 2;
     const int quad = warp & 3;                  // TMEM lane quadrant of this warp
     const int c0 = (sw >> 2) * NC;              // first column of this thread
-    const int row = quad * 32 + lane;           // key row of the tile / TMEM lane
+    const int row = quad * 32 + lane;           // TMEM lane: output column d of O^T
+    // key row of the tile: with 64-key tiles (M = 64) the S accumulator holds key 16 q + i in
+    // lane 32 q + i of quadrant q, and lanes 16..31 of each quadrant carry nothing
+    const bool klane = (KM == 128) || (lane < 16);
+    const int krow = (KM == 128) ? row : quad * 16 + lane;
     const int stid = tid - 64;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     float* red_m = red;                         // [2][NQ][4]
@@ -652,8 +659,8 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
       auto load_s = [&](float (&s)[NC], int gt, int t) {
         tmem_ld_n<NC>(tl + C::kTmemS + (gt & 1) * NQ + c0, s);
         tmem_ld_wait();
-        const int kpos = it.k0 + t * kTile + row;
-        const bool rv = kpos < it.k0 + it.n;
+        const int kpos = it.k0 + t * KM + krow;
+        const bool rv = klane && kpos < it.k0 + it.n;
 #pragma unroll
         for (int c = 0; c < NC; ++c) s[c] = rv ? s[c] * p.sig2 : -CUDART_INF_F;
         // spec-verify: query token qi sees keys up to L - q_len + qi
@@ -671,13 +678,13 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
         if (stid == 0) TL(3, 1);
         float s[NC];
         load_s(s, gt, t);
-        const bool rv = it.k0 + t * kTile + row < it.k0 + it.n;
+        const bool rv = klane && it.k0 + t * KM + krow < it.k0 + it.n;
         // rows past the item never reach PV with stale contents
-        if (!rv && c0 == 0) {
+        if (!rv && klane && c0 == 0) {
 #pragma unroll 1
           for (int b = 0; b < (F == kBF16 ? 8 : 4); ++b) {
             uint4* dst = reinterpret_cast<uint4*>(
-                ring + static_cast<int>((static_cast<int64_t>(gt) * NB + b) % R) * kSlotBytes + row * 128);
+                ring + static_cast<int>((static_cast<int64_t>(gt) * NB + b) % R) * C::kSlot + krow * 128);
 #pragma unroll
             for (int i = 0; i < 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
           }
@@ -757,7 +764,7 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
             v.y = pack2(s[c + 2], s[c + 3], true);
             v.z = pack2(s[c + 4], s[c + 5], true);
             v.w = pack2(s[c + 6], s[c + 7], true);
-            *reinterpret_cast<uint4*>(ps + (row >> 3) * (NQ * 16) + (row & 7) * 16 + ((c0 + c) >> 3) * 128) = v;
+            if (klane) *reinterpret_cast<uint4*>(ps + (krow >> 3) * (NQ * 16) + (krow & 7) * 16 + ((c0 + c) >> 3) * 128) = v;
           }
         } else {
           // 8 keys x 16 columns core matrices, 8-key groups NQ*8 bytes apart; hi then lo
@@ -773,9 +780,11 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
               hw[u] = h01 | (h23 << 16);
               lw[u] = l01 | (l23 << 16);
             }
-            const int off = (row >> 3) * (NQ * 8) + (row & 7) * 16 + ((c0 + c) >> 4) * 128;
-            *reinterpret_cast<uint4*>(ps + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            *reinterpret_cast<uint4*>(ps + kTile * NQ + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            const int off = (krow >> 3) * (NQ * 8) + (krow & 7) * 16 + ((c0 + c) >> 4) * 128;
+            if (klane) {
+              *reinterpret_cast<uint4*>(ps + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+              *reinterpret_cast<uint4*>(ps + KM * NQ + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
           }
         }
         fence_proxy_async_smem();

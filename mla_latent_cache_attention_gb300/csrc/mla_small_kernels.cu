@@ -74,10 +74,24 @@ __global__ void __launch_bounds__(128) mla_epilogue_kernel(const EpiParams p) {
   for (int i = tid; i < (h_hi - h_lo) * 64; i += blockDim.x) {
     const int h = h_lo + (i >> 6), d0 = (i & 63) * 8;
     const uint16_t* src = qn + b * p.ql_s0 + h * p.ql_s1 + d0;
-    uint16_t v[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = __ldg(src + e);
     const int64_t o = (static_cast<int64_t>(b) * H + h) * 576 + d0;
+    uint16_t v[8];
+    if (p.vec16) {       // 16-byte aligned rows: one vector load (and store for 16-bit outputs)
+      const uint4 w = __ldg(reinterpret_cast<const uint4*>(src));
+      if (F != 1) {
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.mqa_q) + o) = w;
+        continue;
+      }
+      const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[2 * e] = static_cast<uint16_t>(ww[e] & 0xFFFFu);
+        v[2 * e + 1] = static_cast<uint16_t>(ww[e] >> 16);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = __ldg(src + e);
+    }
     if (F == 1) {
       uint8_t* __restrict__ q8 = reinterpret_cast<uint8_t*>(p.mqa_q) + o;
 #pragma unroll
@@ -172,30 +186,66 @@ __global__ void __launch_bounds__(128) mla_merge_kernel(const MergeParams p) {
     const int64_t L = max(p.seq_lens[row / p.q_len], 0);
     S = static_cast<int>(min(static_cast<int64_t>(S), (L + p.chunk - 1) / p.chunk));
   }
+  // the split weights exp(lse_s - max) are formed once, with the LSEs loaded in parallel
+  __shared__ float wsh[128];
+  __shared__ float red[2][4];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   float m = -CUDART_INF_F;
-  for (int s = 0; s < S; ++s) m = fmaxf(m, p.part_lse[s * stride + rh]);
+  for (int s = tid; s < S; s += 128) m = fmaxf(m, p.part_lse[s * stride + rh]);
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if (lane == 0) red[0][warp] = m;
+  __syncthreads();
+  m = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
+  float ws = 0.f;
+  for (int s = tid; s < S; s += 128) {
+    const float ls = p.part_lse[s * stride + rh];
+    const float w = (m == -CUDART_INF_F || ls == -CUDART_INF_F) ? 0.f : expf(ls - m);
+    if (s < 128) wsh[s] = w;
+    ws += w;
+  }
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) ws += __shfl_xor_sync(0xFFFFFFFFu, ws, o);
+  if (lane == 0) red[1][warp] = ws;
+  __syncthreads();
+  const float wsum = (red[1][0] + red[1][1]) + (red[1][2] + red[1][3]);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float wsum = 0.f;
-  if (m != -CUDART_INF_F) {
-    for (int s = 0; s < S; ++s) {
-      const float ls = p.part_lse[s * stride + rh];
-      if (ls == -CUDART_INF_F) continue;
-      const float w = expf(ls - m);
-      wsum += w;
-      const float4 o = reinterpret_cast<const float4*>(p.part_o + (s * stride + rh) * 512)[threadIdx.x];
-      acc.x += w * o.x;
-      acc.y += w * o.y;
-      acc.z += w * o.z;
-      acc.w += w * o.w;
+  const float4* po = reinterpret_cast<const float4*>(p.part_o + rh * 512) + tid;
+  const int64_t step4 = stride * 128;      // one split, in float4
+  int s = 0;
+  for (; s + 4 <= S; s += 4) {             // four independent loads in flight
+    float w4[4];
+    float4 o4[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int ss = s + u;
+      w4[u] = ss < 128 ? wsh[ss] : expf(p.part_lse[ss * stride + rh] - m);
+      o4[u] = w4[u] != 0.f ? po[ss * step4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      acc.x += w4[u] * o4[u].x;
+      acc.y += w4[u] * o4[u].y;
+      acc.z += w4[u] * o4[u].z;
+      acc.w += w4[u] * o4[u].w;
     }
   }
+  for (; s < S; ++s) {
+    const float w = s < 128 ? wsh[s] : expf(p.part_lse[s * stride + rh] - m);
+    if (w == 0.f) continue;
+    const float4 o = po[s * step4];
+    acc.x += w * o.x;
+    acc.y += w * o.y;
+    acc.z += w * o.z;
+    acc.w += w * o.w;
+  }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-  __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out + row * p.o_s0b + h * p.o_s1b) + 4 * threadIdx.x;
+  __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out + row * p.o_s0b + h * p.o_s1b) + 4 * tid;
   dst[0] = __float2bfloat16_rn(acc.x * inv);
   dst[1] = __float2bfloat16_rn(acc.y * inv);
   dst[2] = __float2bfloat16_rn(acc.z * inv);
   dst[3] = __float2bfloat16_rn(acc.w * inv);
-  if (threadIdx.x == 0 && p.lse) p.lse[rh] = wsum > 0.f ? m + logf(wsum) : -CUDART_INF_F;
+  if (tid == 0 && p.lse) p.lse[rh] = wsum > 0.f ? m + logf(wsum) : -CUDART_INF_F;
 }
 
 // ------------------------------------------------------------------------------------------
