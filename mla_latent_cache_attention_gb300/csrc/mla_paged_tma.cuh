@@ -102,7 +102,7 @@ struct PagedCfg {
   static constexpr bool kSlotCommits = MLA_SLOT_COMMITS;
   static constexpr int kQBytes = kNBQ * NQ * 128;
   static constexpr int kPBytes = F == kBF16 ? KM * NQ * 2 : 2 * KM * NQ;
-  static constexpr int kRedBytes = 3 * NQ * 4 * 4;       // max partials [2][NQ][4], sum partials [NQ][4]
+  static constexpr int kRedBytes = 3 * NQ * 4 * 4 + 2 * NQ * 4;   // max / sum partials, reference max, rescale
   static constexpr int kFixed = kQBytes + kPBytes + kRedBytes + kItemDepth * 32 + 8 * (9 + 2 * kItemDepth) + 64;
   static constexpr int ring_slots() {
     int r = (kSmemLimit - 1024 - kFixed) / (kSlot + 16);
@@ -634,6 +634,10 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     float* red_m = red;                         // [2][NQ][4]
     float* red_l = red + 2 * NQ * 4;            // [NQ][4]
+    // the reference max of every column (the same for all threads of a column half) lives in
+    // shared memory rather than in 32 registers per thread; so does a rescale's factor
+    float* mref = red + 3 * NQ * 4;             // [NQ]
+    float* alph = mref + NQ;                    // [NQ]
     constexpr float kTau = F == kFP8 ? 4.f : 8.f;
     // row sums: per thread and column when registers allow (6 warps), else per warp and
     // column (lane % NC), reduced over the warp each tile
@@ -647,11 +651,10 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
       bool w = warp_wait(&item_full[k], (nit / kItemDepth) & 1, abort_flag);
       const WorkItem it = items[k];
       ++nit;
+      if (quad == 0 && (NC == 32 || lane < 16)) mref[c0 + (lane % NC)] = -CUDART_INF_F;
       if (!named_bar_and(1, NT, w)) break;
       if (it.b < 0) break;
-      float m_ref[NC], l_part[NL];
-#pragma unroll
-      for (int c = 0; c < NC; ++c) m_ref[c] = -CUDART_INF_F;
+      float l_part[NL];
 #pragma unroll
       for (int c = 0; c < NL; ++c) l_part[c] = 0.f;
       const int cgb = it.g * NQ + c0;           // global column of this thread's column 0
@@ -691,7 +694,13 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
         }
         bool need = false;
 #pragma unroll
-        for (int c = 0; c < NC; ++c) need |= (s[c] > m_ref[c] + kTau) || (m_ref[c] == -CUDART_INF_F && s[c] > -CUDART_INF_F);
+        for (int c = 0; c < NC; c += 4) {
+          const float4 m4 = *reinterpret_cast<const float4*>(mref + c0 + c);
+          const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            need |= (s[c + u] > mm[u] + kTau) | ((mm[u] == -CUDART_INF_F) & (s[c + u] > -CUDART_INF_F));
+        }
         if (stid == 0) TL(3, 10);
         // one barrier decides: nothing to do (common), or move the reference (or abort)
         const bool rare = named_bar_or(1, NT, need || !w);
@@ -710,18 +719,22 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
             const float4 q4 = reinterpret_cast<const float4*>(rb)[c0 + (lane % NC)];
             mt_l = fmaxf(fmaxf(q4.x, q4.y), fmaxf(q4.z, q4.w));
           }
-          bool resc = false;
+          // column (lane % NC): new reference and its factor, published once all have read the old
+          const float mo_l = mref[c0 + (lane % NC)];
+          const float mn_l = fmaxf(mo_l, mt_l);
+          const float alpha_lane = (mo_l == -CUDART_INF_F) ? 0.f : ex2(mo_l - mn_l);
+          const bool resc = __any_sync(0xFFFFFFFFu, mn_l != mo_l);
+          named_bar_sync(1, NT);
+          if (quad == 0 && (NC == 32 || lane < 16)) {
+            mref[c0 + (lane % NC)] = mn_l;
+            alph[c0 + (lane % NC)] = alpha_lane;
+          }
+          named_bar_sync(1, NT);
           float alpha[NC];
-          float alpha_lane = 1.f;
 #pragma unroll
           for (int c = 0; c < NC; ++c) {
-            const float mo = m_ref[c];
-            const float mn = fmaxf(mo, __shfl_sync(0xFFFFFFFFu, mt_l, c));
-            alpha[c] = (mo == -CUDART_INF_F) ? 0.f : ex2(mo - mn);
-            resc |= (mn != mo);
-            m_ref[c] = mn;
+            alpha[c] = alph[c0 + c];
             if (kLReg) l_part[kLReg ? c : 0] *= alpha[c];
-            alpha_lane = (c == (lane % NC)) ? alpha[c] : alpha_lane;
           }
           if (!kLReg) l_part[0] *= alpha_lane;
           // O of the previous tiles moves to the new reference once PV of the last tile is done
@@ -746,7 +759,8 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
         }
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-          const float mu = (m_ref[c] == -CUDART_INF_F) ? 0.f : m_ref[c];
+          const float mr = mref[c0 + c];
+          const float mu = (mr == -CUDART_INF_F) ? 0.f : mr;
           s[c] = ex2(s[c] - mu + kPExp);
           if (kLReg) l_part[kLReg ? c : 0] += s[c];
         }
@@ -818,50 +832,49 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
       {
         const float4 q4 = reinterpret_cast<const float4*>(red_l)[c0 + cl];
         const float l = (q4.x + q4.y) + (q4.z + q4.w);
-        float m_l = m_ref[0];
-#pragma unroll
-        for (int c = 1; c < NC; ++c) m_l = (c == cl) ? m_ref[c] : m_l;
+        const float m_l = mref[c0 + cl];
         const bool live = l > 0.f;
         inv_l = live ? __fdividef(p.out_scale, l) : 0.f;
         lse_l = live ? (m_l + __log2f(l) - kPExp) * 0.69314718055994531f : -CUDART_INF_F;
       }
-      float inv[NC];
-#pragma unroll
-      for (int c = 0; c < NC; ++c) inv[c] = __shfl_sync(0xFFFFFFFFu, inv_l, c);
       const bool final_out = (p.n_splits == 1);
       // (row, head) of column cg: row = b * q_len + cg / H, head = cg % H, so the flat index
       // row * H + head is b * q_len * H + cg
       const int64_t flat0 = static_cast<int64_t>(it.b) * p.q_len * p.H + cgb;
       const int ncol = min(NC, p.cols - cgb);
-      const int qi0 = cgb / p.H, h0 = cgb % p.H;
+      // O / l in slices of 16 columns (keeps the epilogue's live registers low)
 #pragma unroll 1
-      for (int j = 0; j < 4; ++j) {
-        float o[NC];
+      for (int jq = 0; jq < 4 * (NC / 16); ++jq) {
+        const int j = jq / (NC / 16), cs = 16 * (jq % (NC / 16));
+        float o[16];
         if (it.ntiles > 0) {
-          tmem_ld_n<NC>(tl + C::kTmemO + j * NQ + c0, o);
+          tmem_ld16(tl + C::kTmemO + j * NQ + c0 + cs, o);
           tmem_ld_wait();
         } else {
 #pragma unroll
-          for (int c = 0; c < NC; ++c) o[c] = 0.f;
+          for (int c = 0; c < 16; ++c) o[c] = 0.f;
         }
         const int d = 128 * j + row;
         if (final_out) {
-          int qi = qi0, h = h0;
+          int qi = (cgb + cs) / p.H, h = (cgb + cs) % p.H;
           uint8_t* base = p.out + static_cast<int64_t>(it.b) * p.q_len * p.o_s0b + 2 * d;
 #pragma unroll
-          for (int c = 0; c < NC; ++c) {
-            if (c < ncol)
-              *reinterpret_cast<__nv_bfloat16*>(base + qi * p.o_s0b + h * p.o_s1b) = __float2bfloat16_rn(o[c] * inv[c]);
+          for (int c = 0; c < 16; ++c) {
+            const float iv = __shfl_sync(0xFFFFFFFFu, inv_l, cs + c);
+            if (cs + c < ncol)
+              *reinterpret_cast<__nv_bfloat16*>(base + qi * p.o_s0b + h * p.o_s1b) = __float2bfloat16_rn(o[c] * iv);
             if (++h == p.H) {
               h = 0;
               ++qi;
             }
           }
         } else {
-          float* dst = p.part_o + ((static_cast<int64_t>(it.s) * p.n_rows * p.H + flat0) * kLora + d);
+          float* dst = p.part_o + ((static_cast<int64_t>(it.s) * p.n_rows * p.H + flat0 + cs) * kLora + d);
 #pragma unroll
-          for (int c = 0; c < NC; ++c)
-            if (c < ncol) dst[static_cast<int64_t>(c) * kLora] = o[c] * inv[c];
+          for (int c = 0; c < 16; ++c) {
+            const float iv = __shfl_sync(0xFFFFFFFFu, inv_l, cs + c);
+            if (cs + c < ncol) dst[static_cast<int64_t>(c) * kLora] = o[c] * iv;
+          }
         }
       }
       if (row < 32 && (NC == 32 || lane < 16) && cl < ncol) {
