@@ -400,6 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   TL_DECL;
 
+  // the split-K merge may be scheduled now; it waits for this grid to complete
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(&full[s], 1);

@@ -140,6 +140,8 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   TL_DECL;
 
+  // the split-K merge may be scheduled now; it waits for this grid to complete
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (tid == 0) {
     for (int i = 0; i < R; ++i) mbar_init(&full[i], kSparse ? C::kGatherWarps : 1);
     for (int i = 0; i < 2; ++i) {

@@ -45,7 +45,7 @@
 #define MLA_OVERLAP_FP8 1
 #endif
 #ifndef MLA_LOOKAHEAD
-#define MLA_LOOKAHEAD 2
+#define MLA_LOOKAHEAD 1
 #endif
 #ifndef MLA_L2PF
 #define MLA_L2PF 1
@@ -258,6 +258,8 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   TL_DECL;
 
+  // the split-K merge may be scheduled now; it waits for this grid to complete
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // query rows that no box writes stay zero
   for (int i = tid; i < C::kQBytes / 16; i += C::kThreads)
     reinterpret_cast<uint4*>(qs)[i] = make_uint4(0, 0, 0, 0);
@@ -550,10 +552,18 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
 #pragma unroll 1
         for (int b = 0; b < NB; ++b) {
           const int slot = slot_of(gt, b);
-          if (pv_gt >= 0 && !mbar_test_wait(&full[slot], use_of(gt, b)) &&
-              mbar_test_wait(p_full, static_cast<uint32_t>(pv_gt) & 1u)) {
-            if (!issue_pv(pv_gt, pv_first)) return false;
-            pv_gt = -1;
+          // wait for the block, but issue the pending PV as soon as its P is ready
+          if (pv_gt >= 0 && !mbar_test_wait(&full[slot], use_of(gt, b))) {
+            const uint64_t t0 = globaltimer();
+            for (uint32_t spin = 0;; ++spin) {
+              if (mbar_test_wait(p_full, static_cast<uint32_t>(pv_gt) & 1u)) {
+                if (!issue_pv(pv_gt, pv_first)) return false;
+                pv_gt = -1;
+                break;
+              }
+              if (mbar_test_wait(&full[slot], use_of(gt, b))) break;
+              if ((spin & 63u) == 63u && (*abort_flag || globaltimer() - t0 > kWaitNs)) break;   // the bounded wait below decides
+            }
           }
           if (!mbar_wait(&full[slot], use_of(gt, b), abort_flag)) return false;
           if (b == 0 || b == NB - 1) TL(2, (b == 0 ? 1000 : 2000) + gt % 1000);

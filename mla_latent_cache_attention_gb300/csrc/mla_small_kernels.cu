@@ -178,6 +178,9 @@ __global__ void __launch_bounds__(128) mla_epilogue_kernel(const EpiParams p) {
 // _forward_prefill_fused) applied across the key splits of one decode row.  One CTA of 128
 // threads per (row, head); each thread owns 4 of the 512 columns.
 __global__ void __launch_bounds__(128) mla_merge_kernel(const MergeParams p) {
+  // launched as a programmatic dependent of the attention kernel: wait until its grid has
+  // finished and its partials are visible (a no-op under an ordinary launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t rh = blockIdx.x;
   const int64_t stride = static_cast<int64_t>(p.n_rows) * p.H;
   const int row = static_cast<int>(rh / p.H), h = static_cast<int>(rh % p.H);
@@ -299,8 +302,19 @@ cudaError_t launch_epilogue(int fmt, const EpiParams& p, int B, cudaStream_t str
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   const int64_t n = static_cast<int64_t>(p.n_rows) * p.H;
   if (n == 0) return cudaSuccess;
-  mla_merge_kernel<<<static_cast<unsigned>(n), 128, 0, stream>>>(p);
-  return cudaGetLastError();
+  // programmatic dependent launch: the merge CTAs are scheduled while the attention kernel's
+  // last CTAs finish, and wait on the device instead of behind a launch gap
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(n));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, mla_merge_kernel, p);
 }
 
 cudaError_t launch_gather(int fmt, const GatherParams& p, cudaStream_t stream) {
