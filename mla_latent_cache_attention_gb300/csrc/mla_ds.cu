@@ -35,3 +35,12 @@ cudaError_t launch_ds_paged(const DsParams& p, const void* tkv, const void* tsc,
 }
 
 }  // namespace mla
+
+#ifdef MLA_TIMELINE
+extern "C" __attribute__((visibility("default"))) int mla_debug_timeline_ds(void* events, void* counts) {
+  cudaMemcpyFromSymbol(events, mla::g_tl, sizeof(mla::g_tl));
+  cudaMemcpyFromSymbol(counts, mla::g_tl_n, sizeof(mla::g_tl_n));
+  const int zero[mla::kTlCtas][mla::kTlRoles] = {};
+  return cudaMemcpyToSymbol(mla::g_tl_n, zero, sizeof(zero)) == cudaSuccess ? 0 : -3;
+}
+#endif

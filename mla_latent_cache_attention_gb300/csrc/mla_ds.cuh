@@ -15,11 +15,12 @@
 //     (S_j, 32 TMEM columns) and the softmax forms s = 2^-e_c sum_j s_j (S_j,hi + S_j,lo) +
 //     S_rope, so the per-key scale is applied in fp32.  k_pe . q_pe runs as a bf16 MMA.
 //   * PV on the e4m3 codes as well: O_j^T = V_j^T P_j with P_j = p * s_j * r_j, one P per value
-//     tile so that each key's scale multiplies its own term, as four e5m2 terms (stacked along
-//     N, 16 columns each; e4m3 codes x e5m2 weights).  Each term rounds what the earlier ones
-//     left, so P_j holds to about 2^-12 relative, and e5m2 reaches down to 2^-16, which keeps
-//     the many small weights of a long row (whose values reach 448 times the scale) from
-//     being lost under an e4m3 floor of 2^-9.  r_j is a power of two kept per item so
+//     tile so that each key's scale multiplies its own term, as three e5m2 terms (stacked
+//     along N, 16 columns each; e4m3 codes x e5m2 weights), split in packed f16 arithmetic.
+//     Each term rounds what the earlier ones left, so P_j holds to about 2^-9 relative (f16
+//     rounding of P_j, 2^-11, is below that), and e5m2 reaches down to 2^-16, which keeps the
+//     many small weights of a long row (whose values reach 448 times the scale) from being
+//     lost under an e4m3 floor of 2^-9.  r_j is a power of two kept per item so
 //     that s_j r_j <= 1; when a later key needs a smaller r_j, O_j is rescaled by the (exact)
 //     ratio.
 //   * Online softmax with a lazily moved reference max, as in the page kernel.
@@ -70,8 +71,8 @@ struct DsCfg {
   static constexpr int kScale = kRing + R * kSlotBytes;          // [2][128] float4
   static constexpr int kQ = kScale + 2 * kTile * 16;              // 4 x (32 rows x 128 B) hi/lo + 16 x 128 B rope
   static constexpr int kQRope = kQ + 4 * 32 * 128;
-  static constexpr int kP = kQRope + NQ * 128;                    // 4 x (128 keys x 64 B)
-  static constexpr int kRed = kP + 4 * kTile * 64;                // [2][16][4] max, [16][4] sum, [4][4] scale max
+  static constexpr int kP = kQRope + NQ * 128;                    // 4 x (128 keys x 48 B)
+  static constexpr int kRed = kP + 4 * kTile * 48;                // [2][16][4] max, [16][4] sum, [4][4] scale max
   static constexpr int kColF = kRed + (3 * NQ * 4 + 16) * 4;      // [16] 2^-e_c
   static constexpr int kValid = kColF + NQ * 4;                   // [2][128] row flags (sparse)
   static constexpr int kItems = kValid + 2 * kTile;
@@ -82,7 +83,7 @@ struct DsCfg {
   static constexpr int kAlloc = kTotal + 1024;
   static_assert(kAlloc <= kSmemLimit, "shared memory budget");
   static constexpr int kS = 0;                                    // S (144 columns): S_j at 32 j, rope at 128
-  static constexpr int kTmemO = 160;                              // O_j at kTmemO + 64 j (4 terms x 16 columns)
+  static constexpr int kTmemO = 160;                              // O_j at kTmemO + 64 j (3 terms x 16 columns)
   static constexpr int kTmemCols = 512;
 };
 
@@ -92,6 +93,15 @@ __device__ __forceinline__ uint32_t e5m2x2_sat(float a, float b) {
 __device__ __forceinline__ float2 e5m2x2_to_float2(uint32_t v) {
   const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E5M2);
   return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
+
+__device__ __forceinline__ uint32_t e5m2x2_of_h2(__half2 v) {
+  return static_cast<uint32_t>(
+      __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&v), __NV_SATFINITE, __NV_E5M2));
+}
+__device__ __forceinline__ __half2 h2_of_e5m2x2(uint32_t v) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E5M2);
+  return *reinterpret_cast<const __half2*>(&h);
 }
 
 __device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }   // e in [-126, 127]
@@ -300,15 +310,17 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
       const uint64_t dQ0 = smem_desc(q_a, 16, 1024, kSwizzle128B);
       const uint64_t dQr = smem_desc(qr_a, 16, 1024, kSwizzle128B);
       const uint64_t dV0 = smem_desc(ring_a, kSlotBytes, 1024, kSwizzle128B);
-      const uint64_t dP0 = smem_desc(p_a, 512, 128, kSwizzleNone);
+      const uint64_t dP0 = smem_desc(p_a, 384, 128, kSwizzleNone);
       constexpr uint32_t kIdNope = idesc_e4m3(128, 32, 0, 0);
       constexpr uint32_t kIdRope = idesc_f16(128, 16, 1, 1, 0, 0);
-      constexpr uint32_t kIdPv = idesc_e4m3(128, 64, 1, 1) | (1u << 10);   // B (weights) in e5m2
+      constexpr uint32_t kIdPv = idesc_e4m3(128, 48, 1, 1) | (1u << 10);   // B (weights) in e5m2
       auto slot_of = [&](int gt, int b) -> int { return (gt & 1) * NB + b; };
       auto issue_qk = [&](int gt) -> bool {
+        TL(2, 1);
         // one S buffer: the softmax of the previous tile must have read it
         if (gt > 0 && !mbar_wait(s_free, static_cast<uint32_t>(gt - 1) & 1u, abort_flag)) return false;
         tc_fence_after();
+        TL(2, 5);
         const uint32_t dS = tmem + C::kS;
 #pragma unroll 1
         for (int b = 0; b < NB; ++b) {
@@ -328,21 +340,24 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
           }
         }
         mma_commit(&s_full[0]);
+        TL(2, 2);
         return true;
       };
       auto issue_pv = [&](int gt, bool first) -> bool {
         if (!mbar_wait(p_full, static_cast<uint32_t>(gt) & 1u, abort_flag)) return false;
         tc_fence_after();
+        TL(2, 3);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const uint64_t aV = dV0 + ((slot_of(gt, j) * kSlotBytes) >> 4);
-          const uint64_t bP = dP0 + ((j * kTile * 64) >> 4);
+          const uint64_t bP = dP0 + ((j * kTile * 48) >> 4);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_f8_ss(tmem + C::kTmemO + 64 * j, aV + ((kk * 4096) >> 4), bP + ((kk * 2048) >> 4), kIdPv,
+            mma_f8_ss(tmem + C::kTmemO + 64 * j, aV + ((kk * 4096) >> 4), bP + ((kk * 1536) >> 4), kIdPv,
                       (!first || kk > 0) ? 1u : 0u);
         }
         mma_commit(&pv_done[gt & 1]);
+        TL(2, 4);
         return true;
       };
       bool ok = true;
@@ -458,6 +473,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         const int gt = g + t;
         w = warp_wait(&s_full[0], static_cast<uint32_t>(gt) & 1u, abort_flag);
         tc_fence_after();
+        if (stid == 0) TL(3, 1);
         const float4 s4 = scl[(gt & 1) * kTile + row];
         const float sj[4] = {s4.x, s4.y, s4.z, s4.w};
         const int kpos = it.k0 + t * kTile + row;
@@ -559,13 +575,14 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
             pv_waited = true;
             if (w && resc) {
 #pragma unroll 1
-              for (int jq = 0; jq < 16; ++jq) {     // value tile jq / 4, term jq % 4
+              for (int jq = 0; jq < 12; ++jq) {     // value tile jq / 3, term jq % 3
+                const int j = jq / 3, term = jq % 3;
                 float o[16];
-                tmem_ld16(tl + C::kTmemO + 16 * jq, o);
+                tmem_ld16(tl + C::kTmemO + 64 * j + 16 * term, o);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 16; ++c) o[c] *= alpha[c] * ratio[jq >> 2];
-                tmem_st16(tl + C::kTmemO + 16 * jq, o);
+                for (int c = 0; c < 16; ++c) o[c] *= alpha[c] * ratio[j];
+                tmem_st16(tl + C::kTmemO + 64 * j + 16 * term, o);
               }
               tmem_st_wait();
             }
@@ -581,24 +598,25 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
           w = warp_wait(&pv_done[(gt - 1) & 1], static_cast<uint32_t>((gt - 1) >> 1) & 1u, abort_flag);
           tc_fence_after();
         }
-        // P_j = p s_j r_j as four e5m2 terms (4 x 16 columns), 8 keys x 16 B core matrices
+        // P_j = p s_j r_j as three e5m2 terms (3 x 16 columns), split in packed f16,
+        // 8 keys x 16 B core matrices
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float f = rv ? sj[j] * rj[j] : 0.f;
-          uint8_t* pj = ps + j * (kTile * 64) + (row >> 3) * 512 + (row & 7) * 16;
-          float a[16];
+          uint8_t* pj = ps + j * (kTile * 48) + (row >> 3) * 384 + (row & 7) * 16;
+          __half2 a[8];
 #pragma unroll
-          for (int c = 0; c < 16; ++c) a[c] = s[c] * f;
+          for (int u = 0; u < 8; ++u) a[u] = __floats2half2_rn(s[2 * u] * f, s[2 * u + 1] * f);
 #pragma unroll
-          for (int term = 0; term < 4; ++term) {
+          for (int term = 0; term < 3; ++term) {
             uint32_t wv[4];
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const uint32_t c01 = e5m2x2_sat(a[4 * u], a[4 * u + 1]), c23 = e5m2x2_sat(a[4 * u + 2], a[4 * u + 3]);
+              const uint32_t c01 = e5m2x2_of_h2(a[2 * u]), c23 = e5m2x2_of_h2(a[2 * u + 1]);
               wv[u] = c01 | (c23 << 16);
-              if (term < 3) {
-                const float2 f01 = e5m2x2_to_float2(c01), f23 = e5m2x2_to_float2(c23);
-                a[4 * u] -= f01.x, a[4 * u + 1] -= f01.y, a[4 * u + 2] -= f23.x, a[4 * u + 3] -= f23.y;
+              if (term < 2) {
+                a[2 * u] = __hsub2(a[2 * u], h2_of_e5m2x2(c01));
+                a[2 * u + 1] = __hsub2(a[2 * u + 1], h2_of_e5m2x2(c23));
               }
             }
             *reinterpret_cast<uint4*>(pj + 128 * term) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
@@ -615,9 +633,11 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         }
         fence_proxy_async_smem();
         tc_fence_before();
+        if (stid == 0) TL(3, 2);
         ok = named_bar_and(1, NT, w);
         if (!ok) break;
         if (stid == 0) mbar_arrive(p_full);
+        if (stid == 0) TL(3, 3);
       }
       if (!ok) break;
       // ---- epilogue
@@ -660,7 +680,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         for (int c = 0; c < 16; ++c) o[c] = 0.f;
         if (it.ntiles > 0) {
 #pragma unroll
-          for (int term = 0; term < 4; ++term) {
+          for (int term = 0; term < 3; ++term) {
             float ot[16];
             tmem_ld16(tl + C::kTmemO + 64 * j + 16 * term, ot);
             tmem_ld_wait();
@@ -733,6 +753,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
             errbits |= 1u;
           }
         }
+        if (gi == 0) TL(1, 1);
         uint4 v[21];
 #pragma unroll
         for (int i = 0; i < 21; ++i) {
@@ -744,6 +765,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
           ok = false;
           break;
         }
+        if (gi == 0) TL(1, 2);
 #pragma unroll
         for (int i = 0; i < 21; ++i) {
           const int c = c_lo + i;
@@ -762,6 +784,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         __syncwarp();
         if (lane == 0)
           for (int b = 0; b < NB; ++b) mbar_arrive(&full[(gt & 1) * NB + b]);
+        if (gi == 0) TL(1, 3);
       }
       g += it.ntiles;
     }
