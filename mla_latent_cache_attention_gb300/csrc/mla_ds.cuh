@@ -15,10 +15,11 @@
 //     (S_j, 32 TMEM columns) and the softmax forms s = 2^-e_c sum_j s_j (S_j,hi + S_j,lo) +
 //     S_rope, so the per-key scale is applied in fp32.  k_pe . q_pe runs as a bf16 MMA.
 //   * PV on the e4m3 codes as well: O_j^T = V_j^T P_j with P_j = p * s_j * r_j, one P per value
-//     tile so that each key's scale multiplies its own term, as three e5m2 terms (stacked
-//     along N, 16 columns each; e4m3 codes x e5m2 weights), split in packed f16 arithmetic.
-//     Each term rounds what the earlier ones left, so P_j holds to about 2^-9 relative (f16
-//     rounding of P_j, 2^-11, is below that), and e5m2 reaches down to 2^-16, which keeps the
+//     tile so that each key's scale multiplies its own term, as four e5m2 terms (stacked
+//     along N, 16 columns each; e4m3 codes x e5m2 weights), split on the f16 bits of P_j
+//     (an e5m2 is the upper byte of an f16): three terms keep 3 significant bits each of
+//     what is left and the fourth rounds the rest, so the split carries the f16 value of P_j
+//     (2^-11 relative), and e5m2 reaches down to 2^-16, which keeps the
 //     many small weights of a long row (whose values reach 448 times the scale) from being
 //     lost under an e4m3 floor of 2^-9.  r_j is a power of two kept per item so
 //     that s_j r_j <= 1; when a later key needs a smaller r_j, O_j is rescaled by the (exact)
@@ -71,8 +72,8 @@ struct DsCfg {
   static constexpr int kScale = kRing + R * kSlotBytes;          // [2][128] float4
   static constexpr int kQ = kScale + 2 * kTile * 16;              // 4 x (32 rows x 128 B) hi/lo + 16 x 128 B rope
   static constexpr int kQRope = kQ + 4 * 32 * 128;
-  static constexpr int kP = kQRope + NQ * 128;                    // 4 x (128 keys x 48 B)
-  static constexpr int kRed = kP + 4 * kTile * 48;                // [2][16][4] max, [16][4] sum, [4][4] scale max
+  static constexpr int kP = kQRope + NQ * 128;                    // 4 x (128 keys x 64 B)
+  static constexpr int kRed = kP + 4 * kTile * 64;                // [2][16][4] max, [16][4] sum, [4][4] scale max
   static constexpr int kColF = kRed + (3 * NQ * 4 + 16) * 4;      // [16] 2^-e_c
   static constexpr int kValid = kColF + NQ * 4;                   // [2][128] row flags (sparse)
   static constexpr int kItems = kValid + 2 * kTile;
@@ -83,26 +84,9 @@ struct DsCfg {
   static constexpr int kAlloc = kTotal + 1024;
   static_assert(kAlloc <= kSmemLimit, "shared memory budget");
   static constexpr int kS = 0;                                    // S (144 columns): S_j at 32 j, rope at 128
-  static constexpr int kTmemO = 160;                              // O_j at kTmemO + 64 j (3 terms x 16 columns)
+  static constexpr int kTmemO = 160;                              // O_j at kTmemO + 64 j (4 terms x 16 columns)
   static constexpr int kTmemCols = 512;
 };
-
-__device__ __forceinline__ uint32_t e5m2x2_sat(float a, float b) {
-  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E5M2));
-}
-__device__ __forceinline__ float2 e5m2x2_to_float2(uint32_t v) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E5M2);
-  return __half22float2(*reinterpret_cast<const __half2*>(&h));
-}
-
-__device__ __forceinline__ uint32_t e5m2x2_of_h2(__half2 v) {
-  return static_cast<uint32_t>(
-      __nv_cvt_halfraw2_to_fp8x2(*reinterpret_cast<const __half2_raw*>(&v), __NV_SATFINITE, __NV_E5M2));
-}
-__device__ __forceinline__ __half2 h2_of_e5m2x2(uint32_t v) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E5M2);
-  return *reinterpret_cast<const __half2*>(&h);
-}
 
 __device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }   // e in [-126, 127]
 
@@ -253,6 +237,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
             }
           }
           // the two-tile ring: tile gt reuses the slots of tile gt - 2
+          if (lane == 0) TL(0, 1);
           if (gt >= 2 && gt - 2 != t_waited) {
             if (!warp_wait(&pv_done[gt & 1], static_cast<uint32_t>((gt - 2) >> 1) & 1u, abort_flag)) {
               ok = false;
@@ -260,6 +245,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
             }
             t_waited = gt - 2;
           }
+          if (lane == 0) TL(0, 2);
 #pragma unroll 1
           for (int b = 0; b < NB; ++b, ++pos) {
             const int slot = static_cast<int>(pos % R);
@@ -310,11 +296,30 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
       const uint64_t dQ0 = smem_desc(q_a, 16, 1024, kSwizzle128B);
       const uint64_t dQr = smem_desc(qr_a, 16, 1024, kSwizzle128B);
       const uint64_t dV0 = smem_desc(ring_a, kSlotBytes, 1024, kSwizzle128B);
-      const uint64_t dP0 = smem_desc(p_a, 384, 128, kSwizzleNone);
+      const uint64_t dP0 = smem_desc(p_a, 512, 128, kSwizzleNone);
       constexpr uint32_t kIdNope = idesc_e4m3(128, 32, 0, 0);
       constexpr uint32_t kIdRope = idesc_f16(128, 16, 1, 1, 0, 0);
-      constexpr uint32_t kIdPv = idesc_e4m3(128, 48, 1, 1) | (1u << 10);   // B (weights) in e5m2
+      constexpr uint32_t kIdPv = idesc_e4m3(128, 64, 1, 1) | (1u << 10);   // B (weights) in e5m2
       auto slot_of = [&](int gt, int b) -> int { return (gt & 1) * NB + b; };
+      auto issue_pv = [&](int gt, bool first) -> bool {
+        if (!mbar_wait(p_full, static_cast<uint32_t>(gt) & 1u, abort_flag)) return false;
+        tc_fence_after();
+        TL(2, 3);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint64_t aV = dV0 + ((slot_of(gt, j) * kSlotBytes) >> 4);
+          const uint64_t bP = dP0 + ((j * kTile * 64) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk)
+            mma_f8_ss(tmem + C::kTmemO + 64 * j, aV + ((kk * 4096) >> 4), bP + ((kk * 2048) >> 4), kIdPv,
+                      (!first || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(&pv_done[gt & 1]);
+        TL(2, 4);
+        return true;
+      };
+      int pv_gt = -1;          // PV still to issue (its P may be ready while QK waits for data)
+      bool pv_first = false;
       auto issue_qk = [&](int gt) -> bool {
         TL(2, 1);
         // one S buffer: the softmax of the previous tile must have read it
@@ -325,7 +330,20 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
 #pragma unroll 1
         for (int b = 0; b < NB; ++b) {
           const int slot = slot_of(gt, b);
-          if (!mbar_wait(&full[slot], static_cast<uint32_t>(gt >> 1) & 1u, abort_flag)) return false;
+          const uint32_t par = static_cast<uint32_t>(gt >> 1) & 1u;
+          if (pv_gt >= 0 && !mbar_test_wait(&full[slot], par)) {
+            const uint64_t t0 = globaltimer();
+            for (uint32_t spin = 0;; ++spin) {
+              if (mbar_test_wait(p_full, static_cast<uint32_t>(pv_gt) & 1u)) {
+                if (!issue_pv(pv_gt, pv_first)) return false;
+                pv_gt = -1;
+                break;
+              }
+              if (mbar_test_wait(&full[slot], par)) break;
+              if ((spin & 63u) == 63u && (*abort_flag || globaltimer() - t0 > kWaitNs)) break;   // the bounded wait below decides
+            }
+          }
+          if (!mbar_wait(&full[slot], par, abort_flag)) return false;
           tc_fence_after();
           const uint64_t aK = dK0 + ((slot * kSlotBytes) >> 4);
           if (b < 4) {
@@ -343,23 +361,6 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         TL(2, 2);
         return true;
       };
-      auto issue_pv = [&](int gt, bool first) -> bool {
-        if (!mbar_wait(p_full, static_cast<uint32_t>(gt) & 1u, abort_flag)) return false;
-        tc_fence_after();
-        TL(2, 3);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint64_t aV = dV0 + ((slot_of(gt, j) * kSlotBytes) >> 4);
-          const uint64_t bP = dP0 + ((j * kTile * 48) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f8_ss(tmem + C::kTmemO + 64 * j, aV + ((kk * 4096) >> 4), bP + ((kk * 1536) >> 4), kIdPv,
-                      (!first || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&pv_done[gt & 1]);
-        TL(2, 4);
-        return true;
-      };
       bool ok = true;
       int nit = 0, nq = 0, g = 0;
       while (ok) {
@@ -374,11 +375,16 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         ++nq;
         tc_fence_after();
         ok = issue_qk(g);
+        pv_gt = g;
+        pv_first = true;
         for (int t = 1; t < it.ntiles && ok; ++t) {
           ok = issue_qk(g + t);
-          ok = ok && issue_pv(g + t - 1, t == 1);
+          if (ok && pv_gt >= 0) ok = issue_pv(pv_gt, pv_first);
+          pv_gt = g + t;
+          pv_first = false;
         }
-        ok = ok && issue_pv(g + it.ntiles - 1, it.ntiles == 1);
+        if (ok && pv_gt >= 0) ok = issue_pv(pv_gt, pv_first);
+        pv_gt = -1;
         g += it.ntiles;
       }
       mma_commit(fin);
@@ -396,7 +402,9 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
     float* red_m = red;                 // [2][16][4]
     float* red_l = red + 2 * NQ * 4;    // [16][4]
     float* red_s = red + 3 * NQ * 4;    // [4 warps][4 tiles] scale maxima
-    constexpr float kTau = 4.f, kPExp = 4.f;
+    // p = 2^(s - m_ref + kPExp) <= 2^(kTau + kPExp) = 2^14 keeps P_j = p s_j r_j inside f16
+    // and e5m2 (both past 2^15), and the lazy reference moves only on a jump of kTau
+    constexpr float kTau = 10.f, kPExp = 4.f;
     int nit = 0, g = 0;
     bool ok = true;
     while (ok) {
@@ -485,12 +493,13 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < NQ; ++c) s[c] = 0.f;
 #pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float hl[32];
-            tmem_ld_n<32>(sb + 32 * j, hl);
+          for (int j = 0; j < 4; j += 2) {
+            float hl[64];
+            tmem_ld_n<64>(sb + 32 * j, hl);
             tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < NQ; ++c) s[c] = fmaf(sj[j], hl[c] + hl[16 + c], s[c]);
+            for (int c = 0; c < NQ; ++c)
+              s[c] = fmaf(sj[j + 1], hl[32 + c] + hl[48 + c], fmaf(sj[j], hl[c] + hl[16 + c], s[c]));
           }
           float sr[16];
           tmem_ld16(sb + 128, sr);
@@ -498,6 +507,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
 #pragma unroll
           for (int c = 0; c < NQ; ++c) s[c] = rv ? p.sig2 * fmaf(colf[c], s[c], sr[c]) : -CUDART_INF_F;
         }
+        if (stid == 0) TL(3, 4);
         if (!kSparse) {
           const int dq = kpos - it.L + p.q_len;
           if (rv && dq > 0) {
@@ -513,6 +523,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         for (int j = 0; j < 4; ++j) need |= rv && (sj[j] * rj[j] > 1.f || rj[j] == 0.f);
         tc_fence_before();
         const bool rare = named_bar_or(1, NT, need || !w);
+        if (stid == 0) TL(3, rare ? 6 : 5);
         if (stid == 0) mbar_arrive(s_free);     // S is in registers: the next QK may overwrite it
         bool pv_waited = false;
         if (rare) {
@@ -575,14 +586,13 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
             pv_waited = true;
             if (w && resc) {
 #pragma unroll 1
-              for (int jq = 0; jq < 12; ++jq) {     // value tile jq / 3, term jq % 3
-                const int j = jq / 3, term = jq % 3;
-                float o[16];
-                tmem_ld16(tl + C::kTmemO + 64 * j + 16 * term, o);
+              for (int j = 0; j < 4; ++j) {     // value tile j: four terms x 16 columns
+                float o[64];
+                tmem_ld_n<64>(tl + C::kTmemO + 64 * j, o);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 16; ++c) o[c] *= alpha[c] * ratio[j];
-                tmem_st16(tl + C::kTmemO + 64 * j + 16 * term, o);
+                for (int c = 0; c < 64; ++c) o[c] *= alpha[c % 16] * ratio[j];
+                tmem_st_n<64>(tl + C::kTmemO + 64 * j, o);
               }
               tmem_st_wait();
             }
@@ -598,30 +608,44 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
           w = warp_wait(&pv_done[(gt - 1) & 1], static_cast<uint32_t>((gt - 1) >> 1) & 1u, abort_flag);
           tc_fence_after();
         }
-        // P_j = p s_j r_j as three e5m2 terms (3 x 16 columns), split in packed f16,
-        // 8 keys x 16 B core matrices
+        if (stid == 0) TL(3, 7);
+        // P_j = p s_j r_j as four e5m2 terms (4 x 16 columns), 8 keys x 16 B core matrices.
+        // e5m2 is the upper byte of an f16 (same sign, exponent bias and subnormals): the
+        // first three terms keep the upper byte of what is left (the remainder, an exact f16
+        // subtraction, keeps the sign), the last rounds it to nearest even.
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float f = rv ? sj[j] * rj[j] : 0.f;
-          uint8_t* pj = ps + j * (kTile * 48) + (row >> 3) * 384 + (row & 7) * 16;
-          __half2 a[8];
+          uint8_t* pj = ps + j * (kTile * 64) + (row >> 3) * 512 + (row & 7) * 16;
+          uint32_t a[8];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) a[u] = __floats2half2_rn(s[2 * u] * f, s[2 * u + 1] * f);
+          for (int u = 0; u < 8; ++u) {
+            const __half2 h = __floats2half2_rn(s[2 * u] * f, s[2 * u + 1] * f);
+            a[u] = *reinterpret_cast<const uint32_t*>(&h);
+          }
 #pragma unroll
-          for (int term = 0; term < 3; ++term) {
+          for (int term = 0; term < 4; ++term) {
             uint32_t wv[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const uint32_t c01 = e5m2x2_of_h2(a[2 * u]), c23 = e5m2x2_of_h2(a[2 * u + 1]);
-              wv[u] = c01 | (c23 << 16);
-              if (term < 2) {
-                a[2 * u] = __hsub2(a[2 * u], h2_of_e5m2x2(c01));
-                a[2 * u + 1] = __hsub2(a[2 * u + 1], h2_of_e5m2x2(c23));
+            for (int u = 0; u < 8; u += 2) {
+              uint32_t t0, t1;
+              if (term < 3) {
+                t0 = a[u] & 0xFF00FF00u;
+                t1 = a[u + 1] & 0xFF00FF00u;
+                const __half2 r0 = __hsub2(*reinterpret_cast<const __half2*>(&a[u]), *reinterpret_cast<const __half2*>(&t0));
+                const __half2 r1 = __hsub2(*reinterpret_cast<const __half2*>(&a[u + 1]), *reinterpret_cast<const __half2*>(&t1));
+                a[u] = *reinterpret_cast<const uint32_t*>(&r0);
+                a[u + 1] = *reinterpret_cast<const uint32_t*>(&r1);
+              } else {
+                t0 = a[u] + 0x007F007Fu + ((a[u] >> 8) & 0x00010001u);
+                t1 = a[u + 1] + 0x007F007Fu + ((a[u + 1] >> 8) & 0x00010001u);
               }
+              wv[u >> 1] = __byte_perm(t0, t1, 0x7531);
             }
             *reinterpret_cast<uint4*>(pj + 128 * term) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
           }
         }
+        if (stid == 0) TL(3, 8);
         // rows past the item or masked: their codes never reach PV (stale slot contents)
         if (!rv) {
 #pragma unroll 1
@@ -679,14 +703,11 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
 #pragma unroll
         for (int c = 0; c < 16; ++c) o[c] = 0.f;
         if (it.ntiles > 0) {
+          float ot[64];
+          tmem_ld_n<64>(tl + C::kTmemO + 64 * j, ot);
+          tmem_ld_wait();
 #pragma unroll
-          for (int term = 0; term < 3; ++term) {
-            float ot[16];
-            tmem_ld16(tl + C::kTmemO + 64 * j + 16 * term, ot);
-            tmem_ld_wait();
-#pragma unroll
-            for (int c = 0; c < 16; ++c) o[c] += ot[c];
-          }
+          for (int c = 0; c < 16; ++c) o[c] = (ot[c] + ot[16 + c]) + (ot[32 + c] + ot[48 + c]);
         }
         const float ur = (rj[j] > 0.f) ? 1.f / rj[j] : 0.f;     // exact: a power of two
         const int d = 128 * j + row;
