@@ -33,7 +33,7 @@ WORKLOADS = ("decode_bf16_epilogue", "sparse_prefill", "fp8_spec_verify", "ds_ml
 # the attention kernel each workload times (the profiling hook brackets exactly its launch)
 KERNELS = {
     "decode_bf16_epilogue": "mla_paged_tma_kernel<bf16, 16 columns>",
-    "sparse_prefill": "mla_attn_kernel<fp8_ds_mla, sparse> (staged converters)",
+    "sparse_prefill": "mla_ds_kernel<sparse> (gather warps)",
     "fp8_spec_verify": "mla_paged_tma_kernel<fp8, 64 columns>",
     "ds_mla_h96_decode": "mla_ds_kernel<paged>",
 }

@@ -111,12 +111,13 @@ size_t workspace_bytes_for(int64_t n_rows, int H, const SplitPlan& sp) {
   return ((po + 255) & ~size_t(255)) + ((pl + 255) & ~size_t(255)) + 256;
 }
 
-// The sparse forward runs the staged-converter kernel unless MLA_SPARSE_GATHER=1 selects the
-// vector-load gather kernel (faster on some index patterns, slower on the uniform top-k one).
+// The sparse forward runs the gather-warp fp8_ds_mla kernel (codes straight into the tensor
+// cores) unless MLA_SPARSE_GATHER=0 selects the staged-converter kernel (codes converted to
+// f16 in shared memory).  Read once per process.
 bool sparse_gather_kernel() {
   static const int v = [] {
     const char* e = getenv("MLA_SPARSE_GATHER");
-    return (e && e[0] == '1') ? 1 : 0;
+    return (e && e[0] == '0') ? 0 : 1;
   }();
   return v == 1;
 }

@@ -75,7 +75,10 @@ struct DsCfg {
   static constexpr int kP = kQRope + NQ * 128;                    // 4 x (128 keys x 64 B)
   static constexpr int kRed = kP + 4 * kTile * 64;                // [2][16][4] max, [16][4] sum, [4][4] scale max
   static constexpr int kColF = kRed + (3 * NQ * 4 + 16) * 4;      // [16] 2^-e_c
-  static constexpr int kValid = kColF + NQ * 4;                   // [2][128] row flags (sparse)
+  static constexpr int kMref = kColF + NQ * 4;                    // [4 warps][16] reference max, per warp
+  static constexpr int kAlph = kMref + 4 * NQ * 4;                // [4 warps][16] rescale factors, per warp
+  static constexpr int kRj = kAlph + 4 * NQ * 4;                  // [4 warps][8] r_j, O_j rescale ratios
+  static constexpr int kValid = kRj + 4 * 8 * 4;                  // [2][128] row flags (sparse)
   static constexpr int kItems = kValid + 2 * kTile;
   static constexpr int kBar = kItems + kItemDepth * 32;
   static constexpr int kNumBars = R + 8 + 2 * kItemDepth;
@@ -405,12 +408,13 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
     // p = 2^(s - m_ref + kPExp) <= 2^(kTau + kPExp) = 2^14 keeps P_j = p s_j r_j inside f16
     // and e5m2 (both past 2^15), and the lazy reference moves only on a jump of kTau
     constexpr float kTau = 10.f, kPExp = 4.f;
+    constexpr int kOB = kSparse ? 16 : 64;      // TMEM columns per O-rescale round trip (registers)
     int nit = 0, g = 0;
     bool ok = true;
     while (ok) {
       const int k = nit % kItemDepth;
       bool w = warp_wait(&item_full[k], (nit / kItemDepth) & 1, abort_flag);
-      const WorkItem it = items[k];
+      const WorkItem& it = items[k];     // read in place (registers): the slot is ours until item_empty
       ++nit;
       if (!named_bar_and(1, NT, w)) break;
       if (it.b < 0) break;
@@ -470,13 +474,19 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         named_bar_sync(1, NT);
         if (stid == 0) mbar_arrive(q_full);
       }
-      float m_ref[NQ], l_part[NQ];
+      // the column reference maxima and rescale factors are the same for every thread: one
+      // copy per warp in shared memory keeps them out of the registers
+      float* mref = reinterpret_cast<float*>(smem + C::kMref) + quad * NQ;
+      float* alph = reinterpret_cast<float*>(smem + C::kAlph) + quad * NQ;
+      if (lane < NQ) mref[lane] = -CUDART_INF_F;
+      __syncwarp();
+      float l_part[NQ];
 #pragma unroll
-      for (int c = 0; c < NQ; ++c) {
-        m_ref[c] = -CUDART_INF_F;
-        l_part[c] = 0.f;
-      }
-      float rj[4] = {0.f, 0.f, 0.f, 0.f};   // per value tile: P_j = p s_j r_j (0: not set yet)
+      for (int c = 0; c < NQ; ++c) l_part[c] = 0.f;
+      float* rj = reinterpret_cast<float*>(smem + C::kRj) + quad * 8;   // per value tile: P_j = p s_j r_j (0: not set yet)
+      float* ratio = rj + 4;
+      if (lane < 4) rj[lane] = 0.f;
+      __syncwarp();
       for (int t = 0; t < it.ntiles; ++t) {
         const int gt = g + t;
         w = warp_wait(&s_full[0], static_cast<uint32_t>(gt) & 1u, abort_flag);
@@ -492,14 +502,16 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
           const uint32_t sb = tl + C::kS;
 #pragma unroll
           for (int c = 0; c < NQ; ++c) s[c] = 0.f;
+          constexpr int kSB = kSparse ? 1 : 2;     // S tiles per TMEM round trip (registers)
 #pragma unroll
-          for (int j = 0; j < 4; j += 2) {
-            float hl[64];
-            tmem_ld_n<64>(sb + 32 * j, hl);
+          for (int j = 0; j < 4; j += kSB) {
+            float hl[32 * kSB];
+            tmem_ld_n<32 * kSB>(sb + 32 * j, hl);
             tmem_ld_wait();
 #pragma unroll
-            for (int c = 0; c < NQ; ++c)
-              s[c] = fmaf(sj[j + 1], hl[32 + c] + hl[48 + c], fmaf(sj[j], hl[c] + hl[16 + c], s[c]));
+            for (int u = 0; u < kSB; ++u)
+#pragma unroll
+              for (int c = 0; c < NQ; ++c) s[c] = fmaf(sj[j + u], hl[32 * u + c] + hl[32 * u + 16 + c], s[c]);
           }
           float sr[16];
           tmem_ld16(sb + 128, sr);
@@ -518,7 +530,10 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         }
         bool need = false;
 #pragma unroll
-        for (int c = 0; c < NQ; ++c) need |= (s[c] > m_ref[c] + kTau) | ((m_ref[c] == -CUDART_INF_F) & (s[c] > -CUDART_INF_F));
+        for (int c = 0; c < NQ; ++c) {
+          const float mr = mref[c];
+          need |= (s[c] > mr + kTau) | ((mr == -CUDART_INF_F) & (s[c] > -CUDART_INF_F));
+        }
 #pragma unroll
         for (int j = 0; j < 4; ++j) need |= rv && (sj[j] * rj[j] > 1.f || rj[j] == 0.f);
         tc_fence_before();
@@ -551,34 +566,44 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
             const float4 q4 = reinterpret_cast<const float4*>(rb)[lane % NQ];
             mt_l = fmaxf(fmaxf(q4.x, q4.y), fmaxf(q4.z, q4.w));
           }
-          bool resc = false;
-          float alpha[NQ];
-#pragma unroll
-          for (int c = 0; c < NQ; ++c) {
-            const float mo = m_ref[c];
-            const float mn = fmaxf(mo, __shfl_sync(0xFFFFFFFFu, mt_l, c));
-            alpha[c] = (mo == -CUDART_INF_F) ? 0.f : ex2(mo - mn);
-            resc |= (mn != mo);
-            m_ref[c] = mn;
-            l_part[c] *= alpha[c];
-          }
-          // value-tile references: r_j = 2^-ceil(log2 max s_j) once a larger scale shows up
-          float ratio[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            float mx = 0.f;
-#pragma unroll
-            for (int wq = 0; wq < 4; ++wq) mx = fmaxf(mx, red_s[wq * 4 + j]);
-            ratio[j] = 1.f;
-            if (mx > 0.f && (rj[j] == 0.f || mx * rj[j] > 1.f)) {
-              const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFF) - 127;
-              int e = -(ex + ((__float_as_uint(mx) & 0x7FFFFFu) ? 1 : 0));   // 2^e * mx <= 1
-              e = max(min(e, 126), -126);
-              const float rn = pow2i(e);
-              ratio[j] = (rj[j] == 0.f) ? 0.f : rn / rj[j];
-              resc |= (rj[j] != 0.f);
-              rj[j] = rn;
+          bool resc;
+          {
+            bool moved = false;
+            if (lane < NQ) {      // lane c: column c (mt_l holds column lane % NQ)
+              const float mo = mref[lane];
+              const float mn = fmaxf(mo, mt_l);
+              alph[lane] = (mo == -CUDART_INF_F) ? 0.f : ex2(mo - mn);
+              moved = (mn != mo);
+              mref[lane] = mn;
             }
+            resc = __any_sync(0xFFFFFFFFu, moved);
+            __syncwarp();
+          }
+#pragma unroll
+          for (int c = 0; c < NQ; ++c) l_part[c] *= alph[c];
+          // value-tile references: r_j = 2^-ceil(log2 max s_j) once a larger scale shows up
+          {
+            bool moved = false;
+            if (lane < 4) {       // lane j: value tile j
+              const int j = lane;
+              float mx = 0.f;
+#pragma unroll
+              for (int wq = 0; wq < 4; ++wq) mx = fmaxf(mx, red_s[wq * 4 + j]);
+              const float ro = rj[j];
+              float ra = 1.f;
+              if (mx > 0.f && (ro == 0.f || mx * ro > 1.f)) {
+                const int ex = static_cast<int>((__float_as_uint(mx) >> 23) & 0xFF) - 127;
+                int e = -(ex + ((__float_as_uint(mx) & 0x7FFFFFu) ? 1 : 0));   // 2^e * mx <= 1
+                e = max(min(e, 126), -126);
+                const float rn = pow2i(e);
+                ra = (ro == 0.f) ? 0.f : rn / ro;
+                moved = (ro != 0.f);
+                rj[j] = rn;
+              }
+              ratio[j] = ra;
+            }
+            resc |= __any_sync(0xFFFFFFFFu, moved);
+            __syncwarp();
           }
           if (t > 0) {
             w = warp_wait(&pv_done[(gt - 1) & 1], static_cast<uint32_t>((gt - 1) >> 1) & 1u, abort_flag);
@@ -586,13 +611,14 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
             pv_waited = true;
             if (w && resc) {
 #pragma unroll 1
-              for (int j = 0; j < 4; ++j) {     // value tile j: four terms x 16 columns
-                float o[64];
-                tmem_ld_n<64>(tl + C::kTmemO + 64 * j, o);
+              for (int jq = 0; jq < 4 * (64 / kOB); ++jq) {     // value tile j: four terms x 16 columns
+                const int j = jq / (64 / kOB);
+                float o[kOB];
+                tmem_ld_n<kOB>(tl + C::kTmemO + kOB * jq, o);
                 tmem_ld_wait();
 #pragma unroll
-                for (int c = 0; c < 64; ++c) o[c] *= alpha[c % 16] * ratio[j];
-                tmem_st_n<64>(tl + C::kTmemO + 64 * j, o);
+                for (int c = 0; c < kOB; ++c) o[c] *= alph[c % 16] * ratio[j];
+                tmem_st_n<kOB>(tl + C::kTmemO + kOB * jq, o);
               }
               tmem_st_wait();
             }
@@ -600,7 +626,8 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         }
 #pragma unroll
         for (int c = 0; c < NQ; ++c) {
-          const float mu = (m_ref[c] == -CUDART_INF_F) ? 0.f : m_ref[c];
+          const float mr = mref[c];
+          const float mu = (mr == -CUDART_INF_F) ? 0.f : mr;
           s[c] = ex2(s[c] - mu + kPExp);
           l_part[c] += s[c];
         }
@@ -683,9 +710,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
       {
         const float4 q4 = reinterpret_cast<const float4*>(red_l)[cl];
         const float l = (q4.x + q4.y) + (q4.z + q4.w);
-        float m_l = m_ref[0];
-#pragma unroll
-        for (int c = 1; c < NQ; ++c) m_l = (c == cl) ? m_ref[c] : m_l;
+        const float m_l = mref[cl];
         const bool live = l > 0.f;
         inv_l = live ? __fdividef(1.f, l) : 0.f;
         lse_l = live ? (m_l + __log2f(l) - kPExp) * 0.69314718055994531f : -CUDART_INF_F;

@@ -144,14 +144,14 @@ def test_config2_full_size_sampled_rows(m):
     assert m.read_device_errors() == 0
 
 
-def test_gather_kernel_variant():
-    # the vector-load gather kernel (selected per process by MLA_SPARSE_GATHER=1) against the
+def test_staged_converter_variant():
+    # the staged-converter kernel (selected per process by MLA_SPARSE_GATHER=0) against the
     # same cases, full-size prefill included, in a child process
     import subprocess
     import sys
-    env = dict(os.environ, MLA_SPARSE_GATHER="1")
+    env = dict(os.environ, MLA_SPARSE_GATHER="0")
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     r = subprocess.run([sys.executable, "-m", "pytest", os.path.abspath(__file__), "-m", "gpu", "-q", "-x",
-                        "-p", "no:cacheprovider", "-k", "not gather_kernel_variant"],
+                        "-p", "no:cacheprovider", "-k", "not staged_converter_variant"],
                        cwd=root, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
