@@ -342,8 +342,8 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
                 pv_gt = -1;
                 break;
               }
-              if (mbar_test_wait(&full[slot], par)) break;
-              if ((spin & 63u) == 63u && (*abort_flag || globaltimer() - t0 > kWaitNs)) break;   // the bounded wait below decides
+              if (mbar_try_wait_ns(&full[slot], par, 200)) break;
+              if ((spin & 15u) == 15u && (*abort_flag || globaltimer() - t0 > kWaitNs)) break;   // the bounded wait below decides
             }
           }
           if (!mbar_wait(&full[slot], par, abort_flag)) return false;
@@ -673,8 +673,9 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
           }
         }
         if (stid == 0) TL(3, 8);
-        // rows past the item or masked: their codes never reach PV (stale slot contents)
-        if (!rv) {
+        // rows past the item or masked: their codes never reach PV (stale slot contents);
+        // the gather warps already store zeros for them
+        if (!kSparse && !rv) {
 #pragma unroll 1
           for (int j = 0; j < 4; ++j) {
             uint4* dst = reinterpret_cast<uint4*>(ring + ((gt & 1) * NB + j) * kSlotBytes + row * 128);

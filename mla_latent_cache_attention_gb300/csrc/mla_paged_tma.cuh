@@ -561,8 +561,8 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
                 pv_gt = -1;
                 break;
               }
-              if (mbar_test_wait(&full[slot], use_of(gt, b))) break;
-              if ((spin & 63u) == 63u && (*abort_flag || globaltimer() - t0 > kWaitNs)) break;   // the bounded wait below decides
+              if (mbar_try_wait_ns(&full[slot], use_of(gt, b), 200)) break;
+              if ((spin & 15u) == 15u && (*abort_flag || globaltimer() - t0 > kWaitNs)) break;   // the bounded wait below decides
             }
           }
           if (!mbar_wait(&full[slot], use_of(gt, b), abort_flag)) return false;
