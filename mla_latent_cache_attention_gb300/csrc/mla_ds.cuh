@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
     // p = 2^(s - m_ref + kPExp) <= 2^(kTau + kPExp) = 2^14 keeps P_j = p s_j r_j inside f16
     // and e5m2 (both past 2^15), and the lazy reference moves only on a jump of kTau
     constexpr float kTau = 10.f, kPExp = 4.f;
-    constexpr int kOB = kSparse ? 16 : 64;      // TMEM columns per O-rescale round trip (registers)
+    constexpr int kOB = kSparse ? 32 : 64;      // TMEM columns per O-rescale round trip (registers)
     int nit = 0, g = 0;
     bool ok = true;
     while (ok) {
@@ -502,7 +502,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
           const uint32_t sb = tl + C::kS;
 #pragma unroll
           for (int c = 0; c < NQ; ++c) s[c] = 0.f;
-          constexpr int kSB = kSparse ? 1 : 2;     // S tiles per TMEM round trip (registers)
+          constexpr int kSB = 2;     // S tiles per TMEM round trip (registers)
 #pragma unroll
           for (int j = 0; j < 4; j += kSB) {
             float hl[32 * kSB];
@@ -770,11 +770,13 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
     }
   } else {
     // ------------------------------------------------------------------ gather (sparse)
-    // thread gi (0..255): record r = gi / 2 of the tile, half h = gi % 2 of its 41 16-byte
-    // chunks (0..31 codes, 32 scales, 33..40 k_pe)
-    const int gi = tid - 192;
-    const int r = gi >> 1, h = gi & 1;
-    const int c_lo = h ? 21 : 0, c_hi = h ? 41 : 21;
+    // Gather warp w (0..7) loads records 16 w .. 16 w + 15 of the tile; a record is 41 16-byte
+    // chunks (0..31 codes, 32 scales, 33..40 k_pe).  Loads are coalesced per record: load
+    // i < 16 brings the 32 code chunks of record 16 w + i (lane l: chunk l), and loads 16..20
+    // bring the 9 other chunks of all 16 records (lane l of load 16 + u: flat chunk
+    // f = 32 u + l < 144, record f / 9, chunk 32 + f % 9).  The tile waits in registers while
+    // its ring slots drain.
+    const int gw = warp - 6, rbase = 16 * gw;
     uint32_t errbits = 0;
     int nit = 0, g = 0;
     bool ok = true;
@@ -788,50 +790,62 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
       if (it.b < 0) break;
       for (int t = 0; t < it.ntiles && ok; ++t) {
         const int gt = g + t;
-        const int e = t * kTile + r;
-        bool valid = false;
-        const uint8_t* src = nullptr;
-        if (e < it.n) {
-          const int idx = p.indices[it.k0 + e];
-          if (idx >= 0 && idx < p.num_records) {
-            valid = true;
-            src = p.records + static_cast<int64_t>(idx) * p.rec_stride;
-          } else if (idx >= p.num_records || !p.has_invalid) {
-            errbits |= 1u;
+        // lane l < 16: record rbase + l of the tile (-1: past the row, masked or bad)
+        int idx = -1;
+        if (lane < 16) {
+          const int e = t * kTile + rbase + lane;
+          if (e < it.n) {
+            idx = p.indices[it.k0 + e];
+            if (idx < 0 || idx >= p.num_records) {
+              if (idx >= p.num_records || !p.has_invalid) errbits |= 1u;
+              idx = -1;
+            }
           }
         }
-        if (gi == 0) TL(1, 1);
+        if (warp == 6 && lane == 0) TL(1, 1);
         uint4 v[21];
 #pragma unroll
-        for (int i = 0; i < 21; ++i) {
-          const int c = c_lo + i;
-          v[i] = (valid && c < c_hi) ? *reinterpret_cast<const uint4*>(src + 16 * c) : make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < 16; ++i) {
+          const int ri = __shfl_sync(0xFFFFFFFFu, idx, i);
+          v[i] = (ri >= 0) ? *reinterpret_cast<const uint4*>(p.records + static_cast<int64_t>(ri) * p.rec_stride + 16 * lane)
+                           : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < 5; ++u) {
+          const int f = 32 * u + lane, rr = f / 9, c = 32 + f - 9 * rr;
+          const int ri = __shfl_sync(0xFFFFFFFFu, idx, rr & 15);
+          v[16 + u] = (f < 144 && ri >= 0)
+                          ? *reinterpret_cast<const uint4*>(p.records + static_cast<int64_t>(ri) * p.rec_stride + 16 * c)
+                          : make_uint4(0, 0, 0, 0);
         }
         // tile gt reuses the slots of tile gt - 2
         if (gt >= 2 && !warp_wait(&pv_done[gt & 1], static_cast<uint32_t>((gt - 2) >> 1) & 1u, abort_flag)) {
           ok = false;
           break;
         }
-        if (gi == 0) TL(1, 2);
+        if (warp == 6 && lane == 0) TL(1, 2);
+        {
+          uint8_t* codes = ring + ((gt & 1) * NB + (lane >> 3)) * kSlotBytes;
 #pragma unroll
-        for (int i = 0; i < 21; ++i) {
-          const int c = c_lo + i;
-          if (c >= c_hi) continue;
-          if (c < 32) {
-            const int j = c >> 3, cc = c & 7;
-            *reinterpret_cast<uint4*>(ring + ((gt & 1) * NB + j) * kSlotBytes + sw128(r, cc)) = v[i];
-          } else if (c == 32) {
-            *reinterpret_cast<uint4*>(scl + (gt & 1) * kTile + r) = v[i];
-          } else {
-            *reinterpret_cast<uint4*>(ring + ((gt & 1) * NB + 4) * kSlotBytes + sw128(r, c - 33)) = v[i];
+          for (int i = 0; i < 16; ++i) *reinterpret_cast<uint4*>(codes + sw128(rbase + i, lane & 7)) = v[i];
+        }
+#pragma unroll
+        for (int u = 0; u < 5; ++u) {
+          const int f = 32 * u + lane, rr = f / 9, c = 32 + f - 9 * rr;
+          if (f < 144) {
+            const int r = rbase + rr;
+            if (c == 32)
+              *reinterpret_cast<uint4*>(scl + (gt & 1) * kTile + r) = v[16 + u];
+            else
+              *reinterpret_cast<uint4*>(ring + ((gt & 1) * NB + 4) * kSlotBytes + sw128(r, c - 33)) = v[16 + u];
           }
         }
-        if (h == 0) vrow[(gt & 1) * kTile + r] = valid ? 1 : 0;
+        if (lane < 16) vrow[(gt & 1) * kTile + rbase + lane] = (idx >= 0) ? 1 : 0;
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0)
           for (int b = 0; b < NB; ++b) mbar_arrive(&full[(gt & 1) * NB + b]);
-        if (gi == 0) TL(1, 3);
+        if (warp == 6 && lane == 0) TL(1, 3);
       }
       g += it.ntiles;
     }
