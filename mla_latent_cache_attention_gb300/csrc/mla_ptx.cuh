@@ -83,8 +83,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   if (mbar_try_wait(bar, parity)) return true;
   uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0) {
+    // suspended until the phase completes or ~2 us pass: a waiting warp takes no issue slots
+    if (mbar_try_wait_ns(bar, parity, 2000)) return true;
+    if ((it & 7u) == 0) {
       if (*abort_flag) return false;
       if (globaltimer() - t0 > kWaitNs) {
         *abort_flag = 2;
