@@ -30,8 +30,9 @@
 //     record with 16-byte vector loads (a record is 41 of them) and store it in the same
 //     layout; masked or out-of-range indices store zeros and a row flag.
 //
-// Warps: 0 scheduler (+ TMA producer for pages), 1 MMA issuer, 2..5 softmax + query
-// preparation + epilogue, 6..13 gather (sparse only).
+// Warps: 0 scheduler (+ TMA producer for pages), 1 MMA issuer (QK; for the sparse source also
+// PV), 2..5 softmax + query preparation + epilogue, then 6 PV issuer (pages) or 6..13 gather
+// (sparse).
 #pragma once
 #include "mla_paged_tma.cuh"
 
@@ -67,7 +68,10 @@ template <bool kSparse>
 struct DsCfg {
   static constexpr int NQ = 16, NB = 5, R = 10;        // a tile is 5 ring slots; the ring holds two
   static constexpr int kGatherWarps = kSparse ? 8 : 0;
-  static constexpr int kThreads = 192 + 32 * kGatherWarps;
+  // pages: a second MMA-issuing warp for PV (after the softmax warps); sparse: the QK warp
+  // issues PV too (a 15th warp cost more than it saved beside the gather warps)
+  static constexpr int kPvWarp = kSparse ? -1 : 6;
+  static constexpr int kThreads = 192 + 32 * kGatherWarps + (kSparse ? 0 : 32);
   static constexpr int kRing = 0;
   static constexpr int kScale = kRing + R * kSlotBytes;          // [2][128] float4
   static constexpr int kQ = kScale + 2 * kTile * 16;              // 4 x (32 rows x 128 B) hi/lo + 16 x 128 B rope
@@ -81,7 +85,7 @@ struct DsCfg {
   static constexpr int kValid = kRj + 4 * 8 * 4;                  // [2][128] row flags (sparse)
   static constexpr int kItems = kValid + 2 * kTile;
   static constexpr int kBar = kItems + kItemDepth * 32;
-  static constexpr int kNumBars = R + 8 + 2 * kItemDepth;
+  static constexpr int kNumBars = R + 9 + 2 * kItemDepth;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kTotal = kMisc + 16;
   static constexpr int kAlloc = kTotal + 1024;
@@ -131,6 +135,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
   uint64_t* s_free = bars + R + 7;        // the softmax has read S
   uint64_t* item_full = bars + R + 8;
   uint64_t* item_empty = item_full + kItemDepth;
+  uint64_t* fin_pv = item_empty + kItemDepth;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
 
@@ -148,10 +153,11 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
     mbar_init(p_full, 1);
     mbar_init(q_full, 1);
     mbar_init(fin, 1);
+    mbar_init(fin_pv, 1);
     mbar_init(s_free, 1);
     for (int k = 0; k < kItemDepth; ++k) {
       mbar_init(&item_full[k], 1);
-      mbar_init(&item_empty[k], 2 + C::kGatherWarps);
+      mbar_init(&item_empty[k], (kSparse ? 2 : 3) + C::kGatherWarps);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -292,107 +298,162 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
     errbits = __reduce_or_sync(0xFFFFFFFFu, errbits);
     if (lane == 0 && errbits) set_device_error(p.err, errbits);
   } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------------ QK issuer (TMEM owner)
     if (lane == 0) {
       const uint32_t ring_a = smem_u32(ring), q_a = smem_u32(qs), qr_a = smem_u32(qr), p_a = smem_u32(ps);
       const uint64_t dK0 = smem_desc(ring_a, 16, 1024, kSwizzle128B);
       const uint64_t dQ0 = smem_desc(q_a, 16, 1024, kSwizzle128B);
       const uint64_t dQr = smem_desc(qr_a, 16, 1024, kSwizzle128B);
-      const uint64_t dV0 = smem_desc(ring_a, kSlotBytes, 1024, kSwizzle128B);
-      const uint64_t dP0 = smem_desc(p_a, 512, 128, kSwizzleNone);
-      constexpr uint32_t kIdNope = idesc_e4m3(128, 32, 0, 0);
-      constexpr uint32_t kIdRope = idesc_f16(128, 16, 1, 1, 0, 0);
-      constexpr uint32_t kIdPv = idesc_e4m3(128, 64, 1, 1) | (1u << 10);   // B (weights) in e5m2
-      auto slot_of = [&](int gt, int b) -> int { return (gt & 1) * NB + b; };
-      auto issue_pv = [&](int gt, bool first) -> bool {
-        if (!mbar_wait(p_full, static_cast<uint32_t>(gt) & 1u, abort_flag)) return false;
-        tc_fence_after();
-        TL(2, 3);
+      if constexpr (kSparse) {
+        // one issuer: a ready PV goes to the tensor cores while QK waits for data
+        const uint64_t dV0 = smem_desc(ring_a, kSlotBytes, 1024, kSwizzle128B);
+        const uint64_t dP0 = smem_desc(p_a, 512, 128, kSwizzleNone);
+        constexpr uint32_t kIdNope = idesc_e4m3(128, 32, 0, 0);
+        constexpr uint32_t kIdRope = idesc_f16(128, 16, 1, 1, 0, 0);
+        constexpr uint32_t kIdPv = idesc_e4m3(128, 64, 1, 1) | (1u << 10);   // B (weights) in e5m2
+        auto slot_of = [&](int gt, int b) -> int { return (gt & 1) * NB + b; };
+        auto issue_pv = [&](int gt, bool first) -> bool {
+          if (!mbar_wait(p_full, static_cast<uint32_t>(gt) & 1u, abort_flag)) return false;
+          tc_fence_after();
+          TL(2, 3);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint64_t aV = dV0 + ((slot_of(gt, j) * kSlotBytes) >> 4);
-          const uint64_t bP = dP0 + ((j * kTile * 64) >> 4);
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t aV = dV0 + ((slot_of(gt, j) * kSlotBytes) >> 4);
+            const uint64_t bP = dP0 + ((j * kTile * 64) >> 4);
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_f8_ss(tmem + C::kTmemO + 64 * j, aV + ((kk * 4096) >> 4), bP + ((kk * 2048) >> 4), kIdPv,
-                      (!first || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(&pv_done[gt & 1]);
-        TL(2, 4);
-        return true;
-      };
-      int pv_gt = -1;          // PV still to issue (its P may be ready while QK waits for data)
-      bool pv_first = false;
-      auto issue_qk = [&](int gt) -> bool {
-        TL(2, 1);
-        // one S buffer: the softmax of the previous tile must have read it
-        if (gt > 0 && !mbar_wait(s_free, static_cast<uint32_t>(gt - 1) & 1u, abort_flag)) return false;
-        tc_fence_after();
-        TL(2, 5);
-        const uint32_t dS = tmem + C::kS;
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f8_ss(tmem + C::kTmemO + 64 * j, aV + ((kk * 4096) >> 4), bP + ((kk * 2048) >> 4), kIdPv,
+                        (!first || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&pv_done[gt & 1]);
+          TL(2, 4);
+          return true;
+        };
+        int pv_gt = -1;          // PV still to issue (its P may be ready while QK waits for data)
+        bool pv_first = false;
+        auto issue_qk = [&](int gt) -> bool {
+          TL(2, 1);
+          // one S buffer: the softmax of the previous tile must have read it
+          if (gt > 0 && !mbar_wait(s_free, static_cast<uint32_t>(gt - 1) & 1u, abort_flag)) return false;
+          tc_fence_after();
+          TL(2, 5);
+          const uint32_t dS = tmem + C::kS;
 #pragma unroll 1
-        for (int b = 0; b < NB; ++b) {
-          const int slot = slot_of(gt, b);
-          const uint32_t par = static_cast<uint32_t>(gt >> 1) & 1u;
-          if (pv_gt >= 0 && !mbar_test_wait(&full[slot], par)) {
-            const uint64_t t0 = globaltimer();
-            for (uint32_t spin = 0;; ++spin) {
-              if (mbar_test_wait(p_full, static_cast<uint32_t>(pv_gt) & 1u)) {
-                if (!issue_pv(pv_gt, pv_first)) return false;
-                pv_gt = -1;
-                break;
+          for (int b = 0; b < NB; ++b) {
+            const int slot = slot_of(gt, b);
+            const uint32_t par = static_cast<uint32_t>(gt >> 1) & 1u;
+            if (pv_gt >= 0 && !mbar_test_wait(&full[slot], par)) {
+              const uint64_t t0 = globaltimer();
+              for (uint32_t spin = 0;; ++spin) {
+                if (mbar_test_wait(p_full, static_cast<uint32_t>(pv_gt) & 1u)) {
+                  if (!issue_pv(pv_gt, pv_first)) return false;
+                  pv_gt = -1;
+                  break;
+                }
+                if (mbar_try_wait_ns(&full[slot], par, 200)) break;
+                if ((spin & 15u) == 15u && (*abort_flag || globaltimer() - t0 > kWaitNs)) break;   // the bounded wait below decides
               }
-              if (mbar_try_wait_ns(&full[slot], par, 200)) break;
-              if ((spin & 15u) == 15u && (*abort_flag || globaltimer() - t0 > kWaitNs)) break;   // the bounded wait below decides
+            }
+            if (!mbar_wait(&full[slot], par, abort_flag)) return false;
+            tc_fence_after();
+            const uint64_t aK = dK0 + ((slot * kSlotBytes) >> 4);
+            if (b < 4) {
+              const uint64_t bQ = dQ0 + ((b * 32 * 128) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f8_ss(dS + 32 * b, aK + ((kk * 32) >> 4), bQ + ((kk * 32) >> 4), kIdNope, kk > 0 ? 1u : 0u);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f16_ss(dS + 128, aK + ((kk * 32) >> 4), dQr + ((kk * 32) >> 4), kIdRope, kk > 0 ? 1u : 0u);
             }
           }
-          if (!mbar_wait(&full[slot], par, abort_flag)) return false;
+          mma_commit(&s_full[0]);
+          TL(2, 2);
+          return true;
+        };
+        bool ok = true;
+        int nit = 0, nq = 0, g = 0;
+        while (ok) {
+          const int k = nit % kItemDepth;
+          if (!mbar_wait(&item_full[k], (nit / kItemDepth) & 1, abort_flag)) break;
+          const WorkItem it = items[k];
+          mbar_arrive(&item_empty[k]);
+          ++nit;
+          if (it.b < 0) break;
+          if (it.ntiles == 0) continue;
+          if (!mbar_wait(q_full, nq & 1, abort_flag)) break;
+          ++nq;
           tc_fence_after();
-          const uint64_t aK = dK0 + ((slot * kSlotBytes) >> 4);
-          if (b < 4) {
-            const uint64_t bQ = dQ0 + ((b * 32 * 128) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f8_ss(dS + 32 * b, aK + ((kk * 32) >> 4), bQ + ((kk * 32) >> 4), kIdNope, kk > 0 ? 1u : 0u);
-          } else {
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ss(dS + 128, aK + ((kk * 32) >> 4), dQr + ((kk * 32) >> 4), kIdRope, kk > 0 ? 1u : 0u);
+          ok = issue_qk(g);
+          pv_gt = g;
+          pv_first = true;
+          for (int t = 1; t < it.ntiles && ok; ++t) {
+            ok = issue_qk(g + t);
+            if (ok && pv_gt >= 0) ok = issue_pv(pv_gt, pv_first);
+            pv_gt = g + t;
+            pv_first = false;
           }
-        }
-        mma_commit(&s_full[0]);
-        TL(2, 2);
-        return true;
-      };
-      bool ok = true;
-      int nit = 0, nq = 0, g = 0;
-      while (ok) {
-        const int k = nit % kItemDepth;
-        if (!mbar_wait(&item_full[k], (nit / kItemDepth) & 1, abort_flag)) break;
-        const WorkItem it = items[k];
-        mbar_arrive(&item_empty[k]);
-        ++nit;
-        if (it.b < 0) break;
-        if (it.ntiles == 0) continue;
-        if (!mbar_wait(q_full, nq & 1, abort_flag)) break;
-        ++nq;
-        tc_fence_after();
-        ok = issue_qk(g);
-        pv_gt = g;
-        pv_first = true;
-        for (int t = 1; t < it.ntiles && ok; ++t) {
-          ok = issue_qk(g + t);
           if (ok && pv_gt >= 0) ok = issue_pv(pv_gt, pv_first);
-          pv_gt = g + t;
-          pv_first = false;
+          pv_gt = -1;
+          g += it.ntiles;
         }
-        if (ok && pv_gt >= 0) ok = issue_pv(pv_gt, pv_first);
-        pv_gt = -1;
-        g += it.ntiles;
+        mma_commit(fin);
+        volatile int no_abort = 0;
+        mbar_wait(fin, 0, &no_abort);
+      } else {
+        // QK only; the PV warp issues PV
+        constexpr uint32_t kIdNope = idesc_e4m3(128, 32, 0, 0);
+        constexpr uint32_t kIdRope = idesc_f16(128, 16, 1, 1, 0, 0);
+        auto slot_of = [&](int gt, int b) -> int { return (gt & 1) * NB + b; };
+        auto issue_qk = [&](int gt) -> bool {
+          TL(2, 1);
+          // one S buffer: the softmax of the previous tile must have read it
+          if (gt > 0 && !mbar_wait(s_free, static_cast<uint32_t>(gt - 1) & 1u, abort_flag)) return false;
+          tc_fence_after();
+          TL(2, 5);
+          const uint32_t dS = tmem + C::kS;
+#pragma unroll 1
+          for (int b = 0; b < NB; ++b) {
+            const int slot = slot_of(gt, b);
+            if (!mbar_wait(&full[slot], static_cast<uint32_t>(gt >> 1) & 1u, abort_flag)) return false;
+            tc_fence_after();
+            const uint64_t aK = dK0 + ((slot * kSlotBytes) >> 4);
+            if (b < 4) {
+              const uint64_t bQ = dQ0 + ((b * 32 * 128) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f8_ss(dS + 32 * b, aK + ((kk * 32) >> 4), bQ + ((kk * 32) >> 4), kIdNope, kk > 0 ? 1u : 0u);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f16_ss(dS + 128, aK + ((kk * 32) >> 4), dQr + ((kk * 32) >> 4), kIdRope, kk > 0 ? 1u : 0u);
+            }
+          }
+          mma_commit(&s_full[0]);
+          TL(2, 2);
+          return true;
+        };
+        bool ok = true;
+        int nit = 0, nq = 0, g = 0;
+        while (ok) {
+          const int k = nit % kItemDepth;
+          if (!mbar_wait(&item_full[k], (nit / kItemDepth) & 1, abort_flag)) break;
+          const WorkItem it = items[k];
+          mbar_arrive(&item_empty[k]);
+          ++nit;
+          if (it.b < 0) break;
+          if (it.ntiles == 0) continue;
+          if (!mbar_wait(q_full, nq & 1, abort_flag)) break;
+          ++nq;
+          tc_fence_after();
+          for (int t = 0; t < it.ntiles && ok; ++t) ok = issue_qk(g + t);
+          g += it.ntiles;
+        }
+        mma_commit(fin);
+        volatile int no_abort = 0;
+        mbar_wait(fin, 0, &no_abort);
       }
-      mma_commit(fin);
-      volatile int no_abort = 0;
-      mbar_wait(fin, 0, &no_abort);
     }
     __syncwarp();
   } else if (warp < 6) {
@@ -768,6 +829,50 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
       named_bar_sync(1, NT);
       if (stid == 0) mbar_arrive(&item_empty[k]);
     }
+  } else if (warp == C::kPvWarp) {
+    // ------------------------------------------------------------------ PV issuer
+    // A second MMA-issuing thread: PV(t) goes to the tensor cores as soon as P(t) is written,
+    // in parallel with the QK of the next tile (a commit tracks the issuing thread's MMAs).
+    if (lane == 0) {
+      const uint64_t dV0 = smem_desc(smem_u32(ring), kSlotBytes, 1024, kSwizzle128B);
+      const uint64_t dP0 = smem_desc(smem_u32(ps), 512, 128, kSwizzleNone);
+      constexpr uint32_t kIdPv = idesc_e4m3(128, 64, 1, 1) | (1u << 10);   // B (weights) in e5m2
+      bool ok = true;
+      int nit = 0, g = 0;
+      while (ok) {
+        const int k = nit % kItemDepth;
+        if (!mbar_wait(&item_full[k], (nit / kItemDepth) & 1, abort_flag)) break;
+        const WorkItem it = items[k];
+        mbar_arrive(&item_empty[k]);
+        ++nit;
+        if (it.b < 0) break;
+        for (int t = 0; t < it.ntiles && ok; ++t) {
+          const int gt = g + t;
+          if (!mbar_wait(p_full, static_cast<uint32_t>(gt) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          TL(2, 3);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint64_t aV = dV0 + ((((gt & 1) * NB + j) * kSlotBytes) >> 4);
+            const uint64_t bP = dP0 + ((j * kTile * 64) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f8_ss(tmem + C::kTmemO + 64 * j, aV + ((kk * 4096) >> 4), bP + ((kk * 2048) >> 4), kIdPv,
+                        (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&pv_done[gt & 1]);
+          TL(2, 4);
+        }
+        g += it.ntiles;
+      }
+      mma_commit(fin_pv);
+      volatile int no_abort = 0;
+      mbar_wait(fin_pv, 0, &no_abort);
+    }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------------ gather (sparse)
     // Gather warp w (0..7) loads records 16 w .. 16 w + 15 of the tile; a record is 41 16-byte
