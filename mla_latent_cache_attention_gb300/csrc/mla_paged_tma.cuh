@@ -41,6 +41,7 @@
 //   MLA_LOOKAHEAD    tiles between a page-table lookup and the tile's loads
 //   MLA_L2PF         also prefetch that tile into L2 when its pages are known
 //   MLA_SLOT_COMMITS release each ring slot by its own commit (else by PV of its tile)
+//   MLA_PV_WARP      PV issued by a warp of its own (else by the QK issuer)
 #ifndef MLA_OVERLAP_FP8
 #define MLA_OVERLAP_FP8 1
 #endif
@@ -52,6 +53,9 @@
 #endif
 #ifndef MLA_SLOT_COMMITS
 #define MLA_SLOT_COMMITS 1
+#endif
+#ifndef MLA_PV_WARP
+#define MLA_PV_WARP 1
 #endif
 
 namespace mla {
@@ -95,7 +99,9 @@ struct PagedCfg {
   static constexpr int kRope = F == kBF16 ? 8 : 4;       // block used by QK only
   static constexpr int kSW = NQ == 64 ? 8 : 4;           // softmax warps
   static constexpr int kNC = NQ * 4 / kSW;               // columns per softmax thread
-  static constexpr int kThreads = 64 + 32 * kSW;
+  static constexpr bool kPvSplit = MLA_PV_WARP;
+  static constexpr int kPvWarp = kPvSplit ? 2 + kSW : -1;   // after the softmax warps
+  static constexpr int kThreads = 64 + 32 * kSW + (kPvSplit ? 32 : 0);
   static constexpr bool kOverlap = (F == kFP8 || KM == 64) && MLA_OVERLAP_FP8;
   static constexpr int kPfDist = MLA_LOOKAHEAD;           // tiles between a page lookup and its use
   static constexpr bool kL2Pf = MLA_L2PF;
@@ -118,7 +124,7 @@ struct PagedCfg {
   static constexpr int kRed = kP + kPBytes;
   static constexpr int kItems = kRed + kRedBytes;
   static constexpr int kBar = kItems + kItemDepth * 32;
-  static constexpr int kNumBars = 2 * kR + 8 + 2 * kItemDepth;
+  static constexpr int kNumBars = 2 * kR + 10 + 2 * kItemDepth;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kTotal = kMisc + 16;
   static constexpr int kAlloc = kTotal + 1024;
@@ -252,6 +258,8 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
   uint64_t* item_full = bars + R + 8;
   uint64_t* item_empty = item_full + kItemDepth;
   uint64_t* empty = item_empty + kItemDepth;  // [R] slot consumed (per-slot release)
+  uint64_t* fin_pv = bars + R + 7;
+  uint64_t* s_free = empty + R;           // [2] the softmax has read S[t & 1] (PV warp split)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
 
@@ -276,9 +284,12 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
     mbar_init(p_full, 1);
     mbar_init(q_full, 1);
     mbar_init(fin, 1);
+    mbar_init(fin_pv, 1);
+    mbar_init(&s_free[0], 1);
+    mbar_init(&s_free[1], 1);
     for (int k = 0; k < kItemDepth; ++k) {
       mbar_init(&item_full[k], 1);
-      mbar_init(&item_empty[k], 2);
+      mbar_init(&item_empty[k], C::kPvSplit ? 3 : 2);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -549,6 +560,10 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
       auto issue_qk = [&](int gt, bool last) -> bool {
         const uint32_t dS = tmem + C::kTmemS + (gt & 1) * NQ;
         TL(2, 1);
+        // the PV warp runs on its own: S[gt & 1] must have been read for tile gt - 2
+        if (C::kPvSplit && gt >= 2 &&
+            !mbar_wait(&s_free[gt & 1], static_cast<uint32_t>((gt - 2) >> 1) & 1u, abort_flag))
+          return false;
 #pragma unroll 1
         for (int b = 0; b < NB; ++b) {
           const int slot = slot_of(gt, b);
@@ -602,7 +617,9 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
         if (!mbar_wait(q_full, nq & 1, abort_flag)) break;
         ++nq;
         tc_fence_after();
-        if (C::kOverlap) {
+        if (C::kPvSplit) {
+          for (int t = 0; t < it.ntiles && ok; ++t) ok = issue_qk(g + t, t == it.ntiles - 1);
+        } else if (C::kOverlap) {
           ok = issue_qk(g, it.ntiles == 1);
           for (int t = 1; t < it.ntiles && ok; ++t) {
             pv_gt = g + t - 1;
@@ -623,6 +640,65 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
       mma_commit(fin);
       volatile int no_abort = 0;
       mbar_wait(fin, 0, &no_abort);
+    }
+    __syncwarp();
+  } else if (warp == C::kPvWarp) {
+    // ------------------------------------------------------------------ PV issuer
+    // A second MMA-issuing thread: PV(t) goes to the tensor cores as soon as P(t) is written,
+    // in parallel with the next QK (a commit tracks the MMAs of its issuing thread).
+    if (lane == 0) {
+      const uint64_t dV0 = smem_desc(smem_u32(ring), C::kSlot, 1024, kSwizzle128B);
+      constexpr uint32_t kPLbo = F == kBF16 ? NQ * 16 : NQ * 8;   // 8-key groups of P
+      const uint64_t dP0 = smem_desc(smem_u32(ps), kPLbo, 128, kSwizzleNone);
+      constexpr uint32_t kIdPv = F == kBF16 ? idesc_f16(128, NQ, 1, 1, 1, 1) : idesc_e4m3(128, NQ, 1, 1);
+      auto slot_of = [&](int gt, int b) -> int { return static_cast<int>((static_cast<int64_t>(gt) * NB + b) % R); };
+      bool ok = true;
+      int nit = 0, g = 0;
+      while (ok) {
+        const int k = nit % kItemDepth;
+        if (!mbar_wait(&item_full[k], (nit / kItemDepth) & 1, abort_flag)) break;
+        const WorkItem it = items[k];
+        mbar_arrive(&item_empty[k]);
+        ++nit;
+        if (it.b < 0) break;
+        for (int t = 0; t < it.ntiles && ok; ++t) {
+          const int gt = g + t;
+          const bool first = (t == 0);
+          if (!mbar_wait(p_full, static_cast<uint32_t>(gt) & 1u, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t dO = tmem + C::kTmemO + j * NQ;
+            if (F == kBF16) {
+              const uint64_t aV = dV0 + ((slot_of(gt, 2 * j) * C::kSlot) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < KM / 16; ++kk)
+                mma_f16_ss(dO, aV + ((kk * 2048) >> 4), dP0 + ((kk * NQ * 32) >> 4), kIdPv, (!first || kk > 0) ? 1u : 0u);
+              if (C::kSlotCommits) {
+                mma_commit(&empty[slot_of(gt, 2 * j)]);
+                mma_commit(&empty[slot_of(gt, 2 * j + 1)]);
+              }
+            } else {
+              const uint64_t aV = dV0 + ((slot_of(gt, j) * C::kSlot) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < KM / 32; ++kk) {
+                const uint64_t pb = dP0 + ((kk * NQ * 32) >> 4);
+                mma_f8_ss(dO, aV + ((kk * 4096) >> 4), pb, kIdPv, (!first || kk > 0) ? 1u : 0u);
+                mma_f8_ss(dO, aV + ((kk * 4096) >> 4), pb + ((KM * NQ) >> 4), kIdPv, 1u);
+              }
+              if (C::kSlotCommits) mma_commit(&empty[slot_of(gt, j)]);
+            }
+          }
+          mma_commit(&pv_done[gt & 1]);
+        }
+        g += it.ntiles;
+      }
+      mma_commit(fin_pv);
+      volatile int no_abort = 0;
+      mbar_wait(fin_pv, 0, &no_abort);
     }
     __syncwarp();
   } else {
@@ -651,7 +727,7 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
     constexpr float kTau = F == kFP8 ? 4.f : 8.f;
     // row sums: per thread and column when registers allow (6 warps), else per warp and
     // column (lane % NC), reduced over the warp each tile
-    constexpr bool kLReg = C::kThreads <= 192;
+    constexpr bool kLReg = C::kSW == 4;
     constexpr int NL = kLReg ? NC : 1;
     constexpr float kPExp = F == kFP8 ? 4.f : 0.f;   // fp8: p carried as 2^4 p, at most 2^8 (e4m3 max 448)
     int nit = 0, g = 0;
@@ -713,7 +789,9 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
         }
         if (stid == 0) TL(3, 10);
         // one barrier decides: nothing to do (common), or move the reference (or abort)
+        if (C::kPvSplit) tc_fence_before();
         const bool rare = named_bar_or(1, NT, need || !w);
+        if (C::kPvSplit && stid == 0) mbar_arrive(&s_free[gt & 1]);     // every thread has read S
         bool pv_waited = false;
         if (rare) {
           ok = named_bar_and(1, NT, w);
