@@ -30,9 +30,9 @@
 //     record with 16-byte vector loads (a record is 41 of them) and store it in the same
 //     layout; masked or out-of-range indices store zeros and a row flag.
 //
-// Warps: 0 scheduler (+ TMA producer for pages), 1 MMA issuer (QK; for the sparse source also
-// PV), 2..5 softmax + query preparation + epilogue, then 6 PV issuer (pages) or 6..13 gather
-// (sparse).
+// Warps: 0 scheduler (+ TMA producer for pages; + PV issuer for the sparse source), 1 QK issuer
+// (TMEM owner), 2..5 softmax + query preparation + epilogue, then 6 PV issuer (pages) or
+// 6..13 gather (sparse).
 #pragma once
 #include "mla_paged_tma.cuh"
 
@@ -68,8 +68,8 @@ template <bool kSparse>
 struct DsCfg {
   static constexpr int NQ = 16, NB = 5, R = 10;        // a tile is 5 ring slots; the ring holds two
   static constexpr int kGatherWarps = kSparse ? 8 : 0;
-  // pages: a second MMA-issuing warp for PV (after the softmax warps); sparse: the QK warp
-  // issues PV too (a 15th warp cost more than it saved beside the gather warps)
+  // PV has its own issuing thread: pages, warp 6 (after the softmax warps); sparse, lane 0 of
+  // the scheduler warp (a 15th warp beside the gather warps cost more than it saved)
   static constexpr int kPvWarp = kSparse ? -1 : 6;
   static constexpr int kThreads = 192 + 32 * kGatherWarps + (kSparse ? 0 : 32);
   static constexpr int kRing = 0;
@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
     mbar_init(s_free, 1);
     for (int k = 0; k < kItemDepth; ++k) {
       mbar_init(&item_full[k], 1);
-      mbar_init(&item_empty[k], (kSparse ? 2 : 3) + C::kGatherWarps);
+      mbar_init(&item_empty[k], 3 + C::kGatherWarps);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -194,7 +194,96 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
     return it.n > 0 || p.n_splits == 1;
   };
 
-  if (warp == 0) {
+  if (warp == 0 && kSparse) {
+    // ------------------------------------------------------------------ scheduler + PV issuer
+    // Sparse source: warp 0 has no pages to load, so its lane 0 both hands out work items and
+    // issues PV(t) as soon as P(t) is written (a second MMA-issuing thread beside the QK warp;
+    // a commit tracks its issuing thread).  It polls both sides and never blocks on one.
+    if (lane == 0) {
+      int stride_k = 0;
+      auto take = [&]() -> int {
+        const int item = p.sched ? static_cast<int>(atomicAdd(p.sched, 1u)) : static_cast<int>(blockIdx.x + stride_k * gridDim.x);
+        ++stride_k;
+        return item;
+      };
+      auto next_item = [&]() -> WorkItem {
+        WorkItem it{};
+        while (!decode(take(), it)) {
+        }
+        return it;
+      };
+      const uint64_t dV0 = smem_desc(smem_u32(ring), kSlotBytes, 1024, kSwizzle128B);
+      const uint64_t dP0 = smem_desc(smem_u32(ps), 512, 128, kSwizzleNone);
+      constexpr uint32_t kIdPv = idesc_e4m3(128, 64, 1, 1) | (1u << 10);   // B (weights) in e5m2
+      WorkItem cur = next_item(), pit{};
+      int npush = 0, npv = 0, pv_t = 0, pv_g = 0;
+      bool push_done = false, have = false;
+      uint64_t t_last = globaltimer();
+      for (;;) {
+        bool prog = false;
+        if (!push_done) {
+          const int k = npush % kItemDepth;
+          if (npush < kItemDepth || mbar_test_wait(&item_empty[k], static_cast<uint32_t>((npush / kItemDepth) - 1) & 1u)) {
+            items[k] = cur;
+            mbar_arrive(&item_full[k]);
+            ++npush;
+            if (cur.b < 0)
+              push_done = true;
+            else
+              cur = next_item();
+            prog = true;
+          }
+        }
+        if (!have) {
+          const int k = npv % kItemDepth;
+          if (npv < npush && mbar_test_wait(&item_full[k], static_cast<uint32_t>(npv / kItemDepth) & 1u)) {
+            pit = items[k];
+            mbar_arrive(&item_empty[k]);
+            ++npv;
+            prog = true;
+            if (pit.b < 0) break;
+            have = true;
+            pv_t = 0;
+          }
+        } else if (pv_t < pit.ntiles) {
+          const int gt = pv_g + pv_t;
+          if (mbar_test_wait(p_full, static_cast<uint32_t>(gt) & 1u)) {
+            tc_fence_after();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const uint64_t aV = dV0 + ((((gt & 1) * NB + j) * kSlotBytes) >> 4);
+              const uint64_t bP = dP0 + ((j * kTile * 64) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f8_ss(tmem + C::kTmemO + 64 * j, aV + ((kk * 4096) >> 4), bP + ((kk * 2048) >> 4), kIdPv,
+                          (pv_t > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&pv_done[gt & 1]);
+            ++pv_t;
+            prog = true;
+          }
+        } else {
+          pv_g += pit.ntiles;
+          have = false;
+          prog = true;
+        }
+        if (prog) {
+          t_last = globaltimer();
+        } else {
+          if (*abort_flag) break;
+          if (globaltimer() - t_last > kWaitNs) {
+            *abort_flag = 2;
+            break;
+          }
+          if (have && pv_t < pit.ntiles) (void)mbar_try_wait_ns(p_full, static_cast<uint32_t>(pv_g + pv_t) & 1u, 500);
+        }
+      }
+      mma_commit(fin_pv);
+      volatile int no_abort = 0;
+      mbar_wait(fin_pv, 0, &no_abort);
+    }
+    __syncwarp();
+  } else if (warp == 0) {
     // ------------------------------------------------------------------ scheduler / page producer
     uint32_t errbits = 0;
     int nitem = 0, stride_k = 0, gt_next = 0;
@@ -300,160 +389,61 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------------ QK issuer (TMEM owner)
     if (lane == 0) {
-      const uint32_t ring_a = smem_u32(ring), q_a = smem_u32(qs), qr_a = smem_u32(qr), p_a = smem_u32(ps);
+      const uint32_t ring_a = smem_u32(ring), q_a = smem_u32(qs), qr_a = smem_u32(qr);
       const uint64_t dK0 = smem_desc(ring_a, 16, 1024, kSwizzle128B);
       const uint64_t dQ0 = smem_desc(q_a, 16, 1024, kSwizzle128B);
       const uint64_t dQr = smem_desc(qr_a, 16, 1024, kSwizzle128B);
-      if constexpr (kSparse) {
-        // one issuer: a ready PV goes to the tensor cores while QK waits for data
-        const uint64_t dV0 = smem_desc(ring_a, kSlotBytes, 1024, kSwizzle128B);
-        const uint64_t dP0 = smem_desc(p_a, 512, 128, kSwizzleNone);
-        constexpr uint32_t kIdNope = idesc_e4m3(128, 32, 0, 0);
-        constexpr uint32_t kIdRope = idesc_f16(128, 16, 1, 1, 0, 0);
-        constexpr uint32_t kIdPv = idesc_e4m3(128, 64, 1, 1) | (1u << 10);   // B (weights) in e5m2
-        auto slot_of = [&](int gt, int b) -> int { return (gt & 1) * NB + b; };
-        auto issue_pv = [&](int gt, bool first) -> bool {
-          if (!mbar_wait(p_full, static_cast<uint32_t>(gt) & 1u, abort_flag)) return false;
+      // QK only; PV goes to its own issuing thread
+      constexpr uint32_t kIdNope = idesc_e4m3(128, 32, 0, 0);
+      constexpr uint32_t kIdRope = idesc_f16(128, 16, 1, 1, 0, 0);
+      auto slot_of = [&](int gt, int b) -> int { return (gt & 1) * NB + b; };
+      auto issue_qk = [&](int gt) -> bool {
+        TL(2, 1);
+        // one S buffer: the softmax of the previous tile must have read it
+        if (gt > 0 && !mbar_wait(s_free, static_cast<uint32_t>(gt - 1) & 1u, abort_flag)) return false;
+        tc_fence_after();
+        TL(2, 5);
+        const uint32_t dS = tmem + C::kS;
+#pragma unroll 1
+        for (int b = 0; b < NB; ++b) {
+          const int slot = slot_of(gt, b);
+          if (!mbar_wait(&full[slot], static_cast<uint32_t>(gt >> 1) & 1u, abort_flag)) return false;
           tc_fence_after();
-          TL(2, 3);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint64_t aV = dV0 + ((slot_of(gt, j) * kSlotBytes) >> 4);
-            const uint64_t bP = dP0 + ((j * kTile * 64) >> 4);
+          const uint64_t aK = dK0 + ((slot * kSlotBytes) >> 4);
+          if (b < 4) {
+            const uint64_t bQ = dQ0 + ((b * 32 * 128) >> 4);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_f8_ss(tmem + C::kTmemO + 64 * j, aV + ((kk * 4096) >> 4), bP + ((kk * 2048) >> 4), kIdPv,
-                        (!first || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&pv_done[gt & 1]);
-          TL(2, 4);
-          return true;
-        };
-        int pv_gt = -1;          // PV still to issue (its P may be ready while QK waits for data)
-        bool pv_first = false;
-        auto issue_qk = [&](int gt) -> bool {
-          TL(2, 1);
-          // one S buffer: the softmax of the previous tile must have read it
-          if (gt > 0 && !mbar_wait(s_free, static_cast<uint32_t>(gt - 1) & 1u, abort_flag)) return false;
-          tc_fence_after();
-          TL(2, 5);
-          const uint32_t dS = tmem + C::kS;
-#pragma unroll 1
-          for (int b = 0; b < NB; ++b) {
-            const int slot = slot_of(gt, b);
-            const uint32_t par = static_cast<uint32_t>(gt >> 1) & 1u;
-            if (pv_gt >= 0 && !mbar_test_wait(&full[slot], par)) {
-              const uint64_t t0 = globaltimer();
-              for (uint32_t spin = 0;; ++spin) {
-                if (mbar_test_wait(p_full, static_cast<uint32_t>(pv_gt) & 1u)) {
-                  if (!issue_pv(pv_gt, pv_first)) return false;
-                  pv_gt = -1;
-                  break;
-                }
-                if (mbar_try_wait_ns(&full[slot], par, 200)) break;
-                if ((spin & 15u) == 15u && (*abort_flag || globaltimer() - t0 > kWaitNs)) break;   // the bounded wait below decides
-              }
-            }
-            if (!mbar_wait(&full[slot], par, abort_flag)) return false;
-            tc_fence_after();
-            const uint64_t aK = dK0 + ((slot * kSlotBytes) >> 4);
-            if (b < 4) {
-              const uint64_t bQ = dQ0 + ((b * 32 * 128) >> 4);
+              mma_f8_ss(dS + 32 * b, aK + ((kk * 32) >> 4), bQ + ((kk * 32) >> 4), kIdNope, kk > 0 ? 1u : 0u);
+          } else {
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f8_ss(dS + 32 * b, aK + ((kk * 32) >> 4), bQ + ((kk * 32) >> 4), kIdNope, kk > 0 ? 1u : 0u);
-            } else {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f16_ss(dS + 128, aK + ((kk * 32) >> 4), dQr + ((kk * 32) >> 4), kIdRope, kk > 0 ? 1u : 0u);
-            }
+            for (int kk = 0; kk < 4; ++kk)
+              mma_f16_ss(dS + 128, aK + ((kk * 32) >> 4), dQr + ((kk * 32) >> 4), kIdRope, kk > 0 ? 1u : 0u);
           }
-          mma_commit(&s_full[0]);
-          TL(2, 2);
-          return true;
-        };
-        bool ok = true;
-        int nit = 0, nq = 0, g = 0;
-        while (ok) {
-          const int k = nit % kItemDepth;
-          if (!mbar_wait(&item_full[k], (nit / kItemDepth) & 1, abort_flag)) break;
-          const WorkItem it = items[k];
-          mbar_arrive(&item_empty[k]);
-          ++nit;
-          if (it.b < 0) break;
-          if (it.ntiles == 0) continue;
-          if (!mbar_wait(q_full, nq & 1, abort_flag)) break;
-          ++nq;
-          tc_fence_after();
-          ok = issue_qk(g);
-          pv_gt = g;
-          pv_first = true;
-          for (int t = 1; t < it.ntiles && ok; ++t) {
-            ok = issue_qk(g + t);
-            if (ok && pv_gt >= 0) ok = issue_pv(pv_gt, pv_first);
-            pv_gt = g + t;
-            pv_first = false;
-          }
-          if (ok && pv_gt >= 0) ok = issue_pv(pv_gt, pv_first);
-          pv_gt = -1;
-          g += it.ntiles;
         }
-        mma_commit(fin);
-        volatile int no_abort = 0;
-        mbar_wait(fin, 0, &no_abort);
-      } else {
-        // QK only; the PV warp issues PV
-        constexpr uint32_t kIdNope = idesc_e4m3(128, 32, 0, 0);
-        constexpr uint32_t kIdRope = idesc_f16(128, 16, 1, 1, 0, 0);
-        auto slot_of = [&](int gt, int b) -> int { return (gt & 1) * NB + b; };
-        auto issue_qk = [&](int gt) -> bool {
-          TL(2, 1);
-          // one S buffer: the softmax of the previous tile must have read it
-          if (gt > 0 && !mbar_wait(s_free, static_cast<uint32_t>(gt - 1) & 1u, abort_flag)) return false;
-          tc_fence_after();
-          TL(2, 5);
-          const uint32_t dS = tmem + C::kS;
-#pragma unroll 1
-          for (int b = 0; b < NB; ++b) {
-            const int slot = slot_of(gt, b);
-            if (!mbar_wait(&full[slot], static_cast<uint32_t>(gt >> 1) & 1u, abort_flag)) return false;
-            tc_fence_after();
-            const uint64_t aK = dK0 + ((slot * kSlotBytes) >> 4);
-            if (b < 4) {
-              const uint64_t bQ = dQ0 + ((b * 32 * 128) >> 4);
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f8_ss(dS + 32 * b, aK + ((kk * 32) >> 4), bQ + ((kk * 32) >> 4), kIdNope, kk > 0 ? 1u : 0u);
-            } else {
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f16_ss(dS + 128, aK + ((kk * 32) >> 4), dQr + ((kk * 32) >> 4), kIdRope, kk > 0 ? 1u : 0u);
-            }
-          }
-          mma_commit(&s_full[0]);
-          TL(2, 2);
-          return true;
-        };
-        bool ok = true;
-        int nit = 0, nq = 0, g = 0;
-        while (ok) {
-          const int k = nit % kItemDepth;
-          if (!mbar_wait(&item_full[k], (nit / kItemDepth) & 1, abort_flag)) break;
-          const WorkItem it = items[k];
-          mbar_arrive(&item_empty[k]);
-          ++nit;
-          if (it.b < 0) break;
-          if (it.ntiles == 0) continue;
-          if (!mbar_wait(q_full, nq & 1, abort_flag)) break;
-          ++nq;
-          tc_fence_after();
-          for (int t = 0; t < it.ntiles && ok; ++t) ok = issue_qk(g + t);
-          g += it.ntiles;
-        }
-        mma_commit(fin);
-        volatile int no_abort = 0;
-        mbar_wait(fin, 0, &no_abort);
+        mma_commit(&s_full[0]);
+        TL(2, 2);
+        return true;
+      };
+      bool ok = true;
+      int nit = 0, nq = 0, g = 0;
+      while (ok) {
+        const int k = nit % kItemDepth;
+        if (!mbar_wait(&item_full[k], (nit / kItemDepth) & 1, abort_flag)) break;
+        const WorkItem it = items[k];
+        mbar_arrive(&item_empty[k]);
+        ++nit;
+        if (it.b < 0) break;
+        if (it.ntiles == 0) continue;
+        if (!mbar_wait(q_full, nq & 1, abort_flag)) break;
+        ++nq;
+        tc_fence_after();
+        for (int t = 0; t < it.ntiles && ok; ++t) ok = issue_qk(g + t);
+        g += it.ntiles;
       }
+      mma_commit(fin);
+      volatile int no_abort = 0;
+      mbar_wait(fin, 0, &no_abort);
     }
     __syncwarp();
   } else if (warp < 6) {
