@@ -53,7 +53,7 @@ def peaks():
 class Work:
     """Host inputs of one workload plus its byte / row accounting."""
 
-    def __init__(self, name: str, batch: int = 0):
+    def __init__(self, name: str, batch: int = 0, records: int = 0):
         from mla_latent_cache_attention_gb300 import synth
         self.name = name
         self.synth = synth
@@ -64,7 +64,12 @@ class Work:
             self.case, self.epi = synth.config1(**kw)
             self.kind = "paged"
         elif name == "sparse_prefill":
-            self.case = synth.config2(**(dict(T=batch) if batch > 0 else {}))
+            # records > 0: a record pool of that size (2^22 records, 2.75 GB, is past L2, so the
+            # gathered records come from DRAM instead of L2)
+            kw2 = dict(T=batch) if batch > 0 else {}
+            if records > 0:
+                kw2["N"] = records
+            self.case = synth.config2(**kw2)
             self.kind = "sparse"
         elif name == "fp8_spec_verify":
             self.case = synth.config3(**kw)
@@ -248,7 +253,7 @@ def run_native(args, rank, world, dist):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     m.lib()
-    w = Work(args.workload, args.batch)
+    w = Work(args.workload, args.batch, args.records)
     r = GpuRunner(w, dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     for _ in range(args.warmup):
@@ -304,7 +309,8 @@ def run_native(args, rank, world, dist):
     value = world * w.step_bytes * K / (total_ms * 1e-3) / 1e9
     attn_avg = float(np.mean(attn_ms))
     achieved = w.attn_bytes / (attn_avg * 1e-3) / 1e9
-    prof = load_traffic(args.workload)
+    # the committed ncu traffic belongs to the full workload only
+    prof = load_traffic(args.workload) if args.batch == 0 and args.records == 0 else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
@@ -389,7 +395,7 @@ def cpu_baseline(w: Work, budget_s: float = 15.0):
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    w = Work(args.workload, args.batch)
+    w = Work(args.workload, args.batch, args.records)
     budget = max(1.0, args.cpu_seconds / max(1, args.steps))
     vals, rows, secs = [], 0, 0.0
     for _ in range(args.warmup if args.warmup < 1 else 1):
@@ -423,6 +429,8 @@ def main():
                     help="requests (query rows for sparse_prefill) instead of the workload's own; for small profiling captures")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--records", type=int, default=0,
+                    help="sparse_prefill only: size of the record pool (default 65536, L2-resident)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "native":
         args.warmup = 3

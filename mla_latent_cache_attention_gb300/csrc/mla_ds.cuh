@@ -283,7 +283,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
       mbar_wait(fin_pv, 0, &no_abort);
     }
     __syncwarp();
-  } else if (warp == 0) {
+  } else if (!kSparse && warp == 0) {
     // ------------------------------------------------------------------ scheduler / page producer
     uint32_t errbits = 0;
     int nitem = 0, stride_k = 0, gt_next = 0;
@@ -318,7 +318,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         }
         ++nitem;
       }
-      if (!kSparse) {
+      {
         for (int t = 0; t < cur.ntiles && ok; ++t) {
           const int gt = gt_next + t;
           int blk = p.num_blocks, y = 0;
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         }
       }
     }
-    if (!kSparse && lane == 0) {     // never leave copies in flight behind us
+    if (lane == 0) {     // never leave copies in flight behind us
       volatile int no_abort = 0;
       const int64_t first = pos > R ? pos - R : 0;
       for (int64_t q = first; q < pos; ++q) mbar_wait(&full[q % R], static_cast<uint32_t>(q / R) & 1u, &no_abort);
