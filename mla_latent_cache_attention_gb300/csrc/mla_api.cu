@@ -577,6 +577,9 @@ extern "C" int mla_paged_decode(const void* q, int64_t q_s0, int64_t q_s1, const
     const uint32_t qb[3] = {128, static_cast<uint32_t>(cp.box_h), static_cast<uint32_t>(cp.box_q)};
     if (int rc = tmap_3d(q, qd, qs, qb, &tq)) return rc;
     PagedParams p{};
+    p.kv = static_cast<const uint8_t*>(kv_cache);
+    p.kv_blk_stride = block_stride_bytes;
+    p.kv_ent_stride = entry_stride_bytes;
     p.H = H;
     p.q_len = q_len;
     p.B = B;

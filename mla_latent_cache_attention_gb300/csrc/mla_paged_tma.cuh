@@ -39,7 +39,8 @@
 // Pipeline choices (measured on GB300; the defaults are the fastest found):
 //   MLA_OVERLAP_FP8  fp8 issues QK(t+1) before PV(t)
 //   MLA_LOOKAHEAD    tiles between a page-table lookup and the tile's loads
-//   MLA_L2PF         also prefetch that tile into L2 when its pages are known
+//   MLA_L2PF         also prefetch that tile into L2 when its pages are known: 1 by tensor
+//                    boxes, 2 by one bulk prefetch per page (its rows are contiguous)
 //   MLA_SLOT_COMMITS release each ring slot by its own commit (else by PV of its tile)
 //   MLA_PV_WARP      PV issued by a warp of its own (else by the QK issuer)
 #ifndef MLA_OVERLAP_FP8
@@ -49,7 +50,7 @@
 #define MLA_LOOKAHEAD 1
 #endif
 #ifndef MLA_L2PF
-#define MLA_L2PF 1
+#define MLA_L2PF 2
 #endif
 #ifndef MLA_SLOT_COMMITS
 #define MLA_SLOT_COMMITS 1
@@ -61,6 +62,8 @@
 namespace mla {
 
 struct PagedParams {
+  const uint8_t* kv;            // the cache (for whole-page L2 prefetches)
+  int64_t kv_blk_stride, kv_ent_stride;
   int H, q_len, B, G;           // G column groups of NQ columns per request
   int cols;                     // H * q_len
   int qbox_h, qbox_q;           // query TMA box: heads x tokens (rows = qbox_h * qbox_q <= NQ)
@@ -141,6 +144,11 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, in
       "[%5];" ::"r"(smem_u32(dst)),
       "l"(tm), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Contiguous global bytes into L2 (address and size multiples of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* tm, int x, int y, int z) {
@@ -469,7 +477,13 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
           for (int q = 0; q < NPG && av && C::kL2Pf; ++q) {
             const int z = __shfl_sync(0xFFFFFFFFu, ba, q);
             const int yy = __shfl_sync(0xFFFFFFFFu, ya, q);
-            if (z < p.num_blocks && lane < C::kNBQ) tma_prefetch_3d(&tm_kv, (F == kFP8 && lane == 4) ? 448 : 128 * lane, yy, z);
+            if (MLA_L2PF == 2) {
+              if (z < p.num_blocks && lane == 0)
+                bulk_prefetch_l2(p.kv + static_cast<int64_t>(z) * p.kv_blk_stride + static_cast<int64_t>(yy) * p.kv_ent_stride,
+                                 static_cast<uint32_t>(p.BR * p.kv_ent_stride));
+            } else if (z < p.num_blocks && lane < C::kNBQ) {
+              tma_prefetch_3d(&tm_kv, (F == kFP8 && lane == 4) ? 448 : 128 * lane, yy, z);
+            }
           }
         }
       }
