@@ -246,6 +246,22 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
+def max_over_ranks(vals, dist, device):
+    """Each value's maximum over the ranks (the slowest rank's time); unchanged on one rank."""
+    if dist is None:
+        return list(vals)
+    import torch
+    t = torch.tensor(vals, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_rate(world: int, units_per_rank: float, steps: int, total_ms: float) -> float:
+    """Whole-job units per second: every rank processes units_per_rank per step, and the job
+    takes the slowest rank's time."""
+    return world * units_per_rank * steps / (total_ms * 1e-3)
+
+
 def run_native(args, rank, world, dist):
     import torch
     import mla_latent_cache_attention_gb300 as m
@@ -301,12 +317,9 @@ def run_native(args, rank, world, dist):
         torch.cuda.synchronize()
         e2e_ms += e0.elapsed_time(e1)
     assert m.read_device_errors() == 0, "device error word set during the timed steps"
-    if dist is not None:
-        t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, e2e_ms = float(t[0]), float(t[1])
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dist, dev)
     peak, peak_kind = peaks()
-    value = world * w.step_bytes * K / (total_ms * 1e-3) / 1e9
+    value = job_rate(world, w.step_bytes, K, total_ms) / 1e9
     attn_avg = float(np.mean(attn_ms))
     achieved = w.attn_bytes / (attn_avg * 1e-3) / 1e9
     # the committed ncu traffic belongs to the full workload only
@@ -317,14 +330,14 @@ def run_native(args, rank, world, dist):
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded numpy)",
         "config": dict(w.cfg, l2="flushed between steps (256 MiB write, outside the timed events)",
                        parallelism="replicas" if world > 1 else "single GPU"),
-        "query_rows_per_s": round(world * w.rows * K / (total_ms * 1e-3), 1),
-        "row_heads_per_s": round(world * w.rows * w.heads * K / (total_ms * 1e-3), 1),
+        "query_rows_per_s": round(job_rate(world, w.rows, K, total_ms), 1),
+        "row_heads_per_s": round(job_rate(world, w.rows * w.heads, K, total_ms), 1),
         "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": prof, "peak_source": f"{peak_kind} hbm_gbs",
                      "kernel": KERNELS[args.workload] + " (attention only; epilogue and merge outside)",
                      "kernel_ms": round(attn_avg, 5), "bytes_per_launch": w.attn_bytes},
-        "e2e": {"value": round(world * w.step_bytes * K / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(job_rate(world, w.step_bytes, K, e2e_ms) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(r.h2d), "d2h_bytes_per_step": int(r.d2h)},
         "gpu_launches": int(r.launches_per_step * K),
         "clocks": clocks,
