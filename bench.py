@@ -201,7 +201,8 @@ class GpuRunner:
 class ClockSampler:
     def __init__(self, index: int):
         self.index = index
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        import tempfile
+        self.path = os.path.join(tempfile.gettempdir(), f"mla_bench_clocks_{os.getpid()}.csv")
         self.proc = None
 
     def start(self):

@@ -156,7 +156,7 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* tm, int x, in
                : "memory");
 }
 
-// Bounded wait by lane 0 of the warp only (fewer shared-memory polls); the verdict and the
+// Bounded wait by lane 0 of the warp only (fewer shared-memory polls); its outcome and the
 // acquired view reach the other lanes through the warp barrier.
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   bool w = true;

@@ -118,7 +118,7 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
 }
 
 // Named barrier that also ANDs a predicate over the participating threads: every thread
-// leaves with the same verdict, so a failed wait in one thread stops all of them together.
+// leaves with the same answer, so a failed wait in one thread stops all of them together.
 __device__ __forceinline__ bool named_bar_and(uint32_t id, uint32_t nthreads, bool v) {
   uint32_t r;
   asm volatile(
