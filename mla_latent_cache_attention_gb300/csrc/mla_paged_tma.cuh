@@ -41,7 +41,7 @@
 //   MLA_LOOKAHEAD    tiles between a page-table lookup and the tile's loads
 //   MLA_L2PF         also prefetch that tile into L2 when its pages are known: 1 by tensor
 //                    boxes, 2 by one bulk prefetch per page (its rows are contiguous)
-//   MLA_SLOT_COMMITS release each ring slot by its own commit (else by PV of its tile)
+//   MLA_SLOT_COMMITS release each bf16 ring slot by its own commit (else by PV of its tile)
 //   MLA_PV_WARP      PV issued by a warp of its own (else by the QK issuer)
 #ifndef MLA_OVERLAP_FP8
 #define MLA_OVERLAP_FP8 1
@@ -110,7 +110,10 @@ struct PagedCfg {
   static constexpr bool kOverlap = (F == kFP8 || KM == 64) && MLA_OVERLAP_FP8;
   static constexpr int kPfDist = MLA_LOOKAHEAD;           // tiles between a page lookup and its use
   static constexpr bool kL2Pf = MLA_L2PF;
-  static constexpr bool kSlotCommits = MLA_SLOT_COMMITS;
+  // per-slot release commits pay for bf16 (a 147 KB tile fits 1.2 times: its slots refill as
+  // soon as each is done); fp8 (two tiles in the ring) is faster with one release per tile,
+  // since every commit drains the MMA pipe
+  static constexpr bool kSlotCommits = MLA_SLOT_COMMITS && F == kBF16;
   static constexpr int kQBytes = kNBQ * NQ * 128;
   static constexpr int kPBytes = F == kBF16 ? KM * NQ * 2 : 2 * KM * NQ;
   static constexpr int kRedBytes = 3 * NQ * 4 * 4 + 2 * NQ * 4;   // max / sum partials, reference max, rescale
