@@ -75,6 +75,13 @@ def lib():
                                                     i64, vp, vp, i64, i64, i64, i32, vp, flt, flt,
                                                     vp, vp, i64, i32, i32]
             L.orc_q_concat_cache_insert.restype = i32
+            L.orc_key_concat_cache_insert.argtypes = [i32, vp, i64, i64, vp, i64, i64, vp, i64, vp, i64, vp, vp,
+                                                      i64, i64, i64, i32, vp, vp, vp, i64, i32, i32, i32]
+            L.orc_key_concat_cache_insert.restype = i32
+            L.orc_qkv_quant_cache_fp8_insert.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, vp, i64, vp, i64,
+                                                         i64, vp, vp, vp, vp, i64, i64, i64, i32, vp, flt, flt,
+                                                         flt, flt, vp, vp, i64, i32, i32, i32, i32]
+            L.orc_qkv_quant_cache_fp8_insert.restype = i32
             L.orc_ds_tile_exponent.argtypes = [dbl]
             L.orc_ds_tile_exponent.restype = i32
             L.orc_rope_fp32.argtypes = [vp, vp, vp]
@@ -240,3 +247,74 @@ def q_concat_cache_insert(fmt, ql_nope, q_pe, kv_c, k_pe, cache, slot_mapping, *
     if rc != 0:
         raise ValueError("oracle q_concat_cache_insert: slot or position out of range")
     return mqa
+
+
+def _bits16(a, name):
+    a = np.asarray(a)
+    assert a.dtype == np.uint16 and a.strides[-1] == 2, f"{name}: uint16 bf16 bits with a unit last stride"
+    return a
+
+
+def _rope_args(positions, cos_sin):
+    if (positions is None) != (cos_sin is None):
+        raise ValueError("positions and cos_sin must be given together")
+    pos = None if positions is None else np.ascontiguousarray(positions, dtype=np.int64)
+    cs = None if cos_sin is None else np.ascontiguousarray(cos_sin, dtype=np.float32)
+    return pos, cs, (0 if cs is None else cs.shape[0])
+
+
+def key_concat_cache_insert(fmt, q, k_nope, k_pe, kv_c, cache, slot_mapping, *, positions=None, cos_sin=None):
+    """Prefill epilogue for the bf16 (fmt=BF16) or fp8_ds_mla (fmt=DS_MLA) cache.  All
+    activations are uint16 bf16 bits; ``q`` [Tp, H, dn+64] is rotated in place (when RoPE is
+    on) and ``cache`` (uint8 [nb, bs, stride]) is updated in place.  Returns k_out (uint16
+    [Tp, H, dn+64])."""
+    assert fmt in (BF16, DS_MLA)
+    q = _bits16(q, "q")
+    assert q.flags.writeable
+    k_nope = _bits16(k_nope, "k_nope")
+    k_pe = _bits16(np.asarray(k_pe).reshape(np.asarray(k_pe).shape[0], -1), "k_pe")
+    kv_c = _bits16(kv_c, "kv_c")
+    Tp, H, dn = k_nope.shape
+    assert q.shape == (Tp, H, dn + 64)
+    assert cache.dtype == np.uint8 and cache.ndim == 3 and cache.flags.writeable
+    nb, bs, _ = cache.shape
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    pos, cs, maxp = _rope_args(positions, cos_sin)
+    k_out = np.zeros((Tp, H, dn + 64), dtype=np.uint16)
+    rc = lib().orc_key_concat_cache_insert(
+        int(fmt), _P(q), q.strides[0] // 2, q.strides[1] // 2, _P(k_nope), k_nope.strides[0] // 2,
+        k_nope.strides[1] // 2, _P(k_pe), k_pe.strides[0] // 2, _P(kv_c), kv_c.strides[0] // 2, _P(k_out),
+        _P(cache), nb, cache.strides[0], cache.strides[1], bs, _P(sm), _P(pos), _P(cs), maxp, Tp, H, dn)
+    if rc != 0:
+        raise ValueError("oracle key_concat_cache_insert: slot or position out of range")
+    return k_out
+
+
+def qkv_quant_cache_fp8_insert(q, k_nope, k_pe, kv_c, v, cache, slot_mapping, *, q_scale_inv, k_scale_inv,
+                               v_scale_inv, cache_scale_inv, positions=None, cos_sin=None):
+    """Prefill epilogue for the plain fp8 cache.  Returns (q_fp8, k_fp8, v_fp8) as uint8 E4M3
+    codes; ``cache`` (uint8 [nb, bs, stride]) is updated in place; q is not modified."""
+    q = _bits16(q, "q")
+    k_nope = _bits16(k_nope, "k_nope")
+    k_pe = _bits16(np.asarray(k_pe).reshape(np.asarray(k_pe).shape[0], -1), "k_pe")
+    kv_c = _bits16(kv_c, "kv_c")
+    v = _bits16(v, "v")
+    Tp, H, dn = k_nope.shape
+    dv = v.shape[2]
+    assert q.shape == (Tp, H, dn + 64) and v.shape[:2] == (Tp, H)
+    assert cache.dtype == np.uint8 and cache.ndim == 3 and cache.flags.writeable
+    nb, bs, _ = cache.shape
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    pos, cs, maxp = _rope_args(positions, cos_sin)
+    q8 = np.zeros((Tp, H, dn + 64), dtype=np.uint8)
+    k8 = np.zeros((Tp, H, dn + 64), dtype=np.uint8)
+    v8 = np.zeros((Tp, H, dv), dtype=np.uint8)
+    rc = lib().orc_qkv_quant_cache_fp8_insert(
+        _P(q), q.strides[0] // 2, q.strides[1] // 2, _P(k_nope), k_nope.strides[0] // 2, k_nope.strides[1] // 2,
+        _P(k_pe), k_pe.strides[0] // 2, _P(kv_c), kv_c.strides[0] // 2, _P(v), v.strides[0] // 2,
+        v.strides[1] // 2, _P(q8), _P(k8), _P(v8), _P(cache), nb, cache.strides[0], cache.strides[1], bs, _P(sm),
+        float(q_scale_inv), float(k_scale_inv), float(v_scale_inv), float(cache_scale_inv), _P(pos), _P(cs), maxp,
+        Tp, H, dn, dv)
+    if rc != 0:
+        raise ValueError("oracle qkv_quant_cache_fp8_insert: slot or position out of range")
+    return q8, k8, v8

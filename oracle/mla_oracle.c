@@ -23,6 +23,11 @@
  *    from an fp32 cos/sin table.
  *  - "vllm.models.kimi_k3.amd.specialized_decode.mono.attention.mla", fp8_word: the fp8
  *    write is vLLM's saturating E4M3 quant.
+ *  - "vllm.models.kimi_k3.nvidia.ops.fused_mla_key_concat_kv_cache",
+ *    fused_mla_key_concat_kv_cache_insert / fused_mla_key_concat_ds_mla_insert (prefill: full
+ *    key [k_nope | k_pe] per head, q RoPE in place, latent insert) and
+ *    fused_mla_qkv_quant_kv_cache_fp8_insert (fp8 q / k / v with separate scales, cache with
+ *    its own scale).
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *  - fp8_ds_mla tile scale on insert: s = 2^k with k the smallest integer such that
@@ -338,6 +343,41 @@ static int ds_tile_exponent(double amax) {
   return k;
 }
 
+/* Write one cache entry from the latent kc (512 bf16 values) and the rotated rope kpr (64
+ * fp32 values): bf16 [kc | bf16(kpr)]; plain fp8 e4m3_sat(x * cache_scale_inv) for all 576;
+ * fp8_ds_mla per-128-tile power-of-two scale s_j (ds_tile_exponent of the tile's amax),
+ * codes e4m3_sat(x / s_j), the four scales as fp32 at byte 512, bf16(kpr) at byte 528. */
+static void write_latent(int fmt, uint8_t* ent, const uint16_t* kc, const float* kpr, float cache_scale_inv) {
+  float x[KV_LORA];
+  int d;
+  for (d = 0; d < KV_LORA; ++d) x[d] = bf16_to_float(kc[d]);
+  if (fmt == ORC_BF16) {
+    for (d = 0; d < KV_LORA; ++d) wr16(ent + 2 * d, kc[d]);
+    for (d = 0; d < ROPE; ++d) wr16(ent + 2 * (KV_LORA + d), orc_bf16_from_float(kpr[d]));
+  } else if (fmt == ORC_FP8) {
+    for (d = 0; d < KV_LORA; ++d) ent[d] = orc_e4m3_from_float_sat(x[d] * cache_scale_inv);
+    for (d = 0; d < ROPE; ++d) ent[KV_LORA + d] = orc_e4m3_from_float_sat(kpr[d] * cache_scale_inv);
+  } else {
+    int j;
+    for (j = 0; j < 4; ++j) {
+      double amax = 0.0, s;
+      float sf;
+      int k;
+      for (d = 0; d < 128; ++d) {
+        double a = fabs((double)x[128 * j + d]);
+        if (a > amax) amax = a;
+      }
+      k = ds_tile_exponent(amax);
+      s = ldexp(1.0, k);
+      sf = (float)s;
+      memcpy(ent + KV_LORA + 4 * j, &sf, 4);
+      for (d = 0; d < 128; ++d)
+        ent[128 * j + d] = orc_e4m3_from_float_sat((float)((double)x[128 * j + d] / s));
+    }
+    for (d = 0; d < ROPE; ++d) wr16(ent + KV_LORA + 16 + 2 * d, orc_bf16_from_float(kpr[d]));
+  }
+}
+
 /* Inputs are bf16 tensors given by element strides (unit last stride):
  *   ql_nope [B, H, 512], q_pe [B, H, 64], kv_c [B, 512], k_pe [B, 64].
  * mqa_q out: [B, H, 576] contiguous, bf16 (bf16 / ds_mla formats) or e4m3 bytes (plain fp8).
@@ -357,7 +397,7 @@ int orc_q_concat_cache_insert(int fmt, const uint16_t* ql_nope, int64_t ql_s0, i
   int bad = 0, b;
   for (b = 0; b < B; ++b) {
     const float* cs = NULL;
-    float kp[ROPE], kpr[ROPE], x[KV_LORA];
+    float kp[ROPE], kpr[ROPE];
     int h, d;
     int64_t slot;
     if (positions) {
@@ -396,40 +436,138 @@ int orc_q_concat_cache_insert(int fmt, const uint16_t* ql_nope, int64_t ql_s0, i
     }
     {
       uint8_t* ent = cache + (slot / block_size) * block_stride + (slot % block_size) * entry_stride;
-      const uint16_t* kc = kv_c + (int64_t)b * kv_s0;
       const uint16_t* kr = k_pe + (int64_t)b * kp_s0;
       for (d = 0; d < ROPE; ++d) kp[d] = bf16_to_float(kr[d]);
       if (cs)
         rope_fp32(kp, cs, kpr);
       else
         memcpy(kpr, kp, sizeof kpr);
-      for (d = 0; d < KV_LORA; ++d) x[d] = bf16_to_float(kc[d]);
-      if (fmt == ORC_BF16) {
-        for (d = 0; d < KV_LORA; ++d) wr16(ent + 2 * d, kc[d]);
-        for (d = 0; d < ROPE; ++d) wr16(ent + 2 * (KV_LORA + d), orc_bf16_from_float(kpr[d]));
-      } else if (fmt == ORC_FP8) {
-        for (d = 0; d < KV_LORA; ++d) ent[d] = orc_e4m3_from_float_sat(x[d] * cache_scale_inv);
-        for (d = 0; d < ROPE; ++d) ent[KV_LORA + d] = orc_e4m3_from_float_sat(kpr[d] * cache_scale_inv);
-      } else {
-        int j;
-        for (j = 0; j < 4; ++j) {
-          double amax = 0.0, s;
-          float sf;
-          int k;
-          for (d = 0; d < 128; ++d) {
-            double a = fabs((double)x[128 * j + d]);
-            if (a > amax) amax = a;
-          }
-          k = ds_tile_exponent(amax);
-          s = ldexp(1.0, k);
-          sf = (float)s;
-          memcpy(ent + KV_LORA + 4 * j, &sf, 4);
-          for (d = 0; d < 128; ++d)
-            ent[128 * j + d] = orc_e4m3_from_float_sat((float)((double)x[128 * j + d] / s));
-        }
-        for (d = 0; d < ROPE; ++d) wr16(ent + KV_LORA + 16 + 2 * d, orc_bf16_from_float(kpr[d]));
-      }
+      write_latent(fmt, ent, kv_c + (int64_t)b * kv_s0, kpr, cache_scale_inv);
     }
+  }
+  return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Prefill epilogues: full-key concat, in-place query RoPE, latent insert, fp8 q/k/v quant. */
+/* ------------------------------------------------------------------------------------ */
+
+/* The RoPE row of token t (NULL without RoPE); an out-of-range position is clamped and
+ * reported through *bad. */
+static const float* rope_row(const int64_t* positions, const float* cos_sin, int64_t max_position, int t,
+                             int* bad) {
+  int64_t pos;
+  if (!positions) return NULL;
+  pos = positions[t];
+  if (pos < 0 || pos >= max_position) {
+    *bad = 1;
+    pos = pos < 0 ? 0 : max_position - 1;
+  }
+  return cos_sin + pos * ROPE;
+}
+
+/* bf16 vector of 64 -> rotated fp32 (or the plain values without RoPE). */
+static void rope_bf16_vec(const uint16_t* x, const float* cs, float* y) {
+  float xf[ROPE];
+  int d;
+  for (d = 0; d < ROPE; ++d) xf[d] = bf16_to_float(x[d]);
+  if (cs)
+    rope_fp32(xf, cs, y);
+  else
+    memcpy(y, xf, sizeof xf);
+}
+
+/* "vllm.models.kimi_k3.nvidia.ops.fused_mla_key_concat_kv_cache",
+ * fused_mla_key_concat_kv_cache_insert (fmt = bf16) and fused_mla_key_concat_ds_mla_insert
+ * (fmt = fp8_ds_mla).  Per prefill token t (Tp tokens), H heads, dn NoPE dims per head:
+ *   q      bf16 [Tp, H, dn + 64] (element strides q_s0, q_s1): its last 64 values are
+ *          rotated in place when positions are given (bf16 of the fp32 rotation);
+ *   k_nope bf16 [Tp, H, dn]; k_pe bf16 [Tp, 64]; kv_c bf16 [Tp, 512];
+ *   k_out  bf16 [Tp, H, dn + 64] contiguous: [k_nope[t, h] | bf16(rope(k_pe[t]))];
+ *   the latent [kv_c | rope(k_pe)] is written at slot_mapping[t] as in the decode epilogue
+ *   (a negative slot skips it).
+ * Returns -1 if a slot's block or a position is out of range (skipped / clamped). */
+int orc_key_concat_cache_insert(int fmt, uint16_t* q, int64_t q_s0, int64_t q_s1, const uint16_t* k_nope,
+                                int64_t kn_s0, int64_t kn_s1, const uint16_t* k_pe, int64_t kp_s0,
+                                const uint16_t* kv_c, int64_t kv_s0, uint16_t* k_out, uint8_t* cache,
+                                int64_t num_blocks, int64_t block_stride, int64_t entry_stride, int block_size,
+                                const int64_t* slot_mapping, const int64_t* positions, const float* cos_sin,
+                                int64_t max_position, int Tp, int H, int dn) {
+  int bad = 0, t, h, d;
+  for (t = 0; t < Tp; ++t) {
+    const float* cs = rope_row(positions, cos_sin, max_position, t, &bad);
+    float kpr[ROPE];
+    int64_t slot;
+    rope_bf16_vec(k_pe + (int64_t)t * kp_s0, cs, kpr);
+    for (h = 0; h < H; ++h) {
+      uint16_t* qh = q + (int64_t)t * q_s0 + (int64_t)h * q_s1;
+      const uint16_t* kn = k_nope + (int64_t)t * kn_s0 + (int64_t)h * kn_s1;
+      uint16_t* ko = k_out + ((int64_t)t * H + h) * (dn + ROPE);
+      if (cs) {
+        float qr[ROPE];
+        rope_bf16_vec(qh + dn, cs, qr);
+        for (d = 0; d < ROPE; ++d) qh[dn + d] = orc_bf16_from_float(qr[d]);
+      }
+      for (d = 0; d < dn; ++d) ko[d] = kn[d];
+      for (d = 0; d < ROPE; ++d) ko[dn + d] = orc_bf16_from_float(kpr[d]);
+    }
+    slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot / block_size >= num_blocks) {
+      bad = 1;
+      continue;
+    }
+    write_latent(fmt, cache + (slot / block_size) * block_stride + (slot % block_size) * entry_stride,
+                 kv_c + (int64_t)t * kv_s0, kpr, 1.0f);
+  }
+  return bad ? -1 : 0;
+}
+
+/* "vllm.models.kimi_k3.nvidia.ops.fused_mla_key_concat_kv_cache",
+ * fused_mla_qkv_quant_kv_cache_fp8_insert.  Per token t and head h (dn NoPE dims, dv value
+ * dims), with x -> e4m3_sat(x * inv) the saturating quant of the fp32 product:
+ *   q_fp8 [Tp, H, dn + 64] = quant([q_nope | rope(q_pe)], q_scale_inv)   (q is not modified);
+ *   k_fp8 [Tp, H, dn + 64] = quant([k_nope | rope(k_pe)], k_scale_inv);
+ *   v_fp8 [Tp, H, dv]      = quant(v, v_scale_inv);
+ *   cache entry at slot    = quant([kv_c | rope(k_pe)], cache_scale_inv) (plain fp8 cache).
+ * Outputs are contiguous; inputs use element strides.  Returns -1 as above. */
+int orc_qkv_quant_cache_fp8_insert(const uint16_t* q, int64_t q_s0, int64_t q_s1, const uint16_t* k_nope,
+                                   int64_t kn_s0, int64_t kn_s1, const uint16_t* k_pe, int64_t kp_s0,
+                                   const uint16_t* kv_c, int64_t kv_s0, const uint16_t* v, int64_t v_s0,
+                                   int64_t v_s1, uint8_t* q_fp8, uint8_t* k_fp8, uint8_t* v_fp8, uint8_t* cache,
+                                   int64_t num_blocks, int64_t block_stride, int64_t entry_stride, int block_size,
+                                   const int64_t* slot_mapping, float q_scale_inv, float k_scale_inv,
+                                   float v_scale_inv, float cache_scale_inv, const int64_t* positions,
+                                   const float* cos_sin, int64_t max_position, int Tp, int H, int dn, int dv) {
+  int bad = 0, t, h, d;
+  for (t = 0; t < Tp; ++t) {
+    const float* cs = rope_row(positions, cos_sin, max_position, t, &bad);
+    float kpr[ROPE];
+    int64_t slot;
+    rope_bf16_vec(k_pe + (int64_t)t * kp_s0, cs, kpr);
+    for (h = 0; h < H; ++h) {
+      const uint16_t* qh = q + (int64_t)t * q_s0 + (int64_t)h * q_s1;
+      const uint16_t* kn = k_nope + (int64_t)t * kn_s0 + (int64_t)h * kn_s1;
+      const uint16_t* vh = v + (int64_t)t * v_s0 + (int64_t)h * v_s1;
+      uint8_t* qo = q_fp8 + ((int64_t)t * H + h) * (dn + ROPE);
+      uint8_t* ko = k_fp8 + ((int64_t)t * H + h) * (dn + ROPE);
+      uint8_t* vo = v_fp8 + ((int64_t)t * H + h) * dv;
+      float qr[ROPE];
+      rope_bf16_vec(qh + dn, cs, qr);
+      for (d = 0; d < dn; ++d) qo[d] = orc_e4m3_from_float_sat(bf16_to_float(qh[d]) * q_scale_inv);
+      for (d = 0; d < ROPE; ++d) qo[dn + d] = orc_e4m3_from_float_sat(qr[d] * q_scale_inv);
+      for (d = 0; d < dn; ++d) ko[d] = orc_e4m3_from_float_sat(bf16_to_float(kn[d]) * k_scale_inv);
+      for (d = 0; d < ROPE; ++d) ko[dn + d] = orc_e4m3_from_float_sat(kpr[d] * k_scale_inv);
+      for (d = 0; d < dv; ++d) vo[d] = orc_e4m3_from_float_sat(bf16_to_float(vh[d]) * v_scale_inv);
+    }
+    slot = slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot / block_size >= num_blocks) {
+      bad = 1;
+      continue;
+    }
+    write_latent(ORC_FP8, cache + (slot / block_size) * block_stride + (slot % block_size) * entry_stride,
+                 kv_c + (int64_t)t * kv_s0, kpr, cache_scale_inv);
   }
   return bad ? -1 : 0;
 }
