@@ -1,16 +1,23 @@
 #!/usr/bin/env python
 """Benchmark of the MLA latent-cache hot path on GB300.
 
-Default workload: paged bf16 decode with the fused epilogue in front (B=32, q=1, H=16,
-seq_lens ~ U[1024, 8192], block_size 64).  One step = mla_q_concat_cache_insert followed by
-mla_paged_decode (attention + split-K merge) over the whole batch.  Other workloads
-(--workload): sparse_prefill (T=4096, H=16, top-2048 over 65536 fp8_ds_mla records),
-fp8_spec_verify (B=64, q=4, H=16, plain fp8, L ~ U[16k, 128k]) and ds_mla_h96_decode
-(B=128, H=96, fp8_ds_mla, L ~ U[8k, 32k]).
+Headline workload (default --workload): sparse prefill over fp8_ds_mla records (T=4096 query
+rows, H=16, top-2048 of 65536 records, ~5 % masked), the largest configuration that fits one
+GPU.  One step = one mla_sparse_fwd over the whole batch.  The same JSON line carries, under
+"per_config", the other workloads of the path, each timed the same way with its own roofline,
+end-to-end figure and CPU-oracle baseline:
+  decode_bf16_epilogue  mla_q_concat_cache_insert + mla_paged_decode (B=32, q=1, H=16, bf16,
+                        seq_lens ~ U[1024, 8192])
+  fp8_spec_verify       mla_paged_decode (B=64, q=4 causal, H=16, plain fp8, L ~ U[16k, 128k],
+                        split-K + merge)
+  ds_mla_h96_decode     mla_paged_decode (B=128, H=96, fp8_ds_mla, L ~ U[8k, 32k])
+  sparse_prefill_4M_records  the headline over a 2^22-record pool (2.75 GB, past L2)
 
 Metric: achieved GB/s of algorithmic bytes (entries gathered + query read + output written
 (+ lse)), with query-rows/s beside it.  Timing: CUDA events per step after warm-up, L2
-flushed (256 MiB write) between steps outside the timed events; max over ranks.
+flushed (256 MiB write) between steps outside the timed events; max over ranks.  The
+headline times exactly --steps steps; each per-config entry times at least --steps steps and
+at least --min-ms of GPU time (so that clock samples land under load).
 `--impl reference` times the fp64 CPU oracle on a bounded sample of the same workload.
 Multi-GPU (torchrun): every rank runs an independent replica ("replicas only").
 """
@@ -29,7 +36,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MLA attention achieved HBM GB/s (% of GB300 peak); query-rows/s at 1 GPU"
-WORKLOADS = ("decode_bf16_epilogue", "sparse_prefill", "fp8_spec_verify", "ds_mla_h96_decode")
+WORKLOADS = ("sparse_prefill", "decode_bf16_epilogue", "fp8_spec_verify", "ds_mla_h96_decode")
 # the attention kernel each workload times (the profiling hook brackets exactly its launch)
 KERNELS = {
     "decode_bf16_epilogue": "mla_paged_tma_kernel<bf16, 16 columns>",
@@ -37,6 +44,7 @@ KERNELS = {
     "fp8_spec_verify": "mla_paged_tma_kernel<fp8, 64 columns>",
     "ds_mla_h96_decode": "mla_ds_kernel<paged>",
 }
+PAST_L2_RECORDS = 1 << 22
 
 
 def peaks():
@@ -86,7 +94,7 @@ class Work:
             self.heads = c.q.shape[1]
             self.cfg = dict(workload=name, T=int(c.q.shape[0]), H=int(c.q.shape[1]), records=int(c.records.shape[0]),
                             indices_per_row=2048, masked_frac=0.05, cache="fp8_ds_mla", return_lse=True)
-            self.dtype = "bf16"
+            self.dtype = "fp8_ds_mla: e4m3 codes (kind::f8f6f4) + bf16 rope (kind::f16), fp32 accumulate"
         else:
             self.attn_bytes = synth.algorithmic_bytes_paged(c)
             self.rows = c.seq_lens.size * c.q_len
@@ -95,7 +103,9 @@ class Work:
             self.cfg = dict(workload=name, B=int(c.seq_lens.size), q_len=c.q_len, H=c.H, cache=fmtname,
                             block_size=int(c.cache.shape[1]), seq_len_lo=int(c.meta["L_lo"]),
                             seq_len_hi=int(c.meta["L_hi"]), max_context=c.max_context, return_lse=c.return_lse)
-            self.dtype = {0: "bf16", 1: "fp8 e4m3 operands (f16 MMA)", 2: "bf16/f16 (fp8_ds_mla)"}[c.fmt]
+            self.dtype = {0: "bf16 (kind::f16 MMA, fp32 accumulate)",
+                          1: "fp8 e4m3 operands (kind::f8f6f4 MMA, fp32 accumulate)",
+                          2: "fp8_ds_mla: e4m3 codes (kind::f8f6f4) + bf16 rope (kind::f16), fp32 accumulate"}[c.fmt]
         self.epi_bytes = 0
         if name == "decode_bf16_epilogue":
             B, H = self.epi.ql_nope.shape[:2]
@@ -263,6 +273,98 @@ def job_rate(world: int, units_per_rank: float, steps: int, total_ms: float) -> 
     return world * units_per_rank * steps / (total_ms * 1e-3)
 
 
+def timed_steps(r, flush, steps, torch, prof=True):
+    """`steps` steps, each bracketed by CUDA events on the current stream (the attention launch
+    by the library's profiling hook), L2 flushed before each step outside the events.
+    Returns (step times, attention-kernel times) in ms."""
+    m = r.m
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    ea = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ea:      # materialise the handles
+        a.record()
+        b.record()
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.fill_(i & 255)
+        if prof:
+            m.profile_attention_events(*ea[i])
+        ev[i][0].record()
+        r.step()
+        ev[i][1].record()
+    m.profile_attention_events(None, None)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev], [a.elapsed_time(b) for a, b in ea]
+
+
+def e2e_steps(r, flush, steps, torch):
+    """Same steps through the public API with the per-step inputs copied from pinned host
+    memory and the results copied back, inside the timed region.  Returns total ms."""
+    r.e2e_setup()
+    for _ in range(2):
+        r.e2e_step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    total = 0.0
+    for i in range(steps):
+        flush.fill_(i & 255)
+        e0.record()
+        r.e2e_step()
+        e1.record()
+        torch.cuda.synchronize()
+        total += e0.elapsed_time(e1)
+    return total
+
+
+def measure(w: Work, dev, flush, steps: int, warmup: int, min_ms: float, dist, world: int, peak: float,
+            peak_kind: str, traffic, cpu_seconds: float):
+    """Time one workload: warm-up, then at least `steps` steps and (when min_ms > 0) at least
+    min_ms of step time; roofline of its attention kernel, e2e and the oracle baseline."""
+    import torch
+    r = GpuRunner(w, dev)
+    m = r.m
+    for _ in range(warmup):
+        flush.fill_(1)
+        r.step()
+    torch.cuda.synchronize()
+    assert m.read_device_errors() == 0, f"device error word set during the warm-up of {w.name}"
+    K = steps
+    if min_ms > 0:
+        probe, _ = timed_steps(r, flush, 2, torch, prof=False)
+        K = max(steps, int(np.ceil(min_ms / max(min(probe), 1e-3))))
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_ms, attn_ms = timed_steps(r, flush, K, torch)
+    total_ms = float(sum(step_ms))
+    e2e_ms = e2e_steps(r, flush, K, torch)
+    assert m.read_device_errors() == 0, f"device error word set during the timed steps of {w.name}"
+    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dist, dev)
+    attn_avg = float(np.mean(attn_ms))
+    achieved = w.attn_bytes / (attn_avg * 1e-3) / 1e9
+    value = job_rate(world, w.step_bytes, K, total_ms) / 1e9
+    res = {
+        "steps": K, "value": round(value, 2), "unit": "GB/s", "ms_per_step": round(total_ms / K, 5),
+        "query_rows_per_s": round(job_rate(world, w.rows, K, total_ms), 1),
+        "row_heads_per_s": round(job_rate(world, w.rows * w.heads, K, total_ms), 1),
+        "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic, "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel": KERNELS[w.name] + " (attention only; epilogue and merge outside)",
+                     "kernel_ms": round(attn_avg, 5), "kernel_ms_min": round(float(np.min(attn_ms)), 5),
+                     "bytes_per_launch": w.attn_bytes},
+        "e2e": {"value": round(job_rate(world, w.step_bytes, K, e2e_ms) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": int(r.h2d), "d2h_bytes_per_step": int(r.d2h)},
+        "gpu_launches": int(r.launches_per_step * K),
+        "dtype": w.dtype,
+        "config": dict(w.cfg),
+    }
+    del r
+    torch.cuda.empty_cache()
+    if cpu_seconds > 0:
+        res["cpu_baseline"] = cpu_baseline(w, budget_s=cpu_seconds)
+    return res
+
+
 def run_native(args, rank, world, dist):
     import torch
     import mla_latent_cache_attention_gb300 as m
@@ -270,81 +372,55 @@ def run_native(args, rank, world, dist):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     m.lib()
-    w = Work(args.workload, args.batch, args.records)
-    r = GpuRunner(w, dev)
+    peak, peak_kind = peaks()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-    for _ in range(args.warmup):
-        flush.fill_(1)
-        r.step()
-    torch.cuda.synchronize()
-    assert m.read_device_errors() == 0, "device error word set during warm-up"
-    K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    ea = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    for a, b in ea:      # materialise the handles
-        a.record()
-        b.record()
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
+    full = args.batch == 0 and args.records == 0
+    cpu_s = args.cpu_seconds if (rank == 0 and world == 1 and not args.no_cpu_baseline) else 0.0
+    w = Work(args.workload, args.batch, args.records)
     clk = ClockSampler(local)
     clk.start()
     time.sleep(0.3)
-    torch.cuda.synchronize()
-    for i in range(K):
-        flush.fill_(i & 255)
-        m.profile_attention_events(*ea[i])
-        ev[i][0].record()
-        r.step()
-        ev[i][1].record()
-    m.profile_attention_events(None, None)
-    torch.cuda.synchronize()
+    head = measure(w, dev, flush, args.steps, args.warmup, 0.0, dist, world, peak, peak_kind,
+                   load_traffic(args.workload) if full else None, 0.0)
+    per, works = {}, {}
+    if full and not args.headline_only:
+        # the other configurations of the path (and the headline past L2), each timed for at
+        # least --min-ms so that the clock samples land under load
+        for name in [n for n in WORKLOADS if n != args.workload]:
+            works[name] = Work(name)
+            per[name] = measure(works[name], dev, flush, args.steps, args.warmup, args.min_ms, dist, world, peak,
+                                peak_kind, load_traffic(name), 0.0)
+        if args.workload == "sparse_prefill":
+            name = "sparse_prefill_4M_records"
+            works[name] = Work("sparse_prefill", 0, PAST_L2_RECORDS)
+            res = measure(works[name], dev, flush, args.steps, args.warmup, args.min_ms, dist, world, peak,
+                          peak_kind, load_traffic(name), 0.0)
+            res["note"] = ("the headline workload over a 2^22-record pool (2.75 GB, past the 129 MB L2): the "
+                           "gathered records come from DRAM")
+            per[name] = res
     clocks = clk.stop()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
-    attn_ms = [a.elapsed_time(b) for a, b in ea]
-    total_ms = float(sum(step_ms))
-    # e2e through the public API with host buffers
-    r.e2e_setup()
-    for _ in range(2):
-        r.e2e_step()
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_ms = 0.0
-    for i in range(K):
-        flush.fill_(i & 255)
-        e0.record()
-        r.e2e_step()
-        e1.record()
-        torch.cuda.synchronize()
-        e2e_ms += e0.elapsed_time(e1)
-    assert m.read_device_errors() == 0, "device error word set during the timed steps"
-    total_ms, e2e_ms = max_over_ranks([total_ms, e2e_ms], dist, dev)
-    peak, peak_kind = peaks()
-    value = job_rate(world, w.step_bytes, K, total_ms) / 1e9
-    attn_avg = float(np.mean(attn_ms))
-    achieved = w.attn_bytes / (attn_avg * 1e-3) / 1e9
-    # the committed ncu traffic belongs to the full workload only
-    prof = load_traffic(args.workload) if args.batch == 0 and args.records == 0 else None
+    # the CPU-oracle baselines run after the GPU timing (host work outside every timed region)
+    if cpu_s > 0:
+        head["cpu_baseline"] = cpu_baseline(w, budget_s=cpu_s)
+        for name in per:
+            per[name]["cpu_baseline"] = cpu_baseline(works[name], budget_s=max(2.0, cpu_s / 2))
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": round(total_ms / K, 5), "higher_is_better": True,
+        "metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded numpy)",
         "config": dict(w.cfg, l2="flushed between steps (256 MiB write, outside the timed events)",
-                       parallelism="replicas" if world > 1 else "single GPU"),
-        "query_rows_per_s": round(job_rate(world, w.rows, K, total_ms), 1),
-        "row_heads_per_s": round(job_rate(world, w.rows * w.heads, K, total_ms), 1),
-        "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": prof, "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": KERNELS[args.workload] + " (attention only; epilogue and merge outside)",
-                     "kernel_ms": round(attn_avg, 5), "bytes_per_launch": w.attn_bytes},
-        "e2e": {"value": round(job_rate(world, w.step_bytes, K, e2e_ms) / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": int(r.h2d), "d2h_bytes_per_step": int(r.d2h)},
-        "gpu_launches": int(r.launches_per_step * K),
+                       parallelism="replicas" if world > 1 else "single GPU",
+                       config_index_reading="BASELINE configs 2-4 read 0-based: sparse prefill, fp8 spec-verify, "
+                                            "ds_mla H=96 decode"),
+        "query_rows_per_s": head["query_rows_per_s"], "row_heads_per_s": head["row_heads_per_s"],
+        "pct_of_hbm_peak": head["pct_of_hbm_peak"],
+        "roofline": head["roofline"], "e2e": head["e2e"], "gpu_launches": head["gpu_launches"],
         "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    if "cpu_baseline" in head:
+        line["cpu_baseline"] = head["cpu_baseline"]
+    if per:
+        line["per_config"] = per
     return line
 
 
@@ -438,10 +514,14 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--workload", default="decode_bf16_epilogue", choices=WORKLOADS)
+    ap.add_argument("--workload", default="sparse_prefill", choices=WORKLOADS)
+    ap.add_argument("--headline-only", action="store_true",
+                    help="time only --workload (no per_config entries); for profiling captures")
+    ap.add_argument("--min-ms", type=float, default=250.0,
+                    help="GPU time each per_config entry is timed for at least")
     ap.add_argument("--batch", type=int, default=0,
                     help="requests (query rows for sparse_prefill) instead of the workload's own; for small profiling captures")
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--records", type=int, default=0,
                     help="sparse_prefill only: size of the record pool (default 65536, L2-resident)")

@@ -127,6 +127,69 @@ MLA_API int mla_q_concat_cache_insert(const void* ql_nope, int64_t ql_s0, int64_
                               int32_t H, cudaStream_t stream);
 
 /*
+ * Prefill epilogue for the bf16 and fp8_ds_mla caches: full per-head key, query RoPE in place
+ * and latent insert, in one launch.
+ * Follows: "vllm.models.kimi_k3.nvidia.ops.fused_mla_key_concat_kv_cache",
+ * fused_mla_key_concat_kv_cache_insert (bf16 cache) and fused_mla_key_concat_ds_mla_insert
+ * (fp8_ds_mla cache).
+ *
+ *   q            device bf16 [Tp, H, dn + 64], strides (q_s0, q_s1); when RoPE is on its last
+ *                64 values are rotated in place (bf16 of the fp32 rotation), else untouched.
+ *   k_nope       device bf16 [Tp, H, dn], strides (kn_s0, kn_s1); dn a multiple of 8.
+ *   k_pe         device bf16 [Tp, 64] (or [Tp, 1, 64]), row stride kp_s0.
+ *   kv_c_normed  device bf16 [Tp, 512], row stride kv_s0.
+ *   k_out        device out bf16 [Tp, H, dn + 64] contiguous: [k_nope[t, h] | rope(k_pe[t])]
+ *                (the rotated k_pe of a token is shared by all its heads).
+ *   kv_cache, fmt  MLA_CACHE_BF16 or MLA_CACHE_FP8_DS_MLA cache, geometry as in
+ *                mla_q_concat_cache_insert; token t's latent [kv_c_normed | rope(k_pe)] is
+ *                written at slot_mapping[t] in the same format and rounding as there (a
+ *                negative slot skips it; a slot whose block is out of range is skipped and
+ *                reported as MLA_DEVERR_SLOT).
+ *   positions / cos_sin_cache / max_position  as in mla_q_concat_cache_insert (both NULL: no
+ *                RoPE).  RoPE pairs are (2i, 2i+1) of the 64 rope values.
+ * Errors: MLA_ERR_INVALID for NULL tensors, overlapping strides, misaligned (odd) bf16
+ * pointers, a cache format other than the two above; MLA_ERR_UNSUPPORTED for dn not a positive
+ * multiple of 8.
+ */
+MLA_API int mla_key_concat_cache_insert(void* q, int64_t q_s0, int64_t q_s1, const void* k_nope, int64_t kn_s0,
+                                        int64_t kn_s1, const void* k_pe, int64_t kp_s0, const void* kv_c_normed,
+                                        int64_t kv_s0, void* k_out, void* kv_cache, mla_cache_format fmt,
+                                        int64_t num_blocks, int64_t block_stride_bytes, int64_t entry_stride_bytes,
+                                        int32_t block_size, const int64_t* slot_mapping, const int64_t* positions,
+                                        const float* cos_sin_cache, int64_t max_position, int32_t Tp, int32_t H,
+                                        int32_t dn, cudaStream_t stream);
+
+/*
+ * Prefill epilogue for the plain fp8 cache: query, key and value quantised to E4M3, each with
+ * its own scale, and the latent inserted with the cache's scale, in one launch.
+ * Follows: "vllm.models.kimi_k3.nvidia.ops.fused_mla_key_concat_kv_cache",
+ * fused_mla_qkv_quant_kv_cache_fp8_insert (the attention key and the cache latent use separate
+ * scales).  x -> e4m3_sat(x * inv) is the fp32 product rounded to nearest even on the E4M3
+ * grid with saturation at +-448.
+ *
+ *   q, k_nope, k_pe, kv_c_normed  as in mla_key_concat_cache_insert (q is only read).
+ *   v            device bf16 [Tp, H, dv], strides (v_s0, v_s1); dv a multiple of 8.
+ *   q_fp8        device out E4M3 [Tp, H, dn + 64] contiguous: [q_nope | rope(q_pe)] * q_scale_inv.
+ *   k_fp8        device out E4M3 [Tp, H, dn + 64] contiguous: [k_nope | rope(k_pe)] * k_scale_inv.
+ *   v_fp8        device out E4M3 [Tp, H, dv] contiguous: v * v_scale_inv.
+ *   kv_cache     plain fp8 cache (576-byte entries): [kv_c_normed | rope(k_pe)] * cache_scale_inv
+ *                at slot_mapping[t].
+ *   q_scale_inv, k_scale_inv, v_scale_inv, cache_scale_inv  device fp32 scalars (1 / scale).
+ * Errors as mla_key_concat_cache_insert, plus dv.
+ */
+MLA_API int mla_qkv_quant_cache_fp8_insert(const void* q, int64_t q_s0, int64_t q_s1, const void* k_nope,
+                                           int64_t kn_s0, int64_t kn_s1, const void* k_pe, int64_t kp_s0,
+                                           const void* kv_c_normed, int64_t kv_s0, const void* v, int64_t v_s0,
+                                           int64_t v_s1, void* q_fp8, void* k_fp8, void* v_fp8, void* kv_cache,
+                                           int64_t num_blocks, int64_t block_stride_bytes,
+                                           int64_t entry_stride_bytes, int32_t block_size,
+                                           const int64_t* slot_mapping, const float* q_scale_inv,
+                                           const float* k_scale_inv, const float* v_scale_inv,
+                                           const float* cache_scale_inv, const int64_t* positions,
+                                           const float* cos_sin_cache, int64_t max_position, int32_t Tp, int32_t H,
+                                           int32_t dn, int32_t dv, cudaStream_t stream);
+
+/*
  * Sparse MLA forward over fp8_ds_mla records with CSR key lists.
  * Follows: "vllm.models.kimi_k3.amd.ops.flydsl_sparse_mla", flydsl_sparse_mla_fp8ds_fwd
  * (sparse_mla_fwd semantics) and flydsl_sparse_mla_fp8ds_supported (argument checks).
@@ -237,6 +300,30 @@ MLA_API int mla_gather_dequant(const void* kv_cache, mla_cache_format fmt, int64
                        int64_t block_stride_bytes, int64_t entry_stride_bytes,
                        int32_t block_size, const int64_t* slots, int64_t n, float* out,
                        cudaStream_t stream);
+
+/*
+ * Test aid: the same sparse forward as mla_sparse_fwd (same arguments, results within the
+ * attention tolerance of it), computed by the second kernel design of this library: records
+ * gathered by per-entry bulk copies and converted exactly to f16 in shared memory before the
+ * tensor-core products.  The test-suite runs both designs on the same cases; product callers
+ * use mla_sparse_fwd.
+ */
+MLA_API int mla_sparse_fwd_staged(const void* q, int64_t q_s0, int64_t q_s1, const void* kv_records,
+                                  int64_t record_stride_bytes, int64_t num_records, const int32_t* kv_indptr,
+                                  const int32_t* kv_indices, int64_t n_indices, float softmax_scale,
+                                  int has_invalid, void* out, int64_t o_s0, int64_t o_s1, float* lse,
+                                  int32_t T, int32_t H, cudaStream_t stream);
+
+/*
+ * Test aid for the bounded in-kernel waits.  Arms the next mla_paged_decode call on the
+ * calling host thread that runs the bf16 / plain-fp8 page kernel (block sizes 16..128 or
+ * multiples of 128): that launch hands its first work item to the consumer warps but issues
+ * none of its loads, and every wait in it gives up after wait_us microseconds.  The call
+ * returns MLA_OK; its outputs are invalid; MLA_DEVERR_TIMEOUT is set in the device error
+ * word.  No copy or tensor-core operation is in flight when the kernel exits, so the next
+ * call runs normally.  wait_us <= 0 disarms.
+ */
+MLA_API void mla_debug_stall_next_decode(int32_t wait_us);
 
 #ifdef __cplusplus
 }

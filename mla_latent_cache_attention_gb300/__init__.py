@@ -9,9 +9,17 @@ Entry points (same names as the C ABI, without the ``mla_`` prefix):
 
   q_concat_cache_insert  decode epilogue: mqa_q = [ql_nope | q_pe] (+ GPT-J RoPE), latent
                          insert into a bf16 / plain fp8 / fp8_ds_mla paged cache
+  key_concat_cache_insert   prefill epilogue (bf16 / fp8_ds_mla cache): full key
+                         [k_nope | rope(k_pe)], q RoPE in place, latent insert
+  qkv_quant_cache_fp8_insert  prefill epilogue (plain fp8 cache): E4M3 q / k / v with their
+                         own scales, latent insert with the cache scale
   sparse_fwd             sparse CSR forward over 656-byte fp8_ds_mla records
   paged_decode           paged decode / spec-verify (split-K + LSE merge)
   gather_dequant         paged entries -> exact fp32 values (test aid)
+
+Every tensor argument is checked here before the call (CUDA device, dtype, rank, unit
+innermost stride; index tensors contiguous), so that a wrong tensor raises instead of being
+read with the wrong layout.  Sparse indices may be int32 or int64.
 """
 from __future__ import annotations
 
@@ -63,7 +71,16 @@ def lib():
         L.mla_profile_attention_events.argtypes = [vp, vp]
         L.mla_profile_attention_events.restype = None
         L.mla_gather_dequant.argtypes = [vp, i32, i64, i64, i64, i32, vp, i64, vp, vp]
-        for f in ("mla_q_concat_cache_insert", "mla_sparse_fwd", "mla_paged_decode", "mla_gather_dequant"):
+        L.mla_sparse_fwd_staged.argtypes = L.mla_sparse_fwd.argtypes
+        L.mla_key_concat_cache_insert.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, vp, i64, vp, vp, i32, i64, i64,
+                                                  i64, i32, vp, vp, vp, i64, i32, i32, i32, vp]
+        L.mla_qkv_quant_cache_fp8_insert.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, vp, i64, vp, i64, i64, vp,
+                                                     vp, vp, vp, i64, i64, i64, i32, vp, vp, vp, vp, vp, vp, vp, i64,
+                                                     i32, i32, i32, i32, vp]
+        L.mla_debug_stall_next_decode.argtypes = [i32]
+        L.mla_debug_stall_next_decode.restype = None
+        for f in ("mla_q_concat_cache_insert", "mla_sparse_fwd", "mla_sparse_fwd_staged", "mla_paged_decode",
+                  "mla_gather_dequant", "mla_key_concat_cache_insert", "mla_qkv_quant_cache_fp8_insert"):
             getattr(L, f).restype = ctypes.c_int
         L.mla_read_device_errors.restype = ctypes.c_int
         _lib = L
@@ -89,12 +106,51 @@ def _fmt(fmt) -> int:
     return int(fmt)
 
 
+_BYTE_TYPES = (torch.uint8, torch.int8)
+_INT32_MAX = 2 ** 31 - 1
+
+
+def _need(t, name, dtypes, device, *, ndim=None, contiguous=False, inner=True):
+    """Marshalling check of one tensor argument: a CUDA tensor on `device` of one of `dtypes`,
+    with `ndim` dimensions, unit innermost stride (inner) or fully contiguous."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype not in dtypes:
+        raise TypeError(f"{name} has dtype {t.dtype}; expected one of {', '.join(str(d) for d in dtypes)}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dimensions, got shape {tuple(t.shape)}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if inner and t.dim() > 0 and t.stride(-1) != 1 and t.shape[-1] > 1:
+        raise ValueError(f"{name} must have a unit innermost stride")
+    return t
+
+
+def _cuda_device(t) -> torch.device:
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise ValueError("inputs must be CUDA tensors")
+    return t.device
+
+
+def _index_i32(t, name, device, lo, hi):
+    """int32 index tensor for the C ABI.  int64 input (accepted by the sparse forward's
+    interface) is narrowed on the device after clamping to [lo, hi], so an id outside int32
+    keeps its meaning: below lo stays masked / flagged, above hi stays out of range."""
+    _need(t, name, (torch.int32, torch.int64), device, ndim=1, contiguous=True)
+    if t.dtype == torch.int64:
+        t = t.clamp(lo, hi).to(torch.int32)
+    return t
+
+
 def _cache_geometry(kv_cache: torch.Tensor):
     """[num_blocks, block_size, entry_stride] view of a paged cache (any 1- or 2-byte dtype)."""
     es = kv_cache.element_size()
-    if kv_cache.dim() == 4:      # [nb, 1, bs, entry] (a head axis of size 1)
+    if kv_cache.dim() == 4 and kv_cache.shape[1] == 1:      # [nb, 1, bs, entry] (a head axis of size 1)
         kv_cache = kv_cache.squeeze(1)
-    assert kv_cache.dim() == 3 and kv_cache.stride(2) == 1, "cache must be [num_blocks, block_size, entry]"
+    if kv_cache.dim() != 3 or kv_cache.stride(2) != 1:
+        raise ValueError("kv_cache must be [num_blocks, block_size, entry] with a unit innermost stride")
     return kv_cache.shape[0], kv_cache.stride(0) * es, kv_cache.stride(1) * es, kv_cache.shape[1]
 
 
@@ -125,34 +181,129 @@ def q_concat_cache_insert(ql_nope, q_pe, kv_c_normed, k_pe, kv_cache, slot_mappi
     """Decode epilogue.  Returns mqa_q [B, H, 576] (bf16, or uint8 E4M3 codes for fp8);
     writes kv_cache in place."""
     fmt = _fmt(fmt)
-    k_pe = k_pe.reshape(k_pe.shape[0], -1)
+    dev = _cuda_device(ql_nope)
+    bf = (torch.bfloat16,)
+    _need(ql_nope, "ql_nope", bf, dev, ndim=3)
+    _need(q_pe, "q_pe", bf, dev, ndim=3)
+    _need(kv_c_normed, "kv_c_normed", bf, dev, ndim=2)
+    k_pe = _need(k_pe, "k_pe", bf, dev).reshape(k_pe.shape[0], -1)
+    _need(slot_mapping, "slot_mapping", (torch.int64,), dev, ndim=1, contiguous=True)
+    if positions is not None:
+        _need(positions, "positions", (torch.int64,), dev, ndim=1, contiguous=True)
+    if cos_sin_cache is not None:
+        _need(cos_sin_cache, "cos_sin_cache", (torch.float32,), dev, ndim=2, contiguous=True)
+    for n, t in (("q_scale_inv", q_scale_inv), ("cache_scale_inv", cache_scale_inv)):
+        if t is not None:
+            _need(t, n, (torch.float32,), dev)
     B, H, _ = ql_nope.shape
     if mqa_q is None:
         dt = torch.uint8 if fmt == CACHE_FP8 else torch.bfloat16
-        mqa_q = torch.empty((B, H, 576), dtype=dt, device=ql_nope.device)
+        mqa_q = torch.empty((B, H, 576), dtype=dt, device=dev)
+    _need(mqa_q, "mqa_q", _BYTE_TYPES if fmt == CACHE_FP8 else bf, dev, ndim=3, contiguous=True)
+    _need(kv_cache, "kv_cache", _BYTE_TYPES + bf, dev)
     nb, bstride, estride, bs = _cache_geometry(kv_cache)
     max_pos = 0 if cos_sin_cache is None else cos_sin_cache.shape[0]
-    _check(lib().mla_q_concat_cache_insert(
-        _ptr(ql_nope), ql_nope.stride(0), ql_nope.stride(1), _ptr(q_pe), q_pe.stride(0), q_pe.stride(1),
-        _ptr(kv_c_normed), kv_c_normed.stride(0), _ptr(k_pe), k_pe.stride(0), _ptr(mqa_q), _ptr(kv_cache),
-        fmt, nb, bstride, estride, bs, _ptr(slot_mapping), _ptr(q_scale_inv), _ptr(cache_scale_inv),
-        _ptr(positions), _ptr(cos_sin_cache), max_pos, B, H, _stream(ql_nope)))
+    with torch.cuda.device(dev):
+        _check(lib().mla_q_concat_cache_insert(
+            _ptr(ql_nope), ql_nope.stride(0), ql_nope.stride(1), _ptr(q_pe), q_pe.stride(0), q_pe.stride(1),
+            _ptr(kv_c_normed), kv_c_normed.stride(0), _ptr(k_pe), k_pe.stride(0), _ptr(mqa_q), _ptr(kv_cache),
+            fmt, nb, bstride, estride, bs, _ptr(slot_mapping), _ptr(q_scale_inv), _ptr(cache_scale_inv),
+            _ptr(positions), _ptr(cos_sin_cache), max_pos, B, H, _stream(ql_nope)))
     return mqa_q
 
 
+def _prefill_common(q, k_nope, k_pe, kv_c_normed, slot_mapping, positions, cos_sin_cache):
+    dev = _cuda_device(q)
+    bf = (torch.bfloat16,)
+    _need(q, "q", bf, dev, ndim=3)
+    _need(k_nope, "k_nope", bf, dev, ndim=3)
+    k_pe = _need(k_pe, "k_pe", bf, dev).reshape(k_pe.shape[0], -1)
+    _need(kv_c_normed, "kv_c_normed", bf, dev, ndim=2)
+    _need(slot_mapping, "slot_mapping", (torch.int64,), dev, ndim=1, contiguous=True)
+    if positions is not None:
+        _need(positions, "positions", (torch.int64,), dev, ndim=1, contiguous=True)
+    if cos_sin_cache is not None:
+        _need(cos_sin_cache, "cos_sin_cache", (torch.float32,), dev, ndim=2, contiguous=True)
+    Tp, H, dn = k_nope.shape
+    if q.shape != (Tp, H, dn + 64):
+        raise ValueError(f"q must be [Tp, H, dn + 64] = {(Tp, H, dn + 64)}, got {tuple(q.shape)}")
+    return dev, k_pe, Tp, H, dn
+
+
+def key_concat_cache_insert(q, k_nope, k_pe, kv_c_normed, kv_cache, slot_mapping, *, fmt, positions=None,
+                            cos_sin_cache=None, k_out=None):
+    """Prefill epilogue for the bf16 / fp8_ds_mla cache.  Rotates the rope part of q in place
+    (when positions are given), writes kv_cache in place and returns k_out [Tp, H, dn + 64]."""
+    fmt = _fmt(fmt)
+    dev, k_pe, Tp, H, dn = _prefill_common(q, k_nope, k_pe, kv_c_normed, slot_mapping, positions, cos_sin_cache)
+    if k_out is None:
+        k_out = torch.empty((Tp, H, dn + 64), dtype=torch.bfloat16, device=dev)
+    _need(k_out, "k_out", (torch.bfloat16,), dev, ndim=3, contiguous=True)
+    _need(kv_cache, "kv_cache", _BYTE_TYPES + (torch.bfloat16,), dev)
+    nb, bstride, estride, bs = _cache_geometry(kv_cache)
+    max_pos = 0 if cos_sin_cache is None else cos_sin_cache.shape[0]
+    with torch.cuda.device(dev):
+        _check(lib().mla_key_concat_cache_insert(
+            _ptr(q), q.stride(0), q.stride(1), _ptr(k_nope), k_nope.stride(0), k_nope.stride(1), _ptr(k_pe),
+            k_pe.stride(0), _ptr(kv_c_normed), kv_c_normed.stride(0), _ptr(k_out), _ptr(kv_cache), fmt, nb, bstride,
+            estride, bs, _ptr(slot_mapping), _ptr(positions), _ptr(cos_sin_cache), max_pos, Tp, H, dn, _stream(q)))
+    return k_out
+
+
+def qkv_quant_cache_fp8_insert(q, k_nope, k_pe, kv_c_normed, v, kv_cache, slot_mapping, *, q_scale_inv, k_scale_inv,
+                               v_scale_inv, cache_scale_inv, positions=None, cos_sin_cache=None):
+    """Prefill epilogue for the plain fp8 cache.  Returns (q_fp8, k_fp8, v_fp8) as uint8 E4M3
+    codes; writes kv_cache in place.  The four scales are device fp32 scalars (1 / scale)."""
+    dev, k_pe, Tp, H, dn = _prefill_common(q, k_nope, k_pe, kv_c_normed, slot_mapping, positions, cos_sin_cache)
+    _need(v, "v", (torch.bfloat16,), dev, ndim=3)
+    dv = v.shape[2]
+    for n, t in (("q_scale_inv", q_scale_inv), ("k_scale_inv", k_scale_inv), ("v_scale_inv", v_scale_inv),
+                 ("cache_scale_inv", cache_scale_inv)):
+        _need(t, n, (torch.float32,), dev)
+    _need(kv_cache, "kv_cache", _BYTE_TYPES, dev)
+    q8 = torch.empty((Tp, H, dn + 64), dtype=torch.uint8, device=dev)
+    k8 = torch.empty((Tp, H, dn + 64), dtype=torch.uint8, device=dev)
+    v8 = torch.empty((Tp, H, dv), dtype=torch.uint8, device=dev)
+    nb, bstride, estride, bs = _cache_geometry(kv_cache)
+    max_pos = 0 if cos_sin_cache is None else cos_sin_cache.shape[0]
+    with torch.cuda.device(dev):
+        _check(lib().mla_qkv_quant_cache_fp8_insert(
+            _ptr(q), q.stride(0), q.stride(1), _ptr(k_nope), k_nope.stride(0), k_nope.stride(1), _ptr(k_pe),
+            k_pe.stride(0), _ptr(kv_c_normed), kv_c_normed.stride(0), _ptr(v), v.stride(0), v.stride(1), _ptr(q8),
+            _ptr(k8), _ptr(v8), _ptr(kv_cache), nb, bstride, estride, bs, _ptr(slot_mapping), _ptr(q_scale_inv),
+            _ptr(k_scale_inv), _ptr(v_scale_inv), _ptr(cache_scale_inv), _ptr(positions), _ptr(cos_sin_cache), max_pos,
+            Tp, H, dn, dv, _stream(q)))
+    return q8, k8, v8
+
+
 def sparse_fwd(q, kv_records, kv_indptr, kv_indices, softmax_scale, *, has_invalid=False, out=None,
-               return_lse=False, num_records=None):
-    """Sparse forward over fp8_ds_mla records [N, >=656] (uint8).  Returns (out, lse)."""
+               return_lse=False, num_records=None, kernel="gather"):
+    """Sparse forward over fp8_ds_mla records [N, >=656] (uint8).  Returns (out, lse).
+
+    kv_indptr / kv_indices may be int32 or int64 (int64 is narrowed on the device, keeping
+    masked and out-of-range ids as such).  kernel="staged" runs the test aid
+    mla_sparse_fwd_staged (the second kernel design) instead of mla_sparse_fwd."""
+    dev = _cuda_device(q)
+    _need(q, "q", (torch.bfloat16,), dev, ndim=3)
+    _need(kv_records, "kv_records", _BYTE_TYPES, dev)
     T, H, _ = q.shape
-    if out is None:
-        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q.device)
-    lse = torch.empty((T, H), dtype=torch.float32, device=q.device) if return_lse else None
     rec = kv_records.reshape(-1, kv_records.shape[-1]) if kv_records.dim() != 2 else kv_records
     n_rec = rec.shape[0] if num_records is None else num_records
-    _check(lib().mla_sparse_fwd(
-        _ptr(q), q.stride(0), q.stride(1), _ptr(rec), rec.stride(0) * rec.element_size(), n_rec,
-        _ptr(kv_indptr), _ptr(kv_indices), kv_indices.numel(), float(softmax_scale), int(bool(has_invalid)),
-        _ptr(out), out.stride(0), out.stride(1), _ptr(lse), T, H, _stream(q)))
+    if kv_indptr.numel() != T + 1:
+        raise ValueError(f"kv_indptr must have T + 1 = {T + 1} entries, got {kv_indptr.numel()}")
+    n_idx = kv_indices.numel()
+    kv_indptr = _index_i32(kv_indptr, "kv_indptr", dev, 0, min(n_idx, _INT32_MAX))
+    kv_indices = _index_i32(kv_indices, "kv_indices", dev, -1, min(n_rec, _INT32_MAX))
+    if out is None:
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", (torch.bfloat16,), dev, ndim=3)
+    lse = torch.empty((T, H), dtype=torch.float32, device=dev) if return_lse else None
+    fn = {"gather": lib().mla_sparse_fwd, "staged": lib().mla_sparse_fwd_staged}[kernel]
+    with torch.cuda.device(dev):
+        _check(fn(
+            _ptr(q), q.stride(0), q.stride(1), _ptr(rec), rec.stride(0) * rec.element_size(), n_rec,
+            _ptr(kv_indptr), _ptr(kv_indices), n_idx, float(softmax_scale), int(bool(has_invalid)),
+            _ptr(out), out.stride(0), out.stride(1), _ptr(lse), T, H, _stream(q)))
     return out, lse
 
 
@@ -165,30 +316,49 @@ def paged_decode(q, kv_cache, block_table, seq_lens, *, fmt, q_len=1, max_contex
     """Paged decode / spec-verify.  q [B*q_len, H, 576] (bf16, or uint8 E4M3 codes for fp8).
     Returns (out [B*q_len, H, 512] bf16, lse or None)."""
     fmt = _fmt(fmt)
+    dev = _cuda_device(q)
+    _need(q, "q", _BYTE_TYPES if fmt == CACHE_FP8 else (torch.bfloat16,), dev, ndim=3)
+    _need(kv_cache, "kv_cache", _BYTE_TYPES + (torch.bfloat16,), dev)
+    _need(block_table, "block_table", (torch.int32,), dev, ndim=2)
+    _need(seq_lens, "seq_lens", (torch.int32,), dev, ndim=1, contiguous=True)
     rows, H, _ = q.shape
     B = seq_lens.numel()
-    assert rows == B * q_len, "q rows must be B * q_len"
+    if rows != B * q_len:
+        raise ValueError(f"q has {rows} rows; expected B * q_len = {B * q_len}")
     if out is None:
-        out = torch.empty((rows, H, 512), dtype=torch.bfloat16, device=q.device)
-    lse = torch.empty((rows, H), dtype=torch.float32, device=q.device) if return_lse else None
-    need = paged_decode_workspace_size(B, q_len, H, max_context)
-    if workspace is None and need > 0:
-        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    nb, bstride, estride, bs = _cache_geometry(kv_cache)
-    _check(lib().mla_paged_decode(
-        _ptr(q), q.stride(0), q.stride(1), _ptr(kv_cache), fmt, nb, bstride, estride, bs,
-        _ptr(block_table), block_table.stride(0), _ptr(seq_lens), B, q_len, H, int(max_context),
-        float(softmax_scale), float(q_scale), float(k_scale), _ptr(out), out.stride(0), out.stride(1),
-        _ptr(lse), _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
-        _stream(q)))
+        out = torch.empty((rows, H, 512), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", (torch.bfloat16,), dev, ndim=3)
+    lse = torch.empty((rows, H), dtype=torch.float32, device=dev) if return_lse else None
+    with torch.cuda.device(dev):
+        need = paged_decode_workspace_size(B, q_len, H, max_context)
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        if workspace is not None:
+            _need(workspace, "workspace", _BYTE_TYPES, dev, contiguous=True)
+        nb, bstride, estride, bs = _cache_geometry(kv_cache)
+        _check(lib().mla_paged_decode(
+            _ptr(q), q.stride(0), q.stride(1), _ptr(kv_cache), fmt, nb, bstride, estride, bs,
+            _ptr(block_table), block_table.stride(0), _ptr(seq_lens), B, q_len, H, int(max_context),
+            float(softmax_scale), float(q_scale), float(k_scale), _ptr(out), out.stride(0), out.stride(1),
+            _ptr(lse), _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
+            _stream(q)))
     return out, lse
 
 
 def gather_dequant(kv_cache, slots, *, fmt):
     """Exact fp32 values [n, 576] of the entries at `slots` (int64)."""
     fmt = _fmt(fmt)
+    dev = _cuda_device(kv_cache)
+    _need(slots, "slots", (torch.int64,), dev, ndim=1, contiguous=True)
     nb, bstride, estride, bs = _cache_geometry(kv_cache)
-    out = torch.empty((slots.numel(), 576), dtype=torch.float32, device=kv_cache.device)
-    _check(lib().mla_gather_dequant(_ptr(kv_cache), fmt, nb, bstride, estride, bs, _ptr(slots),
-                                    slots.numel(), _ptr(out), _stream(kv_cache)))
+    out = torch.empty((slots.numel(), 576), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        _check(lib().mla_gather_dequant(_ptr(kv_cache), fmt, nb, bstride, estride, bs, _ptr(slots),
+                                        slots.numel(), _ptr(out), _stream(kv_cache)))
     return out
+
+
+def debug_stall_next_decode(wait_us: int):
+    """Test aid (mla_debug_stall_next_decode): the next page-kernel decode on this thread
+    issues no loads and its waits give up after wait_us microseconds."""
+    lib().mla_debug_stall_next_decode(int(wait_us))

@@ -4,7 +4,6 @@
 #include <cuda.h>
 
 #include <cstdarg>
-#include <cstdlib>
 #include <cstdio>
 #include <cstring>
 #include <mutex>
@@ -111,16 +110,9 @@ size_t workspace_bytes_for(int64_t n_rows, int H, const SplitPlan& sp) {
   return ((po + 255) & ~size_t(255)) + ((pl + 255) & ~size_t(255)) + 256;
 }
 
-// The sparse forward runs the gather-warp fp8_ds_mla kernel (codes straight into the tensor
-// cores) unless MLA_SPARSE_GATHER=0 selects the staged-converter kernel (codes converted to
-// f16 in shared memory).  Read once per process.
-bool sparse_gather_kernel() {
-  static const int v = [] {
-    const char* e = getenv("MLA_SPARSE_GATHER");
-    return (e && e[0] == '0') ? 0 : 1;
-  }();
-  return v == 1;
-}
+// Test aid: wait limit (microseconds) of the next page-kernel launch on this thread, whose
+// producer then issues no loads; 0 = none armed.
+thread_local int g_stall_next_us = 0;
 
 int grid_for(int64_t items, int sms) {
   return static_cast<int>(items < sms ? items : sms);
@@ -333,11 +325,158 @@ extern "C" int mla_q_concat_cache_insert(const void* ql_nope, int64_t ql_s0, int
 }
 
 // ------------------------------------------------------------------------------------------
-extern "C" int mla_sparse_fwd(const void* q, int64_t q_s0, int64_t q_s1, const void* kv_records,
-                              int64_t record_stride_bytes, int64_t num_records,
-                              const int32_t* kv_indptr, const int32_t* kv_indices, int64_t n_indices,
-                              float softmax_scale, int has_invalid, void* out, int64_t o_s0,
-                              int64_t o_s1, float* lse, int32_t T, int32_t H, cudaStream_t stream) {
+// ------------------------------------------------------------------------------------------
+// Prefill epilogues: shared argument checks of the key-concat and fp8-quant entry points.
+static int prefill_common_checks(const void* q, int64_t q_s0, int64_t q_s1, const void* k_nope, int64_t kn_s0,
+                                 int64_t kn_s1, const void* k_pe, int64_t kp_s0, const void* kv_c, int64_t kv_s0,
+                                 const void* kv_cache, int fmt, int64_t num_blocks, int64_t block_stride_bytes,
+                                 int64_t entry_stride_bytes, int32_t block_size, const int64_t* slot_mapping,
+                                 const int64_t* positions, const float* cos_sin_cache, int64_t max_position,
+                                 int32_t H, int32_t dn) {
+  if (!q || !k_nope || !k_pe || !kv_c || !kv_cache || !slot_mapping)
+    return fail(MLA_ERR_INVALID, "a required pointer is NULL");
+  if (dn < 8 || dn % 8) return fail(MLA_ERR_UNSUPPORTED, "the NoPE head dim must be a positive multiple of 8, got %d", dn);
+  if (q_s1 < dn + 64 || q_s0 < static_cast<int64_t>(H) * q_s1 || kn_s1 < dn || kn_s0 < static_cast<int64_t>(H) * kn_s1 ||
+      kp_s0 < 64 || kv_s0 < 512)
+    return fail(MLA_ERR_INVALID, "activation strides overlap rows");
+  if (!aligned(q, 2) || !aligned(k_nope, 2) || !aligned(k_pe, 2) || !aligned(kv_c, 2))
+    return fail(MLA_ERR_INVALID, "bf16 tensors must be 2-byte aligned");
+  if (block_size < 1 || num_blocks < 1) return fail(MLA_ERR_INVALID, "bad cache geometry");
+  if (entry_stride_bytes < entry_bytes(static_cast<mla_cache_format>(fmt)) ||
+      block_stride_bytes < entry_stride_bytes * block_size)
+    return fail(MLA_ERR_INVALID, "cache strides smaller than the entries");
+  if (fmt != MLA_CACHE_FP8 && (entry_stride_bytes % 4 || block_stride_bytes % 4 || !aligned(kv_cache, 4)))
+    return fail(MLA_ERR_INVALID, "bf16 / fp8_ds_mla cache entries must be 4-byte aligned");
+  if ((positions == nullptr) != (cos_sin_cache == nullptr))
+    return fail(MLA_ERR_INVALID, "positions and cos_sin_cache must be given together");
+  if (positions && max_position < 1) return fail(MLA_ERR_INVALID, "max_position must be >= 1");
+  return MLA_OK;
+}
+
+extern "C" int mla_key_concat_cache_insert(void* q, int64_t q_s0, int64_t q_s1, const void* k_nope, int64_t kn_s0,
+                                           int64_t kn_s1, const void* k_pe, int64_t kp_s0, const void* kv_c_normed,
+                                           int64_t kv_s0, void* k_out, void* kv_cache, mla_cache_format fmt,
+                                           int64_t num_blocks, int64_t block_stride_bytes, int64_t entry_stride_bytes,
+                                           int32_t block_size, const int64_t* slot_mapping, const int64_t* positions,
+                                           const float* cos_sin_cache, int64_t max_position, int32_t Tp, int32_t H,
+                                           int32_t dn, cudaStream_t stream) {
+  if (fmt != MLA_CACHE_BF16 && fmt != MLA_CACHE_FP8_DS_MLA)
+    return fail(MLA_ERR_INVALID, "the key-concat epilogue writes a bf16 or fp8_ds_mla cache (format %d)",
+                static_cast<int>(fmt));
+  if (Tp < 0 || H < 1) return fail(MLA_ERR_INVALID, "bad shape Tp=%d H=%d", Tp, H);
+  if (Tp == 0) return ok();
+  if (int rc = prefill_common_checks(q, q_s0, q_s1, k_nope, kn_s0, kn_s1, k_pe, kp_s0, kv_c_normed, kv_s0, kv_cache,
+                                     fmt, num_blocks, block_stride_bytes, entry_stride_bytes, block_size, slot_mapping,
+                                     positions, cos_sin_cache, max_position, H, dn))
+    return rc;
+  if (!k_out) return fail(MLA_ERR_INVALID, "k_out is NULL");
+  if (!aligned(k_out, 2)) return fail(MLA_ERR_INVALID, "k_out must be 2-byte aligned");
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  PrefillEpiParams p{};
+  p.q = static_cast<uint16_t*>(q);
+  p.q_s0 = q_s0;
+  p.q_s1 = q_s1;
+  p.k_nope = static_cast<const uint16_t*>(k_nope);
+  p.kn_s0 = kn_s0;
+  p.kn_s1 = kn_s1;
+  p.k_pe = static_cast<const uint16_t*>(k_pe);
+  p.kp_s0 = kp_s0;
+  p.kv_c = static_cast<const uint16_t*>(kv_c_normed);
+  p.kv_s0 = kv_s0;
+  p.k_out = static_cast<uint16_t*>(k_out);
+  p.cache = static_cast<uint8_t*>(kv_cache);
+  p.num_blocks = num_blocks;
+  p.block_stride = block_stride_bytes;
+  p.entry_stride = entry_stride_bytes;
+  p.block_size = block_size;
+  p.slot_mapping = slot_mapping;
+  p.positions = positions;
+  p.cos_sin = cos_sin_cache;
+  p.max_position = max_position;
+  p.H = H;
+  p.dn = dn;
+  p.vec = aligned(k_nope, 16) && aligned(k_out, 16) && kn_s0 % 8 == 0 && kn_s1 % 8 == 0;
+  p.err = d->err;
+  if (launch_prefill_epilogue(static_cast<int>(fmt), p, Tp, stream) != cudaSuccess)
+    return fail(MLA_ERR_CUDA, "prefill epilogue launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  return ok();
+}
+
+extern "C" int mla_qkv_quant_cache_fp8_insert(const void* q, int64_t q_s0, int64_t q_s1, const void* k_nope,
+                                              int64_t kn_s0, int64_t kn_s1, const void* k_pe, int64_t kp_s0,
+                                              const void* kv_c_normed, int64_t kv_s0, const void* v, int64_t v_s0,
+                                              int64_t v_s1, void* q_fp8, void* k_fp8, void* v_fp8, void* kv_cache,
+                                              int64_t num_blocks, int64_t block_stride_bytes,
+                                              int64_t entry_stride_bytes, int32_t block_size,
+                                              const int64_t* slot_mapping, const float* q_scale_inv,
+                                              const float* k_scale_inv, const float* v_scale_inv,
+                                              const float* cache_scale_inv, const int64_t* positions,
+                                              const float* cos_sin_cache, int64_t max_position, int32_t Tp, int32_t H,
+                                              int32_t dn, int32_t dv, cudaStream_t stream) {
+  if (Tp < 0 || H < 1) return fail(MLA_ERR_INVALID, "bad shape Tp=%d H=%d", Tp, H);
+  if (Tp == 0) return ok();
+  if (int rc = prefill_common_checks(q, q_s0, q_s1, k_nope, kn_s0, kn_s1, k_pe, kp_s0, kv_c_normed, kv_s0, kv_cache,
+                                     MLA_CACHE_FP8, num_blocks, block_stride_bytes, entry_stride_bytes, block_size,
+                                     slot_mapping, positions, cos_sin_cache, max_position, H, dn))
+    return rc;
+  if (!v || !q_fp8 || !k_fp8 || !v_fp8 || !q_scale_inv || !k_scale_inv || !v_scale_inv || !cache_scale_inv)
+    return fail(MLA_ERR_INVALID, "a required pointer is NULL");
+  if (dv < 8 || dv % 8) return fail(MLA_ERR_UNSUPPORTED, "the value head dim must be a positive multiple of 8, got %d", dv);
+  if (v_s1 < dv || v_s0 < static_cast<int64_t>(H) * v_s1) return fail(MLA_ERR_INVALID, "v strides overlap rows");
+  if (!aligned(v, 2)) return fail(MLA_ERR_INVALID, "v must be 2-byte aligned");
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  PrefillEpiParams p{};
+  p.q = const_cast<uint16_t*>(static_cast<const uint16_t*>(q));   // read only for the fp8 epilogue
+  p.q_s0 = q_s0;
+  p.q_s1 = q_s1;
+  p.k_nope = static_cast<const uint16_t*>(k_nope);
+  p.kn_s0 = kn_s0;
+  p.kn_s1 = kn_s1;
+  p.k_pe = static_cast<const uint16_t*>(k_pe);
+  p.kp_s0 = kp_s0;
+  p.kv_c = static_cast<const uint16_t*>(kv_c_normed);
+  p.kv_s0 = kv_s0;
+  p.v = static_cast<const uint16_t*>(v);
+  p.v_s0 = v_s0;
+  p.v_s1 = v_s1;
+  p.q8 = static_cast<uint8_t*>(q_fp8);
+  p.k8 = static_cast<uint8_t*>(k_fp8);
+  p.v8 = static_cast<uint8_t*>(v_fp8);
+  p.cache = static_cast<uint8_t*>(kv_cache);
+  p.num_blocks = num_blocks;
+  p.block_stride = block_stride_bytes;
+  p.entry_stride = entry_stride_bytes;
+  p.block_size = block_size;
+  p.slot_mapping = slot_mapping;
+  p.q_scale_inv = q_scale_inv;
+  p.k_scale_inv = k_scale_inv;
+  p.v_scale_inv = v_scale_inv;
+  p.cache_scale_inv = cache_scale_inv;
+  p.positions = positions;
+  p.cos_sin = cos_sin_cache;
+  p.max_position = max_position;
+  p.H = H;
+  p.dn = dn;
+  p.dv = dv;
+  p.vec = aligned(q, 16) && aligned(k_nope, 16) && aligned(v, 16) && aligned(q_fp8, 8) && aligned(k_fp8, 8) &&
+          aligned(v_fp8, 8) && q_s0 % 8 == 0 && q_s1 % 8 == 0 && kn_s0 % 8 == 0 && kn_s1 % 8 == 0 && v_s0 % 8 == 0 &&
+          v_s1 % 8 == 0;
+  p.err = d->err;
+  if (launch_prefill_epilogue(1, p, Tp, stream) != cudaSuccess)
+    return fail(MLA_ERR_CUDA, "prefill epilogue launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  return ok();
+}
+
+// The sparse forward: the gather-warp fp8_ds_mla kernel (codes straight into the tensor
+// cores), or for the test aid mla_sparse_fwd_staged the staged-converter kernel (codes
+// converted to f16 in shared memory).
+static int sparse_fwd_impl(const void* q, int64_t q_s0, int64_t q_s1, const void* kv_records,
+                           int64_t record_stride_bytes, int64_t num_records, const int32_t* kv_indptr,
+                           const int32_t* kv_indices, int64_t n_indices, float softmax_scale, int has_invalid,
+                           void* out, int64_t o_s0, int64_t o_s1, float* lse, int32_t T, int32_t H,
+                           cudaStream_t stream, bool staged) {
   if (T < 0) return fail(MLA_ERR_INVALID, "T must be >= 0");
   if (H < 1 || H > 128) return fail(MLA_ERR_UNSUPPORTED, "H must be in [1, 128], got %d", H);
   if (T == 0) return ok();
@@ -385,7 +524,7 @@ extern "C" int mla_sparse_fwd(const void* q, int64_t q_s0, int64_t q_s1, const v
   p.err = d->err;
   prof_begin(stream);
   cudaError_t e;
-  if (sparse_gather_kernel()) {
+  if (!staged) {
     e = launch_ds_sparse(p, grid_for(items, d->sms), stream);
   } else {
     AttnParams a{};
@@ -419,6 +558,26 @@ extern "C" int mla_sparse_fwd(const void* q, int64_t q_s0, int64_t q_s1, const v
     return fail(MLA_ERR_CUDA, "sparse attention launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return ok();
 }
+
+extern "C" int mla_sparse_fwd(const void* q, int64_t q_s0, int64_t q_s1, const void* kv_records,
+                              int64_t record_stride_bytes, int64_t num_records,
+                              const int32_t* kv_indptr, const int32_t* kv_indices, int64_t n_indices,
+                              float softmax_scale, int has_invalid, void* out, int64_t o_s0,
+                              int64_t o_s1, float* lse, int32_t T, int32_t H, cudaStream_t stream) {
+  return sparse_fwd_impl(q, q_s0, q_s1, kv_records, record_stride_bytes, num_records, kv_indptr, kv_indices,
+                         n_indices, softmax_scale, has_invalid, out, o_s0, o_s1, lse, T, H, stream, false);
+}
+
+extern "C" int mla_sparse_fwd_staged(const void* q, int64_t q_s0, int64_t q_s1, const void* kv_records,
+                                     int64_t record_stride_bytes, int64_t num_records,
+                                     const int32_t* kv_indptr, const int32_t* kv_indices, int64_t n_indices,
+                                     float softmax_scale, int has_invalid, void* out, int64_t o_s0,
+                                     int64_t o_s1, float* lse, int32_t T, int32_t H, cudaStream_t stream) {
+  return sparse_fwd_impl(q, q_s0, q_s1, kv_records, record_stride_bytes, num_records, kv_indptr, kv_indices,
+                         n_indices, softmax_scale, has_invalid, out, o_s0, o_s1, lse, T, H, stream, true);
+}
+
+extern "C" void mla_debug_stall_next_decode(int32_t wait_us) { g_stall_next_us = wait_us > 0 ? wait_us : 0; }
 
 // ------------------------------------------------------------------------------------------
 extern "C" size_t mla_paged_decode_workspace_size(int32_t B, int32_t q_len, int32_t H,
@@ -607,6 +766,9 @@ extern "C" int mla_paged_decode(const void* q, int64_t q_s0, int64_t q_s1, const
     p.part_lse = part_lse;
     p.sched = sched;
     p.err = d->err;
+    p.wait_us = g_stall_next_us;
+    p.stall = g_stall_next_us > 0 ? 1 : 0;
+    g_stall_next_us = 0;
     if (sched && cudaMemsetAsync(sched, 0, sizeof(uint32_t), stream) != cudaSuccess)
       return fail(MLA_ERR_CUDA, "scheduler reset failed");
     const int grid = grid_for(items, d->sms);

@@ -413,6 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
     mbar_init(o_done, 1);
     mbar_init(mma_final, 1);
     *abort_flag = 0;
+    abort_flag[1] = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -517,9 +518,9 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
       __syncwarp();
       cur = nxt;
     }
-    volatile int no_abort = 0;     // never leave bulk copies in flight behind us
+    volatile int no_abort[2] = {0, 0};     // never leave bulk copies in flight behind us
     for (int s = 0; s < NST; ++s)
-      if (armed[s]) mbar_wait(&full[s], armed_par[s], &no_abort);
+      if (armed[s]) mbar_wait(&full[s], armed_par[s], no_abort);
     errbits = __reduce_or_sync(0xFFFFFFFFu, errbits);
     if (lane == 0 && errbits) set_device_error(p.err, errbits);
   } else if (warp == 1) {
@@ -583,8 +584,8 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
         }
       }
       mma_commit(mma_final);
-      volatile int no_abort = 0;
-      mbar_wait(mma_final, 0, &no_abort);
+      volatile int no_abort[2] = {0, 0};
+      mbar_wait(mma_final, 0, no_abort);
     }
     __syncwarp();
   } else if (warp >= 6) {

@@ -1,10 +1,12 @@
 // mla_ds.cuh -- MLA over the 656-byte fp8_ds_mla record: the sparse (CSR-indexed) forward and
 // the paged decode / spec-verify.
 //
-// What it computes ("FlashMLA: Multi-head Latent Attention decode kernels", sparse attention
-// over the fp8_ds_mla cache; "vLLM MLA backend", the fp8_ds_mla record): a record holds 512
-// e4m3 codes of kv_c_normed in four 128-wide tiles with one fp32 scale each, then 64 bf16 of
-// k_pe.  The key is k = [s_j * code_j (j = 0..3) | k_pe], the value its first 512 entries; the
+// What it computes ("vllm.models.kimi_k3.amd.ops.flydsl_sparse_mla", flydsl_sparse_mla_fp8ds_fwd:
+// the sparse forward over CSR key lists, masked negative indices, empty row -> 0 / -inf,
+// natural-log lse, and the 656-byte record; "vllm.models.kimi_k3.nvidia.specialized_decode.
+// cutedsl.mla.prepared", trtllm_decode: the paged decode over the same records): a record holds
+// 512 e4m3 codes of kv_c_normed in four 128-wide tiles with one fp32 scale each, then 64 bf16
+// of k_pe.  The key is k = [s_j * code_j (j = 0..3) | k_pe], the value its first 512 entries; the
 // logit of query q is softmax_scale * q . k.
 //
 // How (GB300 design, exact up to fp32 accumulation):
@@ -160,6 +162,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
       mbar_init(&item_empty[k], 3 + C::kGatherWarps);
     }
     *abort_flag = 0;
+    abort_flag[1] = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -279,8 +282,8 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         }
       }
       mma_commit(fin_pv);
-      volatile int no_abort = 0;
-      mbar_wait(fin_pv, 0, &no_abort);
+      volatile int no_abort[2] = {0, 0};
+      mbar_wait(fin_pv, 0, no_abort);
     }
     __syncwarp();
   } else if (!kSparse && warp == 0) {
@@ -379,9 +382,9 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
       }
     }
     if (lane == 0) {     // never leave copies in flight behind us
-      volatile int no_abort = 0;
+      volatile int no_abort[2] = {0, 0};
       const int64_t first = pos > R ? pos - R : 0;
-      for (int64_t q = first; q < pos; ++q) mbar_wait(&full[q % R], static_cast<uint32_t>(q / R) & 1u, &no_abort);
+      for (int64_t q = first; q < pos; ++q) mbar_wait(&full[q % R], static_cast<uint32_t>(q / R) & 1u, no_abort);
     }
     __syncwarp();
     errbits = __reduce_or_sync(0xFFFFFFFFu, errbits);
@@ -442,8 +445,8 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         g += it.ntiles;
       }
       mma_commit(fin);
-      volatile int no_abort = 0;
-      mbar_wait(fin, 0, &no_abort);
+      volatile int no_abort[2] = {0, 0};
+      mbar_wait(fin, 0, no_abort);
     }
     __syncwarp();
   } else if (warp < 6) {
@@ -859,8 +862,8 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         g += it.ntiles;
       }
       mma_commit(fin_pv);
-      volatile int no_abort = 0;
-      mbar_wait(fin_pv, 0, &no_abort);
+      volatile int no_abort[2] = {0, 0};
+      mbar_wait(fin_pv, 0, no_abort);
     }
     __syncwarp();
   } else {

@@ -32,6 +32,39 @@ struct EpiParams {
   uint32_t* err;
 };
 
+// Prefill epilogues: key concat + in-place q RoPE + latent insert (bf16 / fp8_ds_mla cache),
+// or fp8 q / k / v quant + fp8 latent insert.
+struct PrefillEpiParams {
+  uint16_t* q;             // bf16 [Tp, H, dn + 64]; rotated in place (key concat) or read (fp8)
+  int64_t q_s0, q_s1;
+  const uint16_t* k_nope;  // bf16 [Tp, H, dn]
+  int64_t kn_s0, kn_s1;
+  const uint16_t* k_pe;    // bf16 [Tp, 64]
+  int64_t kp_s0;
+  const uint16_t* kv_c;    // bf16 [Tp, 512]
+  int64_t kv_s0;
+  const uint16_t* v;       // bf16 [Tp, H, dv] (fp8 only)
+  int64_t v_s0, v_s1;
+  uint16_t* k_out;         // bf16 [Tp, H, dn + 64] contiguous (key concat)
+  uint8_t* q8;             // e4m3 [Tp, H, dn + 64], [Tp, H, dn + 64], [Tp, H, dv] contiguous (fp8)
+  uint8_t* k8;
+  uint8_t* v8;
+  uint8_t* cache;
+  int64_t num_blocks, block_stride, entry_stride;
+  int block_size;
+  const int64_t* slot_mapping;
+  const float* q_scale_inv;  // device fp32 scalars (fp8 only)
+  const float* k_scale_inv;
+  const float* v_scale_inv;
+  const float* cache_scale_inv;
+  const int64_t* positions;
+  const float* cos_sin;
+  int64_t max_position;
+  int H, dn, dv;
+  int vec;                 // every row, stride and base 16-byte aligned: 8-element vector accesses
+  uint32_t* err;
+};
+
 struct MergeParams {
   const float* part_o;     // [S][n_rows][H][512]
   const float* part_lse;   // [S][n_rows][H]
@@ -58,6 +91,8 @@ struct GatherParams {
 void set_error_message(const char* msg);
 
 cudaError_t launch_epilogue(int fmt, const EpiParams& p, int B, cudaStream_t stream);
+// fmt 0 / 2: key concat for the bf16 / fp8_ds_mla cache; fmt 1: fp8 q / k / v quant.
+cudaError_t launch_prefill_epilogue(int fmt, const PrefillEpiParams& p, int Tp, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_gather(int fmt, const GatherParams& p, cudaStream_t stream);
 

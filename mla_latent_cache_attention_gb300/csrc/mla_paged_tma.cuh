@@ -1,8 +1,10 @@
 // mla_paged_tma.cuh -- paged MLA decode / spec-verify over bf16 and plain-fp8 caches.
 //
-// What it computes ("FlashMLA: Multi-head Latent Attention decode kernels", decode with an
-// absorbed query over the 576-wide latent cache; "vLLM MLA backend", paged decode with
-// spec-verify query tokens): for every request b and query token qi, attention of the
+// What it computes ("vllm.models.kimi_k3.nvidia.specialized_decode.cutedsl.mla.prepared",
+// PreparedMla.stock_core and trtllm_decode: decode of q query tokens per request over the
+// paged latent cache, causal among them, split count bounded by max_context; bmm1_scale =
+// softmax_scale * q_scale * k_scale and bmm2_scale = k_scale for the plain fp8 cache): for
+// every request b and query token qi, attention of the
 // absorbed query q[b, qi, h, 0:576] over the keys at positions 0 .. L_b - q_len + qi of the
 // paged cache (each key is the 576-wide latent [kv_c_normed | k_pe], the value its first 512),
 // softmax scale applied to the logits, output O / l in bf16 and the natural-log LSE.
@@ -81,6 +83,8 @@ struct PagedParams {
   float* part_lse;              // [n_splits][n_rows][H]
   uint32_t* sched;              // item counter, zero at launch; null: static striding
   uint32_t* err;
+  int wait_us;                  // in-kernel wait limit (0: the default, about 1 s)
+  int stall;                    // test aid: the producer issues no loads (every wait runs out)
 };
 
 struct WorkItem {
@@ -90,14 +94,11 @@ struct WorkItem {
 constexpr int kItemDepth = 4;
 constexpr int kSlotBytes = kTile * 128;
 
-template <int F, int NQ, int KM>
+template <int F, int NQ>
 struct PagedCfg {
   static_assert(F == kBF16 || F == kFP8, "format");
   static_assert(NQ == 16 || NQ == 32 || NQ == 64, "columns per item");
-  static_assert(KM == 64 || KM == 128, "keys per tile");
-  // 64-key fp8 tiles failed the full-size spec-verify parity (long rows), so they stay out
-  static_assert(F != kFP8 || KM == 128, "fp8 pages use 128-key tiles");
-  static constexpr int kM = KM;                           // keys per tile (QK MMA M)
+  static constexpr int KM = kTile;                        // keys per tile (QK MMA M)
   static constexpr int kSlot = KM * 128;                  // one ring slot: KM rows of 128 B
   static constexpr int kNB = F == kBF16 ? 10 : 5;        // ring positions per tile (bf16: 9 blocks + 1 pad)
   static constexpr int kNBQ = F == kBF16 ? 9 : 5;        // query blocks
@@ -107,7 +108,7 @@ struct PagedCfg {
   static constexpr bool kPvSplit = MLA_PV_WARP;
   static constexpr int kPvWarp = kPvSplit ? 2 + kSW : -1;   // after the softmax warps
   static constexpr int kThreads = 64 + 32 * kSW + (kPvSplit ? 32 : 0);
-  static constexpr bool kOverlap = (F == kFP8 || KM == 64) && MLA_OVERLAP_FP8;
+  static constexpr bool kOverlap = F == kFP8 && MLA_OVERLAP_FP8;
   static constexpr int kPfDist = MLA_LOOKAHEAD;           // tiles between a page lookup and its use
   static constexpr bool kL2Pf = MLA_L2PF;
   // per-slot release commits pay for bf16 (a 147 KB tile fits 1.2 times: its slots refill as
@@ -244,12 +245,12 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t v) {
   return __half22float2(*reinterpret_cast<const __half2*>(&h));
 }
 
-template <int F, int NQ, int KM>
-__global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
+template <int F, int NQ>
+__global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
     mla_paged_tma_kernel(const __grid_constant__ PagedParams p, const __grid_constant__ CUtensorMap tm_kv,
                          const __grid_constant__ CUtensorMap tm_q) {
-  using C = PagedCfg<F, NQ, KM>;
-  constexpr int R = C::kR, NB = C::kNB, NC = C::kNC;
+  using C = PagedCfg<F, NQ>;
+  constexpr int R = C::kR, NB = C::kNB, NC = C::kNC, KM = C::KM;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem + C::kRing;
@@ -305,6 +306,7 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
       mbar_init(&item_empty[k], C::kPvSplit ? 3 : 2);
     }
     *abort_flag = 0;
+    abort_flag[1] = p.wait_us;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -382,6 +384,18 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
     WorkItem cur = next_item(take_ticket());
     WorkItem nxt{};
     bool have_nxt = false;
+    if (p.stall) {
+      // test aid: hand the first item to the consumers and issue none of its loads, so that
+      // their waits run out under the launch's short wait limit; no copy is ever in flight
+      if (cur.b >= 0) {
+        if (lane == 0) {
+          items[0] = cur;
+          mbar_arrive(&item_full[0]);
+        }
+        nitem = 1;
+      }
+      ok = false;
+    }
     while (ok && cur.b >= 0) {
       {
         const int k = nitem % kItemDepth;
@@ -512,13 +526,13 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
     }
     // never leave copies in flight behind us
     if (lane == 0) {
-      volatile int no_abort = 0;
+      volatile int no_abort[2] = {0, 0};
       const int64_t first = pos > R ? pos - R : 0;
       for (int64_t q = first; q < pos; ++q) {
         const int slot = static_cast<int>(q % R);
-        mbar_wait(&full[slot], static_cast<uint32_t>(q / R) & 1u, &no_abort);
+        mbar_wait(&full[slot], static_cast<uint32_t>(q / R) & 1u, no_abort);
       }
-      if (nq > 0) mbar_wait(q_full, (nq - 1) & 1, &no_abort);
+      if (nq > 0) mbar_wait(q_full, (nq - 1) & 1, no_abort);
     }
     __syncwarp();
     errbits = __reduce_or_sync(0xFFFFFFFFu, errbits);
@@ -657,8 +671,8 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
         g += it.ntiles;
       }
       mma_commit(fin);
-      volatile int no_abort = 0;
-      mbar_wait(fin, 0, &no_abort);
+      volatile int no_abort[2] = {0, 0};
+      mbar_wait(fin, 0, no_abort);
     }
     __syncwarp();
   } else if (warp == C::kPvWarp) {
@@ -716,8 +730,8 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
         g += it.ntiles;
       }
       mma_commit(fin_pv);
-      volatile int no_abort = 0;
-      mbar_wait(fin_pv, 0, &no_abort);
+      volatile int no_abort[2] = {0, 0};
+      mbar_wait(fin_pv, 0, no_abort);
     }
     __syncwarp();
   } else {
@@ -731,10 +745,7 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
     const int quad = warp & 3;                  // TMEM lane quadrant of this warp
     const int c0 = (sw >> 2) * NC;              // first column of this thread
     const int row = quad * 32 + lane;           // TMEM lane: output column d of O^T
-    // key row of the tile: with 64-key tiles (M = 64) the S accumulator holds key 16 q + i in
-    // lane 32 q + i of quadrant q, and lanes 16..31 of each quadrant carry nothing
-    const bool klane = (KM == 128) || (lane < 16);
-    const int krow = (KM == 128) ? row : quad * 16 + lane;
+    const int krow = row;                       // key row of the tile (S^T lane)
     const int stid = tid - 64;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     float* red_m = red;                         // [2][NQ][4]
@@ -768,7 +779,7 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
         tmem_ld_n<NC>(tl + C::kTmemS + (gt & 1) * NQ + c0, s);
         tmem_ld_wait();
         const int kpos = it.k0 + t * KM + krow;
-        const bool rv = klane && kpos < it.k0 + it.n;
+        const bool rv = kpos < it.k0 + it.n;
 #pragma unroll
         for (int c = 0; c < NC; ++c) s[c] = rv ? s[c] * p.sig2 : -CUDART_INF_F;
         // spec-verify: query token qi sees keys up to L - q_len + qi
@@ -786,9 +797,9 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
         if (stid == 0) TL(3, 1);
         float s[NC];
         load_s(s, gt, t);
-        const bool rv = klane && it.k0 + t * KM + krow < it.k0 + it.n;
+        const bool rv = it.k0 + t * KM + krow < it.k0 + it.n;
         // rows past the item never reach PV with stale contents
-        if (!rv && klane && c0 == 0) {
+        if (!rv && c0 == 0) {
 #pragma unroll 1
           for (int b = 0; b < (F == kBF16 ? 8 : 4); ++b) {
             uint4* dst = reinterpret_cast<uint4*>(
@@ -885,7 +896,7 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
             v.y = pack2(s[c + 2], s[c + 3], true);
             v.z = pack2(s[c + 4], s[c + 5], true);
             v.w = pack2(s[c + 6], s[c + 7], true);
-            if (klane) *reinterpret_cast<uint4*>(ps + (krow >> 3) * (NQ * 16) + (krow & 7) * 16 + ((c0 + c) >> 3) * 128) = v;
+            *reinterpret_cast<uint4*>(ps + (krow >> 3) * (NQ * 16) + (krow & 7) * 16 + ((c0 + c) >> 3) * 128) = v;
           }
         } else {
           // 8 keys x 16 columns core matrices, 8-key groups NQ*8 bytes apart; hi then lo
@@ -902,10 +913,8 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ, KM>::kThreads, 1)
               lw[u] = l01 | (l23 << 16);
             }
             const int off = (krow >> 3) * (NQ * 8) + (krow & 7) * 16 + ((c0 + c) >> 4) * 128;
-            if (klane) {
-              *reinterpret_cast<uint4*>(ps + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-              *reinterpret_cast<uint4*>(ps + KM * NQ + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-            }
+            *reinterpret_cast<uint4*>(ps + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            *reinterpret_cast<uint4*>(ps + KM * NQ + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
         }
         fence_proxy_async_smem();

@@ -7,18 +7,18 @@ namespace {
 
 template <int NQ>
 cudaError_t launch_nq(const PagedParams& p, const void* tkv, const void* tq, int grid, cudaStream_t stream) {
-  using C = PagedCfg<kBF16, NQ, 128>;
+  using C = PagedCfg<kBF16, NQ>;
   static bool configured[64] = {};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(mla_paged_tma_kernel<kBF16, NQ, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
+    e = cudaFuncSetAttribute(mla_paged_tma_kernel<kBF16, NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  mla_paged_tma_kernel<kBF16, NQ, 128><<<grid, C::kThreads, C::kAlloc, stream>>>(
+  mla_paged_tma_kernel<kBF16, NQ><<<grid, C::kThreads, C::kAlloc, stream>>>(
       p, *static_cast<const CUtensorMap*>(tkv), *static_cast<const CUtensorMap*>(tq));
   return cudaGetLastError();
 }

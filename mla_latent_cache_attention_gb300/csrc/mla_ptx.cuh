@@ -1,9 +1,10 @@
 // mla_ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarriers, bulk async copies,
 // tcgen05 (TMEM allocation, MMA, commit, TMEM loads/stores) and shared-memory descriptors.
 //
-// Every wait here is bounded: after ~kWaitNs of polling the waiter sets the CTA's abort flag
-// to 2 (timeout) and returns false, so a pipeline fault ends the kernel instead of hanging
-// the GPU; the kernel reports the timeout in the caller's device error word.
+// Every wait here is bounded: after ~kWaitNs of polling (or the launch's own limit, see
+// wait_limit_ns) the waiter sets the CTA's abort flag to 2 (timeout) and returns false, so a
+// pipeline fault ends the kernel instead of hanging the GPU; the kernel reports the timeout
+// in the caller's device error word.
 #pragma once
 #include <cstdint>
 
@@ -77,6 +78,14 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The CTA's abort word is two ints in shared memory: [0] the abort flag (0 running, 1 a role
+// failed, 2 a wait ran out), [1] the launch's wait limit in microseconds (0: kWaitNs).  A
+// kernel writes both before its first barrier.
+__device__ __forceinline__ uint64_t wait_limit_ns(volatile int* abort_flag) {
+  const int us = abort_flag[1];
+  return us > 0 ? static_cast<uint64_t>(us) * 1000ull : kWaitNs;
+}
+
 // Bounded wait for the phase with the given parity.  `abort_flag` (shared) is polled so that
 // one role's failure releases the others.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
@@ -87,7 +96,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try_wait_ns(bar, parity, 2000)) return true;
     if ((it & 7u) == 0) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitNs) {
+      if (globaltimer() - t0 > wait_limit_ns(abort_flag)) {
         *abort_flag = 2;
         return false;
       }

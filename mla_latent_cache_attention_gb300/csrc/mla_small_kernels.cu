@@ -49,6 +49,55 @@ __device__ __forceinline__ int ds_tile_exponent(float amax) {
   return k < -126 ? -126 : k;
 }
 
+// Write one cache entry (128 threads): [kv_c | rope(k_pe)] as bf16 (F = 0), as
+// e4m3_sat(x * cinv) (F = 1), or as a 656-byte fp8_ds_mla record (F = 2: per-128-tile scale
+// 2^k from ds_tile_exponent, codes e4m3(x / 2^k), rope bf16).  cs: the RoPE row or null.
+template <int F>
+__device__ __forceinline__ void insert_latent(uint8_t* ent, const uint16_t* __restrict__ kc,
+                                              const uint16_t* __restrict__ kr, const float* __restrict__ cs, float cinv,
+                                              int tid) {
+  if (tid < 32) {   // rope part, one pair per lane
+    float y0 = bf16_at(kr + 2 * tid), y1 = bf16_at(kr + 2 * tid + 1);
+    if (cs) rope_pair(y0, y1, cs[tid], cs[32 + tid], y0, y1);
+    if (F == 0) {
+      reinterpret_cast<uint16_t*>(ent)[512 + 2 * tid] = bf16_bits(y0);
+      reinterpret_cast<uint16_t*>(ent)[512 + 2 * tid + 1] = bf16_bits(y1);
+    } else if (F == 1) {
+      ent[512 + 2 * tid] = e4m3_sat(y0 * cinv);
+      ent[512 + 2 * tid + 1] = e4m3_sat(y1 * cinv);
+    } else {
+      reinterpret_cast<uint16_t*>(ent + 528)[2 * tid] = bf16_bits(y0);
+      reinterpret_cast<uint16_t*>(ent + 528)[2 * tid + 1] = bf16_bits(y1);
+    }
+  }
+  // NoPE part: warp w owns the 128-wide tile w, 4 values per lane
+  const int w = tid >> 5, lane = tid & 31;
+  float x[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) x[i] = bf16_at(kc + 128 * w + 4 * lane + i);
+  if (F == 0) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) reinterpret_cast<uint16_t*>(ent)[128 * w + 4 * lane + i] = kc[128 * w + 4 * lane + i];
+  } else if (F == 1) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ent[128 * w + 4 * lane + i] = e4m3_sat(x[i] * cinv);
+  } else {
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(x[i]));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    const int k = ds_tile_exponent(amax);
+    const float inv = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);   // 2^-k, exact
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ent[128 * w + 4 * lane + i] = e4m3_sat(x[i] * inv);
+    if (lane == 0) {
+      const float s = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+      *reinterpret_cast<float*>(ent + 512 + 4 * w) = s;
+    }
+  }
+}
+
 // Grid (B, ceil(H / 4)): CTA (b, g) builds the query rows of heads 4g..4g+3 of token b; the
 // CTAs with g == 0 also insert token b's latent.  Loads go through restrict-qualified
 // pointers in batches of 8 so that they are all in flight before the stores.
@@ -127,49 +176,151 @@ __global__ void __launch_bounds__(128) mla_epilogue_kernel(const EpiParams p) {
     if (tid == 0) set_device_error(p.err, 4u);
     return;
   }
-  uint8_t* ent = p.cache + blk * p.block_stride + (slot % p.block_size) * p.entry_stride;
-  const uint16_t* __restrict__ kc = p.kv_c + b * p.kv_s0;
-  const uint16_t* __restrict__ kr = p.k_pe + b * p.kp_s0;
-  if (tid < 32) {   // rope part, one pair per lane
+  insert_latent<F>(p.cache + blk * p.block_stride + (slot % p.block_size) * p.entry_stride, p.kv_c + b * p.kv_s0,
+                   p.k_pe + b * p.kp_s0, cs, cinv, tid);
+}
+
+// ------------------------------------------------------------------------------------------
+// Prefill epilogues.  "vllm.models.kimi_k3.nvidia.ops.fused_mla_key_concat_kv_cache":
+//   F = 0 / 2  fused_mla_key_concat_kv_cache_insert / fused_mla_key_concat_ds_mla_insert:
+//              k_out[t, h] = [k_nope[t, h] | rope(k_pe[t])] (bf16), the last 64 values of
+//              q[t, h] rotated in place, the latent inserted into the bf16 / fp8_ds_mla cache;
+//   F = 1      fused_mla_qkv_quant_kv_cache_fp8_insert: q / k / v quantised to E4M3 with their
+//              own scales (q rotated on the way, not in place), the latent into the plain fp8
+//              cache with the cache scale.
+// Grid (Tp, ceil(H / 4)), 128 threads: CTA (t, g) handles heads 4g..4g+3 of token t and, for
+// g == 0, the latent insert of token t.  rope(k_pe[t]) is formed once per CTA in shared memory.
+
+// 8 consecutive bf16 values as fp32 (one 16-byte load when vec, else scalar loads)
+__device__ __forceinline__ void load8(const uint16_t* __restrict__ src, bool vec, float (&x)[8]) {
+  if (vec) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(src));
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      x[2 * e] = __uint_as_float(ww[e] << 16);
+      x[2 * e + 1] = __uint_as_float(ww[e] & 0xFFFF0000u);
+    }
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = bf16_at(src + e);
+  }
+}
+
+// 8 values quantised with inv to E4M3 (one 8-byte store when vec)
+__device__ __forceinline__ void store8_e4m3(uint8_t* dst, bool vec, const float (&x)[8], float inv) {
+  uint8_t c[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) c[e] = e4m3_sat(x[e] * inv);
+  if (vec) {
+    uint2 w;
+    w.x = c[0] | (c[1] << 8) | (c[2] << 16) | (static_cast<uint32_t>(c[3]) << 24);
+    w.y = c[4] | (c[5] << 8) | (c[6] << 16) | (static_cast<uint32_t>(c[7]) << 24);
+    *reinterpret_cast<uint2*>(dst) = w;
+  } else {
+#pragma unroll
+    for (int e = 0; e < 8; ++e) dst[e] = c[e];
+  }
+}
+
+template <int F>
+__global__ void __launch_bounds__(128) mla_prefill_epilogue_kernel(const PrefillEpiParams p) {
+  const int t = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
+  __shared__ float kpr[64];        // rope(k_pe[t]) in fp32
+  const float* __restrict__ cs = nullptr;
+  if (p.positions) {
+    int64_t pos = p.positions[t];
+    if (pos < 0 || pos >= p.max_position) {
+      if (tid == 0 && g == 0) set_device_error(p.err, 8u);
+      pos = pos < 0 ? 0 : p.max_position - 1;
+    }
+    cs = p.cos_sin + pos * 64;
+  }
+  const uint16_t* __restrict__ kr = p.k_pe + t * p.kp_s0;
+  if (tid < 32) {
     float y0 = bf16_at(kr + 2 * tid), y1 = bf16_at(kr + 2 * tid + 1);
     if (cs) rope_pair(y0, y1, cs[tid], cs[32 + tid], y0, y1);
-    if (F == 0) {
-      reinterpret_cast<uint16_t*>(ent)[512 + 2 * tid] = bf16_bits(y0);
-      reinterpret_cast<uint16_t*>(ent)[512 + 2 * tid + 1] = bf16_bits(y1);
-    } else if (F == 1) {
-      ent[512 + 2 * tid] = e4m3_sat(y0 * cinv);
-      ent[512 + 2 * tid + 1] = e4m3_sat(y1 * cinv);
+    kpr[2 * tid] = y0;
+    kpr[2 * tid + 1] = y1;
+  }
+  __syncthreads();
+  const float qinv = (F == 1) ? *p.q_scale_inv : 1.f;
+  const float kinv = (F == 1) ? *p.k_scale_inv : 1.f;
+  const float vinv = (F == 1) ? *p.v_scale_inv : 1.f;
+  const int H = p.H, dn = p.dn, de = p.dn + 64;
+  const bool vec = p.vec != 0;
+  const int h_lo = 4 * g, h_hi = min(H, 4 * g + 4), nh = h_hi - h_lo;
+  // ---- NoPE parts: 8 values per item (k_nope -> k_out / k8, and for fp8 q_nope -> q8, v -> v8)
+  const int cn = dn >> 3;
+  for (int i = tid; i < nh * cn; i += blockDim.x) {
+    const int h = h_lo + i / cn, d0 = (i % cn) * 8;
+    const int64_t o = (static_cast<int64_t>(t) * H + h) * de + d0;
+    const uint16_t* kn = p.k_nope + t * p.kn_s0 + h * p.kn_s1 + d0;
+    if (F == 1) {
+      float x[8];
+      load8(kn, vec, x);
+      store8_e4m3(p.k8 + o, vec, x, kinv);
+      load8(p.q + t * p.q_s0 + h * p.q_s1 + d0, vec, x);
+      store8_e4m3(p.q8 + o, vec, x, qinv);
+    } else if (vec) {
+      *reinterpret_cast<uint4*>(p.k_out + o) = __ldg(reinterpret_cast<const uint4*>(kn));
     } else {
-      reinterpret_cast<uint16_t*>(ent + 528)[2 * tid] = bf16_bits(y0);
-      reinterpret_cast<uint16_t*>(ent + 528)[2 * tid + 1] = bf16_bits(y1);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) p.k_out[o + e] = kn[e];
     }
   }
-  // NoPE part: warp w owns the 128-wide tile w, 4 values per lane
-  const int w = tid >> 5, lane = tid & 31;
-  float x[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) x[i] = bf16_at(kc + 128 * w + 4 * lane + i);
-  if (F == 0) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) reinterpret_cast<uint16_t*>(ent)[128 * w + 4 * lane + i] = kc[128 * w + 4 * lane + i];
-  } else if (F == 1) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) ent[128 * w + 4 * lane + i] = e4m3_sat(x[i] * cinv);
-  } else {
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(x[i]));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-    const int k = ds_tile_exponent(amax);
-    const float inv = __uint_as_float(static_cast<uint32_t>(127 - k) << 23);   // 2^-k, exact
-#pragma unroll
-    for (int i = 0; i < 4; ++i) ent[128 * w + 4 * lane + i] = e4m3_sat(x[i] * inv);
-    if (lane == 0) {
-      const float s = __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
-      *reinterpret_cast<float*>(ent + 512 + 4 * w) = s;
+  if (F == 1) {
+    const int cv = p.dv >> 3;
+    for (int i = tid; i < nh * cv; i += blockDim.x) {
+      const int h = h_lo + i / cv, d0 = (i % cv) * 8;
+      float x[8];
+      load8(p.v + t * p.v_s0 + h * p.v_s1 + d0, vec, x);
+      store8_e4m3(p.v8 + (static_cast<int64_t>(t) * H + h) * p.dv + d0, vec, x, vinv);
     }
   }
+  // ---- rope parts: one pair per item (q rotated, k_out / k8 from the shared rotation)
+  for (int i = tid; i < nh * 32; i += blockDim.x) {
+    const int h = h_lo + (i >> 5), pr = i & 31;
+    const int64_t o = (static_cast<int64_t>(t) * H + h) * de + dn + 2 * pr;
+    uint16_t* qp = p.q + t * p.q_s0 + h * p.q_s1 + dn + 2 * pr;
+    float y0 = bf16_at(qp), y1 = bf16_at(qp + 1);
+    if (cs) rope_pair(y0, y1, cs[pr], cs[32 + pr], y0, y1);
+    if (F == 1) {
+      p.q8[o] = e4m3_sat(y0 * qinv);
+      p.q8[o + 1] = e4m3_sat(y1 * qinv);
+      p.k8[o] = e4m3_sat(kpr[2 * pr] * kinv);
+      p.k8[o + 1] = e4m3_sat(kpr[2 * pr + 1] * kinv);
+    } else {
+      if (cs) {
+        qp[0] = bf16_bits(y0);
+        qp[1] = bf16_bits(y1);
+      }
+      p.k_out[o] = bf16_bits(kpr[2 * pr]);
+      p.k_out[o + 1] = bf16_bits(kpr[2 * pr + 1]);
+    }
+  }
+  if (g != 0) return;
+  // ---- latent insert
+  const int64_t slot = p.slot_mapping[t];
+  if (slot < 0) return;
+  const int64_t blk = slot / p.block_size;
+  if (blk >= p.num_blocks) {
+    if (tid == 0) set_device_error(p.err, 4u);
+    return;
+  }
+  insert_latent<F>(p.cache + blk * p.block_stride + (slot % p.block_size) * p.entry_stride, p.kv_c + t * p.kv_s0, kr,
+                   cs, (F == 1) ? *p.cache_scale_inv : 1.f, tid);
+}
+
+cudaError_t launch_prefill_epilogue(int fmt, const PrefillEpiParams& p, int Tp, cudaStream_t stream) {
+  const dim3 grid(Tp, (p.H + 3) / 4);
+  if (fmt == 0)
+    mla_prefill_epilogue_kernel<0><<<grid, 128, 0, stream>>>(p);
+  else if (fmt == 1)
+    mla_prefill_epilogue_kernel<1><<<grid, 128, 0, stream>>>(p);
+  else
+    mla_prefill_epilogue_kernel<2><<<grid, 128, 0, stream>>>(p);
+  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------------------------------

@@ -1,7 +1,11 @@
 """GPU parity of the sparse forward (CSR over fp8_ds_mla records) against the fp64 oracle:
 the tiny configuration in full, edge cases (empty / all-masked / ragged rows, duplicates,
-head counts that are not multiples of 16, strided out, no lse), and the full-size prefill
-configuration on sampled rows."""
+head counts that are not multiples of 16, strided out, no lse, int64 indices), and the
+full-size prefill configuration (T=4096, H=16, top-2048 of 65536 records) on all 4096 rows.
+
+Every case runs both kernel designs of the library: mla_sparse_fwd (gather warps, codes
+straight into the tensor cores) and the test aid mla_sparse_fwd_staged (bulk copies and an
+exact e4m3 -> f16 conversion in shared memory)."""
 import json
 import os
 
@@ -11,7 +15,7 @@ import torch
 
 import oracle
 from mla_latent_cache_attention_gb300 import synth
-from tests.gpu_helpers import assert_attn_close, assert_lse_close, t_bf16, t_i32, t_u8
+from tests.gpu_helpers import assert_attn_close, assert_lse_close, t_bf16, t_i32, t_i64, t_u8
 
 pytestmark = pytest.mark.gpu
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -24,44 +28,64 @@ def m():
     return mod
 
 
-def run(m, c: synth.SparseCase, rows=None, out=None, lse=True):
+@pytest.fixture(params=["gather", "staged"])
+def kern(request):
+    return request.param
+
+
+_ORACLE_CACHE = {}
+
+
+def oracle_sparse(c: synth.SparseCase, rows=None, key=None):
+    """The oracle's result for a case (memoised by `key` for the full-size case, which both
+    kernel designs compare against)."""
+    if key is not None and key in _ORACLE_CACHE:
+        return _ORACLE_CACHE[key]
+    r = oracle.sparse_fwd(c.q, c.records, c.indptr, c.indices, c.softmax_scale, c.has_invalid, rows=rows)
+    if key is not None:
+        _ORACLE_CACHE[key] = r
+    return r
+
+
+def run(m, c: synth.SparseCase, rows=None, out=None, lse=True, kern="gather", key=None):
     q = t_bf16(c.q)
     o, l = m.sparse_fwd(q, t_u8(c.records), t_i32(c.indptr), t_i32(c.indices), c.softmax_scale,
-                        has_invalid=c.has_invalid, out=out, return_lse=lse)
-    ro, rl = oracle.sparse_fwd(c.q, c.records, c.indptr, c.indices, c.softmax_scale, c.has_invalid, rows=rows)
+                        has_invalid=c.has_invalid, out=out, return_lse=lse, kernel=kern)
+    ro, rl = oracle_sparse(c, rows=rows, key=key)
     if rows is not None:
         o = o[torch.as_tensor(rows, device=o.device)]
         l = l[torch.as_tensor(rows, device=o.device)] if l is not None else None
     return o, l, ro, rl
 
 
-def test_config0_tiny(m):
+def test_config0_tiny(m, kern):
     c = synth.config0()
-    o, l, ro, rl = run(m, c)
+    o, l, ro, rl = run(m, c, kern=kern)
     assert_attn_close(o, ro, "config0 out")
     assert_lse_close(l, rl, "config0 lse")
     assert torch.all(o[3] == 0) and torch.all(l[3] == -np.inf)
     assert m.read_device_errors() == 0
 
 
-def test_golden_warmup_problem(m):
+def test_golden_warmup_problem(m, kern):
     g = json.load(open(os.path.join(GOLDEN, "warmup_one_token.json")))
     rec = torch.zeros((1, 656), dtype=torch.uint8, device="cuda")
     for H in g["heads"]:
         q = torch.zeros((1, H, 576), dtype=torch.bfloat16, device="cuda")
-        o, l = m.sparse_fwd(q, rec, t_i32(g["indptr"]), t_i32(g["indices"]), g["softmax_scale"], return_lse=True)
+        o, l = m.sparse_fwd(q, rec, t_i32(g["indptr"]), t_i32(g["indices"]), g["softmax_scale"], return_lse=True,
+                            kernel=kern)
         assert torch.all(o == g["expected_out"]) and torch.all(l == g["expected_lse"])
 
 
 @pytest.mark.parametrize("H", [1, 5, 16, 20, 64, 96, 128])
-def test_head_counts(m, H):
+def test_head_counts(m, kern, H):
     c = synth.sparse_case(100 + H, T=6, H=H, N=500, per_row=200, p_invalid=0.1, replace=True, ragged=True)
-    o, l, ro, rl = run(m, c)
+    o, l, ro, rl = run(m, c, kern=kern)
     assert_attn_close(o, ro, f"H={H}")
     assert_lse_close(l, rl, f"H={H}")
 
 
-def test_multi_tile_ragged_rows(m):
+def test_multi_tile_ragged_rows(m, kern):
     # row lengths 0, 1, 127, 128, 129, 255, 256, 257, 1000, all-masked
     lens = [0, 1, 127, 128, 129, 255, 256, 257, 1000, 40]
     rng = np.random.default_rng(5)
@@ -72,60 +96,61 @@ def test_multi_tile_ragged_rows(m):
     idx[ptr[-2]:ptr[-1]] = -1                    # last row fully masked
     c.q = synth.normal_bf16_bits(rng, (len(lens), 16, 576))
     c.indptr, c.indices, c.has_invalid = ptr, idx, True
-    o, l, ro, rl = run(m, c)
+    o, l, ro, rl = run(m, c, kern=kern)
     assert_attn_close(o, ro, "ragged")
     assert_lse_close(l, rl, "ragged")
     assert torch.all(o[0] == 0) and torch.all(o[-1] == 0)
 
 
-def test_duplicates_without_has_invalid_and_no_lse(m):
+def test_duplicates_without_has_invalid_and_no_lse(m, kern):
     c = synth.sparse_case(9, T=8, H=16, N=50, per_row=300, p_invalid=0.0, replace=True)
-    o, l, ro, rl = run(m, c, lse=False)
+    o, l, ro, rl = run(m, c, lse=False, kern=kern)
     assert l is None
     assert_attn_close(o, ro, "duplicates")
 
 
-def test_strided_out_and_q(m):
+def test_strided_out_and_q(m, kern):
     c = synth.sparse_case(13, T=5, H=16, N=400, per_row=150, p_invalid=0.05, replace=False)
     qbig = torch.zeros((5, 16, 640), dtype=torch.bfloat16, device="cuda")
     qbig[:, :, :576] = t_bf16(c.q)
     out = torch.full((5, 16, 600), 7.0, dtype=torch.bfloat16, device="cuda")
     o, l = m.sparse_fwd(qbig[:, :, :576], t_u8(c.records), t_i32(c.indptr), t_i32(c.indices), c.softmax_scale,
-                        has_invalid=True, out=out[:, :, :512], return_lse=True)
+                        has_invalid=True, out=out[:, :, :512], return_lse=True, kernel=kern)
     ro, rl = oracle.sparse_fwd(c.q, c.records, c.indptr, c.indices, c.softmax_scale, True)
     assert_attn_close(out[:, :, :512], ro, "strided")
     assert torch.all(out[:, :, 512:] == 7.0)
     assert_lse_close(l, rl, "strided")
 
 
-def test_padded_record_pitch(m):
+def test_padded_record_pitch(m, kern):
     c = synth.sparse_case(17, T=4, H=16, N=300, per_row=200, p_invalid=0.1, replace=True)
     padded = np.zeros((300, 672), dtype=np.uint8)
     padded[:, :656] = c.records
     o, l = m.sparse_fwd(t_bf16(c.q), t_u8(padded), t_i32(c.indptr), t_i32(c.indices), c.softmax_scale,
-                        has_invalid=True, return_lse=True)
+                        has_invalid=True, return_lse=True, kernel=kern)
     ro, rl = oracle.sparse_fwd(c.q, padded, c.indptr, c.indices, c.softmax_scale, True)
     assert_attn_close(o, ro, "padded pitch")
     assert_lse_close(l, rl, "padded pitch")
 
 
-def test_power_of_two_and_large_scales(m):
+def test_power_of_two_and_large_scales(m, kern):
     rng = np.random.default_rng(21)
     c = synth.sparse_case(21, T=4, H=16, N=256, per_row=256, p_invalid=0.0, replace=False)
     c.records[:, 512:528] = (2.0 ** rng.integers(-6, 8, size=(256, 4))).astype(np.float32).view(np.uint8)
-    o, l, ro, rl = run(m, c)
+    o, l, ro, rl = run(m, c, kern=kern)
     assert_attn_close(o, ro, "pow2 scales")
     # scales up to 2^7 put |lse| near 3e4, where fp32 resolution is 2e-3: allow 1e-6 relative
     assert_lse_close(l, rl, "pow2 scales", rel=1e-6)
 
 
-def test_out_of_range_index_is_masked_and_flagged(m):
+def test_out_of_range_index_is_masked_and_flagged(m, kern):
     c = synth.sparse_case(23, T=3, H=16, N=100, per_row=50, p_invalid=0.0, replace=True)
     m.read_device_errors()
     bad = c.indices.copy()
     bad[7] = 100
     q = t_bf16(c.q)
-    o, l = m.sparse_fwd(q, t_u8(c.records), t_i32(c.indptr), t_i32(bad), c.softmax_scale, return_lse=True)
+    o, l = m.sparse_fwd(q, t_u8(c.records), t_i32(c.indptr), t_i32(bad), c.softmax_scale, return_lse=True,
+                        kernel=kern)
     assert m.read_device_errors() & 1
     masked = bad.copy()
     masked[7] = -1
@@ -133,25 +158,45 @@ def test_out_of_range_index_is_masked_and_flagged(m):
     assert_attn_close(o, ro, "masked bad index")
 
 
+def test_int64_indices_match_int32(m, kern):
+    # the sparse forward's interface takes int32 or int64 kv_indptr / kv_indices; int64 ids
+    # beyond int32 keep their meaning (negative: masked, too large: out of range)
+    c = synth.sparse_case(29, T=5, H=16, N=300, per_row=140, p_invalid=0.1, replace=True, ragged=True)
+    q, rec = t_bf16(c.q), t_u8(c.records)
+    o32, l32 = m.sparse_fwd(q, rec, t_i32(c.indptr), t_i32(c.indices), c.softmax_scale, has_invalid=True,
+                            return_lse=True, kernel=kern)
+    i64 = c.indices.astype(np.int64)
+    i64[i64 < 0] = -(1 << 40)
+    o64, l64 = m.sparse_fwd(q, rec, t_i64(c.indptr), t_i64(i64), c.softmax_scale, has_invalid=True,
+                            return_lse=True, kernel=kern)
+    assert torch.equal(o32, o64) and torch.equal(l32, l64)
+    assert m.read_device_errors() == 0
+    big = c.indices.astype(np.int64)
+    big[3] = (1 << 33) + 5                     # wraps to 5 if narrowed without a clamp
+    o, l = m.sparse_fwd(q, rec, t_i64(c.indptr), t_i64(big), c.softmax_scale, has_invalid=True,
+                        return_lse=True, kernel=kern)
+    assert m.read_device_errors() & 1
+    masked = c.indices.copy()
+    masked[3] = -1
+    ro, rl = oracle.sparse_fwd(c.q, c.records, c.indptr, masked, c.softmax_scale, True)
+    assert_attn_close(o, ro, "int64 out-of-range id")
+    assert_lse_close(l, rl, "int64 out-of-range id")
+
+
+def test_strided_indices_are_rejected(m):
+    c = synth.sparse_case(31, T=2, H=16, N=100, per_row=20, p_invalid=0.0, replace=True)
+    idx = t_i32(np.repeat(c.indices, 2))[::2]
+    assert not idx.is_contiguous()
+    with pytest.raises(ValueError, match="contiguous"):
+        m.sparse_fwd(t_bf16(c.q), t_u8(c.records), t_i32(c.indptr), idx, c.softmax_scale)
+
+
 @pytest.mark.slow
-def test_config2_full_size_sampled_rows(m):
+def test_config2_full_size_all_rows(m, kern):
+    """Sparse prefill at full size (T=4096, H=16, 2048 indices per row over 65536 records,
+    ~5 % masked): all 4096 rows x 16 heads compared with the oracle."""
     c = synth.config2()
-    rng = np.random.default_rng(0)
-    rows = np.unique(np.concatenate([[0, 1, c.q.shape[0] - 1], rng.choice(c.q.shape[0], 61, replace=False)]))
-    o, l, ro, rl = run(m, c, rows=rows)
+    o, l, ro, rl = run(m, c, kern=kern, key="config2")
     assert_attn_close(o, ro, "config2")
     assert_lse_close(l, rl, "config2")
     assert m.read_device_errors() == 0
-
-
-def test_staged_converter_variant():
-    # the staged-converter kernel (selected per process by MLA_SPARSE_GATHER=0) against the
-    # same cases, full-size prefill included, in a child process
-    import subprocess
-    import sys
-    env = dict(os.environ, MLA_SPARSE_GATHER="0")
-    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-    r = subprocess.run([sys.executable, "-m", "pytest", os.path.abspath(__file__), "-m", "gpu", "-q", "-x",
-                        "-p", "no:cacheprovider", "-k", "not staged_converter_variant"],
-                       cwd=root, env=env, capture_output=True, text=True, timeout=900)
-    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
