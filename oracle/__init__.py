@@ -82,6 +82,11 @@ def lib():
                                                          i64, vp, vp, vp, vp, i64, i64, i64, i32, vp, flt, flt,
                                                          flt, flt, vp, vp, i64, i32, i32, i32, i32]
             L.orc_qkv_quant_cache_fp8_insert.restype = i32
+            L.orc_gather_context.argtypes = [i32, vp, i64, i64, i64, i32, vp, i64, vp, vp, i32, i64, i32, flt, vp,
+                                             i64]
+            L.orc_gather_context.restype = i32
+            L.orc_merge_attn_states.argtypes = [vp, i64, i64, vp, vp, i64, i64, vp, i32, i32, i32, vp, vp]
+            L.orc_merge_attn_states.restype = None
             L.orc_ds_tile_exponent.argtypes = [dbl]
             L.orc_ds_tile_exponent.restype = i32
             L.orc_rope_fp32.argtypes = [vp, vp, vp]
@@ -318,3 +323,47 @@ def qkv_quant_cache_fp8_insert(q, k_nope, k_pe, kv_c, v, cache, slot_mapping, *,
     if rc != 0:
         raise ValueError("oracle qkv_quant_cache_fp8_insert: slot or position out of range")
     return q8, k8, v8
+
+
+def gather_context(fmt, cache, block_table, cu_seq_lens, seq_starts=None, *, num_tokens=None, raw=False,
+                   scale=1.0):
+    """Chunk gather of paged context entries.  cache: uint8 [nb, bs, stride].  Returns uint16
+    bf16 bits [num_tokens, 576] (raw=False) or uint8 entry bytes [num_tokens, entry] (raw=True);
+    rows past cu_seq_lens[-1] stay zero."""
+    cache = np.asarray(cache)
+    assert cache.dtype == np.uint8 and cache.ndim == 3
+    nb, bs, _ = cache.shape
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    cu = np.ascontiguousarray(cu_seq_lens, dtype=np.int32)
+    ss = None if seq_starts is None else np.ascontiguousarray(seq_starts, dtype=np.int32)
+    batch = cu.size - 1
+    n = int(cu[-1]) if num_tokens is None else int(num_tokens)
+    if raw:
+        dst = np.zeros((max(n, 1), ENTRY_BYTES[fmt]), dtype=np.uint8)
+        row = dst.strides[0]
+    else:
+        dst = np.zeros((max(n, 1), 576), dtype=np.uint16)
+        row = 576
+    rc = lib().orc_gather_context(int(fmt), _P(cache), nb, cache.strides[0], cache.strides[1], bs, _P(bt),
+                                  bt.shape[1], _P(cu), _P(ss), batch, n, 1 if raw else 0, float(scale), _P(dst), row)
+    if rc != 0:
+        raise ValueError("oracle gather_context: block id out of range")
+    return dst[:n]
+
+
+def merge_attn_states(prefix, prefix_lse, suffix, suffix_lse):
+    """prefix / suffix: uint16 bf16 bits [T, H, D] (last stride 1); lse: fp32 [H, T].
+    Returns (out fp64 [T, H, D], lse fp64 [H, T])."""
+    prefix, suffix = np.asarray(prefix), np.asarray(suffix)
+    assert prefix.dtype == np.uint16 and suffix.dtype == np.uint16
+    assert prefix.strides[2] == 2 and suffix.strides[2] == 2
+    T, H, D = prefix.shape
+    assert suffix.shape == (T, H, D) and D <= 512
+    pl = np.ascontiguousarray(prefix_lse, dtype=np.float32)
+    sl = np.ascontiguousarray(suffix_lse, dtype=np.float32)
+    assert pl.shape == (H, T) and sl.shape == (H, T)
+    out = np.zeros((T, H, D), dtype=np.float64)
+    lse = np.zeros((H, T), dtype=np.float64)
+    lib().orc_merge_attn_states(_P(prefix), prefix.strides[0] // 2, prefix.strides[1] // 2, _P(pl), _P(suffix),
+                                suffix.strides[0] // 2, suffix.strides[1] // 2, _P(sl), T, H, D, _P(out), _P(lse))
+    return out, lse

@@ -28,6 +28,9 @@
  *    key [k_nope | k_pe] per head, q RoPE in place, latent insert) and
  *    fused_mla_qkv_quant_kv_cache_fp8_insert (fp8 q / k / v with separate scales, cache with
  *    its own scale).
+ *  - "vllm.models.kimi_k3.nvidia.mla", _compute_prefill_context / _gather_context_latent (the
+ *    chunked context gathered from the paged cache into a dense workspace, up-converted or as
+ *    stored) and _forward_prefill_fused (merge_attn_states of prefix and suffix partials).
  *
  * Readings where the pages are silent (each also listed in the design notes):
  *  - fp8_ds_mla tile scale on insert: s = 2^k with k the smallest integer such that
@@ -570,6 +573,95 @@ int orc_qkv_quant_cache_fp8_insert(const uint16_t* q, int64_t q_s0, int64_t q_s1
                  kv_c + (int64_t)t * kv_s0, kpr, cache_scale_inv);
   }
   return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Chunked-context prefill: gather of the paged context, and the prefix / suffix merge.   */
+/* ------------------------------------------------------------------------------------ */
+
+/* "vllm.models.kimi_k3.nvidia.mla", _gather_context_latent (cp_gather_and_upconvert_fp8_kv_cache
+ * for fp8_ds_mla, gather_and_maybe_dequant_cache for bf16 / plain fp8 with a bf16 query,
+ * cp_gather_cache for plain fp8 with an fp8 query).  Request b of the chunk (batch requests)
+ * owns output rows cu_seq_lens[b] .. cu_seq_lens[b+1]-1; row cu_seq_lens[b] + i holds context
+ * position p = seq_starts[b] + i (seq_starts NULL: 0) of request b, found through
+ * block_table[b * bt_stride + p / block_size] at offset p % block_size.
+ *   out_kind 0: dst rows of 576 bf16 values (uint16 bits, dst_row elements apart): the entry's
+ *     values, each dequantised in fp32 (e4m3 value times the tile scale for fp8_ds_mla, times
+ *     `scale` for plain fp8; bf16 entries as stored) and rounded once to bf16;
+ *   out_kind 1: dst rows of the entry's stored bytes (entry_bytes of the format, dst_row bytes
+ *     apart).
+ * Rows at or past cu_seq_lens[batch] (up to num_tokens) are not written.  A row whose block
+ * id is out of range is written as zeros and reported by the return value -1. */
+int orc_gather_context(int fmt, const uint8_t* cache, int64_t num_blocks, int64_t block_stride,
+                       int64_t entry_stride, int block_size, const int32_t* block_table, int64_t bt_stride,
+                       const int32_t* cu_seq_lens, const int32_t* seq_starts, int batch, int64_t num_tokens,
+                       int out_kind, float scale, uint8_t* dst, int64_t dst_row) {
+  int bad = 0, b, d;
+  const int eb = fmt == ORC_BF16 ? 1152 : fmt == ORC_FP8 ? ENTRY : 656;
+  for (b = 0; b < batch; ++b) {
+    int64_t r;
+    for (r = cu_seq_lens[b]; r < cu_seq_lens[b + 1] && r < num_tokens; ++r) {
+      int64_t p = (seq_starts ? seq_starts[b] : 0) + (r - cu_seq_lens[b]);
+      int64_t blk = block_table[(int64_t)b * bt_stride + p / block_size];
+      const uint8_t* ent;
+      if (out_kind == 1) {
+        uint8_t* o = dst + r * dst_row;
+        if (blk < 0 || blk >= num_blocks) {
+          bad = 1;
+          memset(o, 0, (size_t)eb);
+          continue;
+        }
+        ent = cache + blk * block_stride + (p % block_size) * entry_stride;
+        memcpy(o, ent, (size_t)eb);
+      } else {
+        uint16_t* o = (uint16_t*)(dst) + r * dst_row;
+        if (blk < 0 || blk >= num_blocks) {
+          bad = 1;
+          for (d = 0; d < ENTRY; ++d) o[d] = 0;
+          continue;
+        }
+        ent = cache + blk * block_stride + (p % block_size) * entry_stride;
+        if (fmt == ORC_BF16) {
+          for (d = 0; d < ENTRY; ++d) o[d] = rd16(ent + 2 * d);
+        } else if (fmt == ORC_FP8) {
+          for (d = 0; d < ENTRY; ++d) o[d] = orc_bf16_from_float((float)orc_e4m3_to_double(ent[d]) * scale);
+        } else {
+          for (d = 0; d < KV_LORA; ++d)
+            o[d] = orc_bf16_from_float((float)orc_e4m3_to_double(ent[d]) * rdf32(ent + KV_LORA + 4 * (d / 128)));
+          for (d = 0; d < ROPE; ++d) o[KV_LORA + d] = rd16(ent + KV_LORA + 16 + 2 * d);
+        }
+      }
+    }
+  }
+  return bad ? -1 : 0;
+}
+
+/* "vllm.models.kimi_k3.nvidia.mla", _forward_prefill_fused: merge_attn_states of the
+ * context (prefix) and new-token (suffix) partial attentions.  For token t and head h:
+ *   lse = ln(e^{lse_p} + e^{lse_s}),  out = e^{lse_p - lse} O_p + e^{lse_s - lse} O_s
+ * (orc_merge with two parts).  O_p, O_s: bf16 [T, H, D] with element strides; lse_p, lse_s:
+ * fp32 [H, T]; out: fp64 [T, H, D]; out_lse: fp64 [H, T]. */
+void orc_merge_attn_states(const uint16_t* prefix, int64_t p_s0, int64_t p_s1, const float* prefix_lse,
+                           const uint16_t* suffix, int64_t s_s0, int64_t s_s1, const float* suffix_lse, int T, int H,
+                           int D, double* out, double* out_lse) {
+  int t, h, d;
+  double* parts = (double*)malloc(sizeof(double) * 2 * KV_LORA);
+  for (t = 0; t < T; ++t)
+    for (h = 0; h < H; ++h) {
+      double lp[2], o[KV_LORA], l;
+      const uint16_t* a = prefix + (int64_t)t * p_s0 + (int64_t)h * p_s1;
+      const uint16_t* c = suffix + (int64_t)t * s_s0 + (int64_t)h * s_s1;
+      for (d = 0; d < KV_LORA; ++d) {
+        parts[d] = d < D ? orc_bf16_to_double(a[d]) : 0.0;
+        parts[KV_LORA + d] = d < D ? orc_bf16_to_double(c[d]) : 0.0;
+      }
+      lp[0] = (double)prefix_lse[(int64_t)h * T + t];
+      lp[1] = (double)suffix_lse[(int64_t)h * T + t];
+      orc_merge(2, parts, lp, o, &l);
+      for (d = 0; d < D; ++d) out[((int64_t)t * H + h) * D + d] = o[d];
+      out_lse[(int64_t)h * T + t] = l;
+    }
+  free(parts);
 }
 
 /* Exposed for the self-tests: the tile exponent rule and the fp32 rotation. */
