@@ -287,6 +287,57 @@ MLA_API int mla_paged_decode_noalloc(const void* q, int64_t q_s0, int64_t q_s1, 
                                      float softmax_scale, float q_scale, float k_scale, void* out,
                                      int64_t o_s0, int64_t o_s1, float* lse, cudaStream_t stream);
 
+/* Output kinds of mla_gather_context. */
+#define MLA_GATHER_BF16 0   /* the 576 values as bf16 */
+#define MLA_GATHER_RAW 1    /* the entry bytes as stored */
+
+/*
+ * Chunked-context gather: one chunk of the requests' cached context, read through their block
+ * tables into a dense workspace for the context part of a long prefill.
+ * Follows: "vllm.models.kimi_k3.nvidia.mla", _compute_prefill_context / _gather_context_latent
+ * (cp_gather_and_upconvert_fp8_kv_cache for fp8_ds_mla, gather_and_maybe_dequant_cache for the
+ * bf16 and plain fp8 caches under a bf16 query, cp_gather_cache for plain fp8 under an fp8 query).
+ *
+ *   kv_cache, fmt, num_blocks, block_stride_bytes, entry_stride_bytes, block_size
+ *                the paged cache, as in mla_paged_decode.
+ *   block_table  device int32 [batch, >= blocks needed], row stride bt_stride: the chunk's
+ *                requests' rows.
+ *   cu_seq_lens  device int32 [batch + 1], non-decreasing from 0: request b fills rows
+ *                cu_seq_lens[b] .. cu_seq_lens[b+1]-1 of dst.
+ *   seq_starts   device int32 [batch] or NULL (all 0): row cu_seq_lens[b] + i holds context
+ *                position seq_starts[b] + i of request b.
+ *   num_tokens   rows of dst; rows at or past cu_seq_lens[batch] are not written.
+ *   out_kind     MLA_GATHER_BF16: dst rows of 576 bf16 values -- bf16 entries as stored; plain
+ *                fp8 entries e4m3 * scale; fp8_ds_mla codes e4m3 * tile scale and the bf16 rope;
+ *                every product in fp32, rounded once to bf16 (round to nearest even).
+ *                MLA_GATHER_RAW: dst rows of the entry bytes as stored (1152 / 576 / 656).
+ *   scale        the plain fp8 cache's dequantisation scale (k_scale); unused otherwise.
+ *   dst          device out, rows dst_row_stride_bytes apart.
+ * A row whose block id is out of range is written as zeros and sets MLA_DEVERR_BLOCK.
+ */
+MLA_API int mla_gather_context(const void* kv_cache, mla_cache_format fmt, int64_t num_blocks,
+                               int64_t block_stride_bytes, int64_t entry_stride_bytes, int32_t block_size,
+                               const int32_t* block_table, int64_t bt_stride, const int32_t* cu_seq_lens,
+                               const int32_t* seq_starts, int32_t batch, int64_t num_tokens, int32_t out_kind,
+                               float scale, void* dst, int64_t dst_row_stride_bytes, cudaStream_t stream);
+
+/*
+ * Merge of two partial attentions of the same queries over disjoint key sets by their
+ * log-sum-exp: the context (prefix) and new-token (suffix) parts of a chunked prefill.
+ * Follows: "vllm.models.kimi_k3.nvidia.mla", _forward_prefill_fused (merge_attn_states).
+ *   lse = ln(e^{lse_p} + e^{lse_s}),  output = e^{lse_p - lse} prefix + e^{lse_s - lse} suffix,
+ * computed in fp32 and rounded once to bf16; both -inf -> 0 and -inf.
+ *
+ *   output, prefix_output, suffix_output  device bf16 [T, H, D], element strides
+ *                (o_s0, o_s1) / (p_s0, p_s1) / (s_s0, s_s1), unit innermost stride.
+ *   prefix_lse, suffix_lse  device fp32 [H, T] contiguous (natural log).
+ *   output_lse   device fp32 [H, T] contiguous, or NULL to skip.
+ */
+MLA_API int mla_merge_attn_states(void* output, int64_t o_s0, int64_t o_s1, float* output_lse,
+                                  const void* prefix_output, int64_t p_s0, int64_t p_s1, const float* prefix_lse,
+                                  const void* suffix_output, int64_t s_s0, int64_t s_s1, const float* suffix_lse,
+                                  int32_t T, int32_t H, int32_t D, cudaStream_t stream);
+
 /*
  * Gather-and-dequantise (test and debugging aid): out[i, 0..575] = the exact fp32 values of
  * the entry at slots[i] (paged addressing as in mla_paged_decode; NoPE times its tile scale

@@ -15,6 +15,8 @@ Entry points (same names as the C ABI, without the ``mla_`` prefix):
                          own scales, latent insert with the cache scale
   sparse_fwd             sparse CSR forward over 656-byte fp8_ds_mla records
   paged_decode           paged decode / spec-verify (split-K + LSE merge)
+  gather_context         chunked-context gather of paged entries (bf16 values or stored bytes)
+  merge_attn_states      prefix / suffix merge of partial attentions by their LSEs
   gather_dequant         paged entries -> exact fp32 values (test aid)
 
 Every tensor argument is checked here before the call (CUDA device, dtype, rank, unit
@@ -72,6 +74,8 @@ def lib():
         L.mla_profile_attention_events.restype = None
         L.mla_gather_dequant.argtypes = [vp, i32, i64, i64, i64, i32, vp, i64, vp, vp]
         L.mla_sparse_fwd_staged.argtypes = L.mla_sparse_fwd.argtypes
+        L.mla_gather_context.argtypes = [vp, i32, i64, i64, i64, i32, vp, i64, vp, vp, i32, i64, i32, f32, vp, i64, vp]
+        L.mla_merge_attn_states.argtypes = [vp, i64, i64, vp, vp, i64, i64, vp, vp, i64, i64, vp, i32, i32, i32, vp]
         L.mla_key_concat_cache_insert.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, vp, i64, vp, vp, i32, i64, i64,
                                                   i64, i32, vp, vp, vp, i64, i32, i32, i32, vp]
         L.mla_qkv_quant_cache_fp8_insert.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, vp, i64, vp, i64, i64, vp,
@@ -80,7 +84,8 @@ def lib():
         L.mla_debug_stall_next_decode.argtypes = [i32]
         L.mla_debug_stall_next_decode.restype = None
         for f in ("mla_q_concat_cache_insert", "mla_sparse_fwd", "mla_sparse_fwd_staged", "mla_paged_decode",
-                  "mla_gather_dequant", "mla_key_concat_cache_insert", "mla_qkv_quant_cache_fp8_insert"):
+                  "mla_gather_dequant", "mla_key_concat_cache_insert", "mla_qkv_quant_cache_fp8_insert",
+                  "mla_gather_context", "mla_merge_attn_states"):
             getattr(L, f).restype = ctypes.c_int
         L.mla_read_device_errors.restype = ctypes.c_int
         _lib = L
@@ -343,6 +348,59 @@ def paged_decode(q, kv_cache, block_table, seq_lens, *, fmt, q_len=1, max_contex
             _ptr(lse), _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
             _stream(q)))
     return out, lse
+
+
+def gather_context(kv_cache, block_table, cu_seq_lens, seq_starts=None, *, fmt, num_tokens, raw=False,
+                   scale=1.0, dst=None):
+    """Chunked-context gather: rows cu_seq_lens[b] .. cu_seq_lens[b+1]-1 hold request b's context
+    positions seq_starts[b] + i.  Returns dst [num_tokens, 576] bf16 (raw=False) or
+    [num_tokens, entry bytes] uint8 (raw=True)."""
+    fmt = _fmt(fmt)
+    dev = _cuda_device(kv_cache)
+    _need(kv_cache, "kv_cache", _BYTE_TYPES + (torch.bfloat16,), dev)
+    _need(block_table, "block_table", (torch.int32,), dev, ndim=2)
+    _need(cu_seq_lens, "cu_seq_lens", (torch.int32,), dev, ndim=1, contiguous=True)
+    if seq_starts is not None:
+        _need(seq_starts, "seq_starts", (torch.int32,), dev, ndim=1, contiguous=True)
+    batch = cu_seq_lens.numel() - 1
+    if block_table.shape[0] < batch or (seq_starts is not None and seq_starts.numel() < batch):
+        raise ValueError("block_table and seq_starts need a row per request of the chunk")
+    if dst is None:
+        dst = (torch.empty((num_tokens, ENTRY_BYTES[fmt]), dtype=torch.uint8, device=dev) if raw else
+               torch.empty((num_tokens, 576), dtype=torch.bfloat16, device=dev))
+    _need(dst, "dst", _BYTE_TYPES if raw else (torch.bfloat16,), dev, ndim=2)
+    nb, bstride, estride, bs = _cache_geometry(kv_cache)
+    with torch.cuda.device(dev):
+        _check(lib().mla_gather_context(_ptr(kv_cache), fmt, nb, bstride, estride, bs, _ptr(block_table),
+                                        block_table.stride(0), _ptr(cu_seq_lens), _ptr(seq_starts), batch,
+                                        int(num_tokens), 1 if raw else 0, float(scale), _ptr(dst),
+                                        dst.stride(0) * dst.element_size(), _stream(kv_cache)))
+    return dst
+
+
+def merge_attn_states(prefix_output, prefix_lse, suffix_output, suffix_lse, *, output=None, return_lse=False):
+    """Merge of a prefix and a suffix partial attention (bf16 [T, H, D], lse fp32 [H, T]).
+    Returns (output [T, H, D] bf16, lse [H, T] or None)."""
+    dev = _cuda_device(prefix_output)
+    _need(prefix_output, "prefix_output", (torch.bfloat16,), dev, ndim=3)
+    _need(suffix_output, "suffix_output", (torch.bfloat16,), dev, ndim=3)
+    T, H, D = prefix_output.shape
+    if tuple(suffix_output.shape) != (T, H, D):
+        raise ValueError("prefix and suffix outputs differ in shape")
+    for n, t in (("prefix_lse", prefix_lse), ("suffix_lse", suffix_lse)):
+        _need(t, n, (torch.float32,), dev, ndim=2, contiguous=True)
+        if tuple(t.shape) != (H, T):
+            raise ValueError(f"{n} must be [H, T] = {(H, T)}, got {tuple(t.shape)}")
+    if output is None:
+        output = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    _need(output, "output", (torch.bfloat16,), dev, ndim=3)
+    lse = torch.empty((H, T), dtype=torch.float32, device=dev) if return_lse else None
+    with torch.cuda.device(dev):
+        _check(lib().mla_merge_attn_states(
+            _ptr(output), output.stride(0), output.stride(1), _ptr(lse), _ptr(prefix_output), prefix_output.stride(0),
+            prefix_output.stride(1), _ptr(prefix_lse), _ptr(suffix_output), suffix_output.stride(0),
+            suffix_output.stride(1), _ptr(suffix_lse), T, H, D, _stream(prefix_output)))
+    return output, lse
 
 
 def gather_dequant(kv_cache, slots, *, fmt):

@@ -870,3 +870,90 @@ extern "C" int mla_gather_dequant(const void* kv_cache, mla_cache_format fmt, in
     return fail(MLA_ERR_CUDA, "gather launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return ok();
 }
+
+// ------------------------------------------------------------------------------------------
+extern "C" int mla_gather_context(const void* kv_cache, mla_cache_format fmt, int64_t num_blocks,
+                                  int64_t block_stride_bytes, int64_t entry_stride_bytes, int32_t block_size,
+                                  const int32_t* block_table, int64_t bt_stride, const int32_t* cu_seq_lens,
+                                  const int32_t* seq_starts, int32_t batch, int64_t num_tokens, int32_t out_kind,
+                                  float scale, void* dst, int64_t dst_row_stride_bytes, cudaStream_t stream) {
+  if (fmt != MLA_CACHE_BF16 && fmt != MLA_CACHE_FP8 && fmt != MLA_CACHE_FP8_DS_MLA)
+    return fail(MLA_ERR_INVALID, "unknown cache format %d", static_cast<int>(fmt));
+  if (out_kind != MLA_GATHER_BF16 && out_kind != MLA_GATHER_RAW)
+    return fail(MLA_ERR_INVALID, "unknown gather output kind %d", out_kind);
+  if (batch < 0 || num_tokens < 0) return fail(MLA_ERR_INVALID, "batch and num_tokens must be >= 0");
+  if (batch == 0 || num_tokens == 0) return ok();
+  if (!kv_cache || !block_table || !cu_seq_lens || !dst) return fail(MLA_ERR_INVALID, "a required pointer is NULL");
+  if (block_size < 1 || num_blocks < 1 || bt_stride < 1 || entry_stride_bytes < entry_bytes(fmt) ||
+      block_stride_bytes < entry_stride_bytes * block_size)
+    return fail(MLA_ERR_INVALID, "bad cache geometry");
+  const int64_t row_bytes = out_kind == MLA_GATHER_RAW ? entry_bytes(fmt) : 1152;
+  if (dst_row_stride_bytes < row_bytes) return fail(MLA_ERR_INVALID, "dst rows overlap");
+  if (out_kind == MLA_GATHER_BF16 && (!aligned(dst, 2) || dst_row_stride_bytes % 2))
+    return fail(MLA_ERR_INVALID, "bf16 dst rows must be 2-byte aligned");
+  if (fmt == MLA_CACHE_FP8_DS_MLA && (entry_stride_bytes % 4 || block_stride_bytes % 4 || !aligned(kv_cache, 4)))
+    return fail(MLA_ERR_INVALID, "fp8_ds_mla entries must be 4-byte aligned");
+  if (fmt == MLA_CACHE_BF16 && (entry_stride_bytes % 2 || block_stride_bytes % 2 || !aligned(kv_cache, 2)))
+    return fail(MLA_ERR_INVALID, "bf16 entries must be 2-byte aligned");
+  if (num_tokens >= (int64_t(1) << 33)) return fail(MLA_ERR_UNSUPPORTED, "num_tokens too large");
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  GatherCtxParams p{};
+  p.cache = static_cast<const uint8_t*>(kv_cache);
+  p.num_blocks = num_blocks;
+  p.block_stride = block_stride_bytes;
+  p.entry_stride = entry_stride_bytes;
+  p.block_size = block_size;
+  p.block_table = block_table;
+  p.bt_stride = bt_stride;
+  p.cu = cu_seq_lens;
+  p.starts = seq_starts;
+  p.batch = batch;
+  p.num_tokens = num_tokens;
+  p.scale = scale;
+  p.dst = static_cast<uint8_t*>(dst);
+  p.dst_row = dst_row_stride_bytes;
+  p.vec = aligned(kv_cache, 16) && entry_stride_bytes % 16 == 0 && block_stride_bytes % 16 == 0 && aligned(dst, 16) &&
+          dst_row_stride_bytes % 16 == 0;
+  p.err = d->err;
+  if (launch_gather_context(static_cast<int>(fmt), out_kind, p, stream) != cudaSuccess)
+    return fail(MLA_ERR_CUDA, "gather launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  return ok();
+}
+
+extern "C" int mla_merge_attn_states(void* output, int64_t o_s0, int64_t o_s1, float* output_lse,
+                                     const void* prefix_output, int64_t p_s0, int64_t p_s1, const float* prefix_lse,
+                                     const void* suffix_output, int64_t s_s0, int64_t s_s1, const float* suffix_lse,
+                                     int32_t T, int32_t H, int32_t D, cudaStream_t stream) {
+  if (T < 0 || H < 1 || D < 1) return fail(MLA_ERR_INVALID, "bad shape T=%d H=%d D=%d", T, H, D);
+  if (T == 0) return ok();
+  if (!output || !prefix_output || !prefix_lse || !suffix_output || !suffix_lse)
+    return fail(MLA_ERR_INVALID, "a required pointer is NULL");
+  if (o_s1 < D || o_s0 < static_cast<int64_t>(H) * o_s1 || p_s1 < D || p_s0 < static_cast<int64_t>(H) * p_s1 ||
+      s_s1 < D || s_s0 < static_cast<int64_t>(H) * s_s1)
+    return fail(MLA_ERR_INVALID, "strides overlap rows");
+  if (!aligned(output, 2) || !aligned(prefix_output, 2) || !aligned(suffix_output, 2) || !aligned(prefix_lse, 4) ||
+      !aligned(suffix_lse, 4) || (output_lse && !aligned(output_lse, 4)))
+    return fail(MLA_ERR_INVALID, "misaligned tensor");
+  MergeStatesParams p{};
+  p.out = static_cast<uint16_t*>(output);
+  p.o_s0 = o_s0;
+  p.o_s1 = o_s1;
+  p.out_lse = output_lse;
+  p.prefix = static_cast<const uint16_t*>(prefix_output);
+  p.p_s0 = p_s0;
+  p.p_s1 = p_s1;
+  p.prefix_lse = prefix_lse;
+  p.suffix = static_cast<const uint16_t*>(suffix_output);
+  p.s_s0 = s_s0;
+  p.s_s1 = s_s1;
+  p.suffix_lse = suffix_lse;
+  p.T = T;
+  p.H = H;
+  p.D = D;
+  p.vec = D % 8 == 0 && aligned(output, 16) && aligned(prefix_output, 16) && aligned(suffix_output, 16) &&
+          o_s0 % 8 == 0 && o_s1 % 8 == 0 && p_s0 % 8 == 0 && p_s1 % 8 == 0 && s_s0 % 8 == 0 && s_s1 % 8 == 0;
+  if (launch_merge_states(p, stream) != cudaSuccess)
+    return fail(MLA_ERR_CUDA, "merge launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  return ok();
+}

@@ -77,6 +77,39 @@ struct MergeParams {
   float* lse;              // [n_rows, H] or null
 };
 
+// Chunked-context gather: rows of a chunk's context entries through the block table.
+struct GatherCtxParams {
+  const uint8_t* cache;
+  int64_t num_blocks, block_stride, entry_stride;
+  int block_size;
+  const int32_t* block_table;
+  int64_t bt_stride;
+  const int32_t* cu;       // [batch + 1]
+  const int32_t* starts;   // [batch] or null
+  int batch;
+  int64_t num_tokens;
+  float scale;             // plain fp8 dequantisation scale
+  uint8_t* dst;
+  int64_t dst_row;         // bytes
+  int vec;                 // cache entries and dst rows 16-byte aligned
+  uint32_t* err;
+};
+
+// merge_attn_states of a prefix and a suffix partial (bf16 [T, H, D], lse fp32 [H, T]).
+struct MergeStatesParams {
+  uint16_t* out;
+  int64_t o_s0, o_s1;
+  float* out_lse;
+  const uint16_t* prefix;
+  int64_t p_s0, p_s1;
+  const float* prefix_lse;
+  const uint16_t* suffix;
+  int64_t s_s0, s_s1;
+  const float* suffix_lse;
+  int T, H, D;
+  int vec;                 // rows 16-byte aligned, D a multiple of 8
+};
+
 struct GatherParams {
   const uint8_t* cache;
   int64_t num_blocks, block_stride, entry_stride;
@@ -95,6 +128,9 @@ cudaError_t launch_epilogue(int fmt, const EpiParams& p, int B, cudaStream_t str
 cudaError_t launch_prefill_epilogue(int fmt, const PrefillEpiParams& p, int Tp, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
 cudaError_t launch_gather(int fmt, const GatherParams& p, cudaStream_t stream);
+// kind 0: bf16 values, 1: stored bytes
+cudaError_t launch_gather_context(int fmt, int kind, const GatherCtxParams& p, cudaStream_t stream);
+cudaError_t launch_merge_states(const MergeStatesParams& p, cudaStream_t stream);
 
 // Attention launchers (one translation unit per cache format).  `grid` CTAs, each looping
 // over work items; dynamic shared memory is set up on first use per device.

@@ -3,6 +3,7 @@
 //   * the split-K merge of partial attentions by their log-sum-exp;
 //   * gather-and-dequantise of cache entries (a test aid with the kernels' addressing).
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <math_constants.h>
@@ -476,6 +477,157 @@ cudaError_t launch_gather(int fmt, const GatherParams& p, cudaStream_t stream) {
     mla_gather_kernel<1><<<grid, 128, 0, stream>>>(p);
   else
     mla_gather_kernel<2><<<grid, 128, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------
+// Chunked-context gather.  "vllm.models.kimi_k3.nvidia.mla", _gather_context_latent: request b
+// of a chunk owns rows cu[b] .. cu[b+1]-1; row cu[b] + i is context position starts[b] + i of
+// request b, found through its block-table row.  kind 0 writes the 576 values as bf16 (fp8
+// codes times their scale in fp32, rounded once; bf16 entries as stored), kind 1 the stored
+// entry bytes.  One warp per row, 16-byte pieces per lane.
+
+__device__ __forceinline__ void e4m3x16_to_bf16(const uint4 c, float scale, uint4 (&o)[2]) {
+  const uint32_t w[4] = {c.x, c.y, c.z, c.w};
+  uint32_t r[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] >> (16 * hh)), __NV_E4M3);
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2));     // exact
+      r[2 * i + hh] = static_cast<uint32_t>(bf16_bits(f.x * scale)) | (static_cast<uint32_t>(bf16_bits(f.y * scale)) << 16);
+    }
+  }
+  o[0] = make_uint4(r[0], r[1], r[2], r[3]);
+  o[1] = make_uint4(r[4], r[5], r[6], r[7]);
+}
+
+template <int F, int KIND>
+__global__ void __launch_bounds__(128) mla_gather_context_kernel(const GatherCtxParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t r = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (r >= p.num_tokens || r >= p.cu[p.batch]) return;
+  int lo = 0, hi = p.batch - 1;           // the last request b with cu[b] <= r
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (p.cu[mid] <= r) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const int64_t pos = (p.starts ? p.starts[b] : 0) + (r - p.cu[b]);
+  const int64_t blk = p.block_table[static_cast<int64_t>(b) * p.bt_stride + pos / p.block_size];
+  constexpr int kEntry = F == 0 ? 1152 : F == 1 ? 576 : 656;
+  constexpr int kOut = KIND == 1 ? kEntry : 1152;
+  uint8_t* dst = p.dst + r * p.dst_row;
+  if (blk < 0 || blk >= p.num_blocks) {
+    if (lane == 0) set_device_error(p.err, 2u);
+    for (int i = lane; i < kOut; i += 32) dst[i] = 0;
+    return;
+  }
+  const uint8_t* ent = p.cache + blk * p.block_stride + (pos % p.block_size) * p.entry_stride;
+  if (!p.vec) {
+    if (KIND == 1 || F == 0) {
+      for (int i = lane; i < kEntry; i += 32) dst[i] = ent[i];
+    } else {
+      uint16_t* o = reinterpret_cast<uint16_t*>(dst);
+      for (int d = lane; d < 576; d += 32) {
+        float x;
+        if (F == 1) {
+          x = __half2float(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(ent[d]), __NV_E4M3)) * p.scale;
+          o[d] = bf16_bits(x);
+        } else if (d < 512) {
+          const float sj = *reinterpret_cast<const float*>(ent + 512 + 4 * (d >> 7));
+          o[d] = bf16_bits(__half2float(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(ent[d]), __NV_E4M3)) * sj);
+        } else {
+          o[d] = static_cast<uint16_t>(ent[528 + 2 * (d - 512)] | (ent[529 + 2 * (d - 512)] << 8));
+        }
+      }
+    }
+    return;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(ent);
+  uint4* out = reinterpret_cast<uint4*>(dst);
+  if (KIND == 1 || F == 0) {
+    for (int i = lane; i < kEntry / 16; i += 32) out[i] = __ldg(src + i);
+  } else if (F == 1) {
+    for (int i = lane; i < 36; i += 32) {       // 16 codes -> 16 bf16 values
+      uint4 o[2];
+      e4m3x16_to_bf16(__ldg(src + i), p.scale, o);
+      out[2 * i] = o[0];
+      out[2 * i + 1] = o[1];
+    }
+  } else {
+    uint4 o[2];
+    const float sj = __ldg(reinterpret_cast<const float*>(ent + 512) + (lane >> 3));
+    e4m3x16_to_bf16(__ldg(src + lane), sj, o);
+    out[2 * lane] = o[0];
+    out[2 * lane + 1] = o[1];
+    if (lane < 8) out[64 + lane] = __ldg(src + 33 + lane);     // rope bytes 528.. -> values 512..
+  }
+}
+
+cudaError_t launch_gather_context(int fmt, int kind, const GatherCtxParams& p, cudaStream_t stream) {
+  const unsigned grid = static_cast<unsigned>((p.num_tokens + 3) / 4);
+  if (kind == 1) {
+    if (fmt == 0) mla_gather_context_kernel<0, 1><<<grid, 128, 0, stream>>>(p);
+    else if (fmt == 1) mla_gather_context_kernel<1, 1><<<grid, 128, 0, stream>>>(p);
+    else mla_gather_context_kernel<2, 1><<<grid, 128, 0, stream>>>(p);
+  } else {
+    if (fmt == 0) mla_gather_context_kernel<0, 0><<<grid, 128, 0, stream>>>(p);
+    else if (fmt == 1) mla_gather_context_kernel<1, 0><<<grid, 128, 0, stream>>>(p);
+    else mla_gather_context_kernel<2, 0><<<grid, 128, 0, stream>>>(p);
+  }
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------------------------
+// merge_attn_states ("vllm.models.kimi_k3.nvidia.mla", _forward_prefill_fused): the context
+// (prefix) and new-token (suffix) partials of prefill attention combined by their LSEs,
+//   lse = ln(e^{lse_p} + e^{lse_s}),  out = e^{lse_p - lse} O_p + e^{lse_s - lse} O_s,
+// in fp32, rounded once to bf16; both empty (-inf) -> 0 and -inf.  One warp per (token,
+// head), 8 values per lane per step.
+__global__ void __launch_bounds__(128) mla_merge_states_kernel(const MergeStatesParams p) {
+  const int lane = threadIdx.x & 31;
+  const int64_t th = static_cast<int64_t>(blockIdx.x) * 4 + (threadIdx.x >> 5);
+  if (th >= static_cast<int64_t>(p.T) * p.H) return;
+  const int t = static_cast<int>(th / p.H), h = static_cast<int>(th % p.H);
+  const float lp = p.prefix_lse[static_cast<int64_t>(h) * p.T + t];
+  const float ls = p.suffix_lse[static_cast<int64_t>(h) * p.T + t];
+  const float m = fmaxf(lp, ls);
+  float wp = 0.f, ws = 0.f, lse = -CUDART_INF_F;
+  if (m != -CUDART_INF_F) {
+    const float ep = expf(lp - m), es = expf(ls - m);
+    const float inv = 1.f / (ep + es);
+    wp = ep * inv;
+    ws = es * inv;
+    lse = m + logf(ep + es);
+  }
+  const uint16_t* a = p.prefix + t * p.p_s0 + h * p.p_s1;
+  const uint16_t* c = p.suffix + t * p.s_s0 + h * p.s_s1;
+  uint16_t* o = p.out + t * p.o_s0 + h * p.o_s1;
+  if (p.vec) {
+    for (int d0 = 8 * lane; d0 < p.D; d0 += 256) {
+      const uint4 va = __ldg(reinterpret_cast<const uint4*>(a + d0));
+      const uint4 vc = __ldg(reinterpret_cast<const uint4*>(c + d0));
+      const uint32_t xa[4] = {va.x, va.y, va.z, va.w}, xc[4] = {vc.x, vc.y, vc.z, vc.w};
+      uint32_t r[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float lo = wp * __uint_as_float(xa[i] << 16) + ws * __uint_as_float(xc[i] << 16);
+        const float hi = wp * __uint_as_float(xa[i] & 0xFFFF0000u) + ws * __uint_as_float(xc[i] & 0xFFFF0000u);
+        r[i] = static_cast<uint32_t>(bf16_bits(lo)) | (static_cast<uint32_t>(bf16_bits(hi)) << 16);
+      }
+      *reinterpret_cast<uint4*>(o + d0) = make_uint4(r[0], r[1], r[2], r[3]);
+    }
+  } else {
+    for (int d = lane; d < p.D; d += 32) o[d] = bf16_bits(wp * bf16_at(a + d) + ws * bf16_at(c + d));
+  }
+  if (lane == 0 && p.out_lse) p.out_lse[static_cast<int64_t>(h) * p.T + t] = lse;
+}
+
+cudaError_t launch_merge_states(const MergeStatesParams& p, cudaStream_t stream) {
+  const int64_t n = static_cast<int64_t>(p.T) * p.H;
+  mla_merge_states_kernel<<<static_cast<unsigned>((n + 3) / 4), 128, 0, stream>>>(p);
   return cudaGetLastError();
 }
 
