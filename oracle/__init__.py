@@ -87,6 +87,9 @@ def lib():
             L.orc_gather_context.restype = i32
             L.orc_merge_attn_states.argtypes = [vp, i64, i64, vp, vp, i64, i64, vp, i32, i32, i32, vp, vp]
             L.orc_merge_attn_states.restype = None
+            L.orc_sparse_fwd_ext.argtypes = [vp, i64, i64, vp, i64, i64, vp, vp, vp, i64, i64, vp, vp, vp, dbl, i32,
+                                             i32, i32, vp, vp]
+            L.orc_sparse_fwd_ext.restype = i32
             L.orc_ds_tile_exponent.argtypes = [dbl]
             L.orc_ds_tile_exponent.restype = i32
             L.orc_rope_fp32.argtypes = [vp, vp, vp]
@@ -177,6 +180,41 @@ def sparse_fwd(q_bits, records, indptr, indices, softmax_scale, has_invalid, row
                               _P(out), _P(lse))
     if rc != 0:
         raise ValueError("oracle sparse_fwd: index out of range")
+    return out, lse
+
+
+def sparse_fwd_ext(q_bits, records, indptr, indices, softmax_scale, has_invalid, *, extra_records=None,
+                   extra_indptr=None, extra_indices=None, attn_sink=None):
+    """Sparse forward with the general op's extras: an attention sink per head (fp32 [H]) and a
+    second key segment (extra_records [N2, >=656], extra_indptr [T+1], extra_indices).
+    Returns (out [T, H, 512] f64, lse [T, H] f64)."""
+    q_bits = np.asarray(q_bits)
+    assert q_bits.dtype == np.uint16 and q_bits.strides[2] == 2
+    T, H, _ = q_bits.shape
+    rec = np.asarray(records, dtype=np.uint8)
+    assert rec.ndim == 2 and rec.strides[1] == 1 and rec.shape[1] >= 656
+    ip = np.ascontiguousarray(indptr, dtype=np.int64)
+    ix = np.ascontiguousarray(indices, dtype=np.int64)
+    if ix.size == 0:
+        ix = np.zeros(1, dtype=np.int64)
+    rec2 = ip2 = ix2 = None
+    if extra_records is not None:
+        rec2 = np.asarray(extra_records, dtype=np.uint8)
+        assert rec2.ndim == 2 and rec2.strides[1] == 1 and rec2.shape[1] >= 656
+        ip2 = np.ascontiguousarray(extra_indptr, dtype=np.int64)
+        ix2 = np.ascontiguousarray(extra_indices, dtype=np.int64)
+        if ix2.size == 0:
+            ix2 = np.zeros(1, dtype=np.int64)
+    sk = None if attn_sink is None else np.ascontiguousarray(attn_sink, dtype=np.float32)
+    assert sk is None or sk.shape == (H,)
+    out = np.zeros((T, H, 512), dtype=np.float64)
+    lse = np.zeros((T, H), dtype=np.float64)
+    rc = lib().orc_sparse_fwd_ext(_P(q_bits), q_bits.strides[0] // 2, q_bits.strides[1] // 2, _P(rec), rec.strides[0],
+                                  rec.shape[0], _P(ip), _P(ix), _P(rec2), 0 if rec2 is None else rec2.strides[0],
+                                  0 if rec2 is None else rec2.shape[0], _P(ip2), _P(ix2), _P(sk), float(softmax_scale),
+                                  int(bool(has_invalid)), T, H, _P(out), _P(lse))
+    if rc != 0:
+        raise ValueError("oracle sparse_fwd_ext: index out of range")
     return out, lse
 
 

@@ -234,6 +234,90 @@ int orc_sparse_fwd(const uint16_t* q, int64_t q_s0, int64_t q_s1, const uint8_t*
 }
 
 /* ------------------------------------------------------------------------------------ */
+/* Sparse forward with the general op's extras: attention sink and a second KV segment.  */
+/* ------------------------------------------------------------------------------------ */
+
+/* "vllm.models.kimi_k3.amd.ops.flydsl_sparse_mla", flydsl_sparse_mla_fp8ds_supported: the
+ * general sparse_mla_fwd also takes attn_sink, a second key segment (extra_kv, extra_indptr,
+ * extra_indices) and kv_splits, which the FlyDSL slice refuses.  The page names them only;
+ * the readings taken here:
+ *   - extra segment: row t attends the union (a multiset) of its keys in the first segment
+ *     (kv_indices[kv_indptr[t]..] into records) and in the second (extra_indices
+ *     [extra_indptr[t]..] into extra_records), under one softmax; negative entries of either
+ *     are masked when has_invalid;
+ *   - attn_sink[h]: a logit of head h (natural-log units, like softmax_scale * q.k) that
+ *     joins the softmax denominator with a zero value:
+ *       lse = ln(sum_k e^{x_k} + e^{sink_h}),  out = sum_k e^{x_k - lse} V_k,
+ *     so a row without keys gives out = 0 and lse = sink_h (sink = -inf: no sink);
+ *   - kv_splits: a partition of each row's key list for parallelism, which leaves the
+ *     result unchanged (this function has no counterpart of it).
+ * Arguments as orc_sparse_fwd, plus records2 / indptr2 / indices2 (all NULL: no second
+ * segment) and sink [H] (NULL: none). */
+int orc_sparse_fwd_ext(const uint16_t* q, int64_t q_s0, int64_t q_s1, const uint8_t* records,
+                       int64_t record_stride, int64_t num_records, const int64_t* indptr, const int64_t* indices,
+                       const uint8_t* records2, int64_t record_stride2, int64_t num_records2,
+                       const int64_t* indptr2, const int64_t* indices2, const float* sink, double softmax_scale,
+                       int has_invalid, int T, int H, double* out, double* lse) {
+  int bad = 0;
+  int t;
+#pragma omp parallel for schedule(dynamic, 1) reduction(| : bad)
+  for (t = 0; t < T; ++t) {
+    int64_t n1 = indptr[t + 1] - indptr[t], n2 = records2 ? indptr2[t + 1] - indptr2[t] : 0, j, n = 0;
+    int64_t cap = (n1 > 0 ? n1 : 0) + (n2 > 0 ? n2 : 0);
+    double* K = (double*)malloc(sizeof(double) * ENTRY * (size_t)(cap > 0 ? cap : 1));
+    double* x = (double*)malloc(sizeof(double) * (size_t)(cap > 0 ? cap : 1));
+    double qv[ENTRY];
+    int h, d, seg;
+    for (seg = 0; seg < 2; ++seg) {
+      const uint8_t* rec = seg ? records2 : records;
+      int64_t stride = seg ? record_stride2 : record_stride, nrec = seg ? num_records2 : num_records;
+      const int64_t* ptr = seg ? indptr2 : indptr;
+      const int64_t* idxs = seg ? indices2 : indices;
+      if (!rec) continue;
+      for (j = ptr[t]; j < ptr[t + 1]; ++j) {
+        int64_t idx = idxs[j];
+        if (idx < 0 && has_invalid) continue;
+        if (idx < 0 || idx >= nrec) {
+          bad = 1;
+          continue;
+        }
+        orc_decode_entry(ORC_DS_MLA, rec + idx * stride, K + n * ENTRY);
+        ++n;
+      }
+    }
+    for (h = 0; h < H; ++h) {
+      const uint16_t* qp = q + (int64_t)t * q_s0 + (int64_t)h * q_s1;
+      double* o = out + ((int64_t)t * H + h) * KV_LORA;
+      double sk = sink ? (double)sink[h] : -INFINITY, m = sk, l = 0.0, ls;
+      int64_t k;
+      for (d = 0; d < ENTRY; ++d) qv[d] = orc_bf16_to_double(qp[d]);
+      for (d = 0; d < KV_LORA; ++d) o[d] = 0.0;
+      for (k = 0; k < n; ++k) {
+        double acc = 0.0;
+        for (d = 0; d < ENTRY; ++d) acc += qv[d] * K[k * ENTRY + d];
+        x[k] = softmax_scale * acc;
+        if (x[k] > m) m = x[k];
+      }
+      if (m == -INFINITY) {
+        lse[(int64_t)t * H + h] = -INFINITY;
+        continue;
+      }
+      for (k = 0; k < n; ++k) l += exp(x[k] - m);
+      if (sk > -INFINITY) l += exp(sk - m);
+      ls = m + log(l);
+      for (k = 0; k < n; ++k) {
+        double w = exp(x[k] - ls);
+        for (d = 0; d < KV_LORA; ++d) o[d] += w * K[k * ENTRY + d];
+      }
+      lse[(int64_t)t * H + h] = ls;
+    }
+    free(K);
+    free(x);
+  }
+  return bad ? -1 : 0;
+}
+
+/* ------------------------------------------------------------------------------------ */
 /* Paged decode / spec-verify.                                                           */
 /* ------------------------------------------------------------------------------------ */
 
