@@ -218,6 +218,40 @@ MLA_API int mla_sparse_fwd(const void* q, int64_t q_s0, int64_t q_s1, const void
                    int32_t T, int32_t H, cudaStream_t stream);
 
 /*
+ * Sparse forward with the extras of the general sparse_mla_fwd: an attention sink per head, a
+ * second key segment, and a split of each row's key list over several work items.
+ * Follows: "vllm.models.kimi_k3.amd.ops.flydsl_sparse_mla", flydsl_sparse_mla_fp8ds_supported
+ * (the general op's argument list: attn_sink, extra_kv / extra_indptr / extra_indices,
+ * kv_splits), with the semantics of flydsl_sparse_mla_fp8ds_fwd for everything else.  The page
+ * names these three without defining them; this library reads them as:
+ *   - attn_sink  device fp32 [H] or NULL: a logit per head (natural-log units, like
+ *                softmax_scale * q.k) joining the softmax denominator with a zero value:
+ *                lse = ln(sum_k e^{x_k} + e^{sink_h}), out = sum_k e^{x_k - lse} V_k; a row
+ *                without keys gives out = 0 and lse = sink_h.
+ *   - extra_records / extra_indptr / extra_indices  a second pool of fp8_ds_mla records (same
+ *                layout rules as kv_records) with its own CSR lists over T rows: row t attends
+ *                its keys of both segments under one softmax.  All NULL: no second segment.
+ *   - kv_splits  in [1, 64]: each row's key list (of each segment) is cut into kv_splits
+ *                contiguous parts (whole 128-key tiles) computed by separate work items and
+ *                combined by their log-sum-exp; the result equals the unsplit one up to fp32
+ *                rounding.
+ * All other arguments as mla_sparse_fwd.  With kv_splits = 1, no sink and no second segment
+ * this is mla_sparse_fwd (no workspace needed).  Otherwise `workspace` (256-byte aligned, at
+ * least mla_sparse_fwd_ext_workspace_size(...) bytes, contents garbage before and after)
+ * holds the fp32 partials.
+ */
+MLA_API size_t mla_sparse_fwd_ext_workspace_size(int32_t T, int32_t H, int32_t kv_splits, int has_extra,
+                                                 int has_sink);
+MLA_API int mla_sparse_fwd_ext(const void* q, int64_t q_s0, int64_t q_s1, const void* kv_records,
+                               int64_t record_stride_bytes, int64_t num_records, const int32_t* kv_indptr,
+                               const int32_t* kv_indices, int64_t n_indices, const void* extra_records,
+                               int64_t extra_record_stride_bytes, int64_t extra_num_records,
+                               const int32_t* extra_indptr, const int32_t* extra_indices, int64_t n_extra_indices,
+                               const float* attn_sink, int32_t kv_splits, float softmax_scale, int has_invalid,
+                               void* out, int64_t o_s0, int64_t o_s1, float* lse, int32_t T, int32_t H,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Workspace bytes mla_paged_decode needs for this shape (split-K partials).  The split count
  * depends only on (B * q_len, H, max_context, the device's SM count), never on seq_lens, so
  * a graph captured once stays valid.  num_sms <= 0 means "the current device's".

@@ -74,6 +74,10 @@ def lib():
         L.mla_profile_attention_events.restype = None
         L.mla_gather_dequant.argtypes = [vp, i32, i64, i64, i64, i32, vp, i64, vp, vp]
         L.mla_sparse_fwd_staged.argtypes = L.mla_sparse_fwd.argtypes
+        L.mla_sparse_fwd_ext_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        L.mla_sparse_fwd_ext_workspace_size.restype = sz
+        L.mla_sparse_fwd_ext.argtypes = [vp, i64, i64, vp, i64, i64, vp, vp, i64, vp, i64, i64, vp, vp, i64, vp, i32,
+                                         f32, i32, vp, i64, i64, vp, i32, i32, vp, sz, vp]
         L.mla_gather_context.argtypes = [vp, i32, i64, i64, i64, i32, vp, i64, vp, vp, i32, i64, i32, f32, vp, i64, vp]
         L.mla_merge_attn_states.argtypes = [vp, i64, i64, vp, vp, i64, i64, vp, vp, i64, i64, vp, i32, i32, i32, vp]
         L.mla_key_concat_cache_insert.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, vp, i64, vp, vp, i32, i64, i64,
@@ -85,7 +89,7 @@ def lib():
         L.mla_debug_stall_next_decode.restype = None
         for f in ("mla_q_concat_cache_insert", "mla_sparse_fwd", "mla_sparse_fwd_staged", "mla_paged_decode",
                   "mla_gather_dequant", "mla_key_concat_cache_insert", "mla_qkv_quant_cache_fp8_insert",
-                  "mla_gather_context", "mla_merge_attn_states"):
+                  "mla_gather_context", "mla_merge_attn_states", "mla_sparse_fwd_ext"):
             getattr(L, f).restype = ctypes.c_int
         L.mla_read_device_errors.restype = ctypes.c_int
         _lib = L
@@ -282,12 +286,15 @@ def qkv_quant_cache_fp8_insert(q, k_nope, k_pe, kv_c_normed, v, kv_cache, slot_m
 
 
 def sparse_fwd(q, kv_records, kv_indptr, kv_indices, softmax_scale, *, has_invalid=False, out=None,
-               return_lse=False, num_records=None, kernel="gather"):
+               return_lse=False, num_records=None, kernel="gather", attn_sink=None, extra_kv=None, extra_indptr=None,
+               extra_indices=None, kv_splits=1, workspace=None):
     """Sparse forward over fp8_ds_mla records [N, >=656] (uint8).  Returns (out, lse).
 
     kv_indptr / kv_indices may be int32 or int64 (int64 is narrowed on the device, keeping
-    masked and out-of-range ids as such).  kernel="staged" runs the test aid
-    mla_sparse_fwd_staged (the second kernel design) instead of mla_sparse_fwd."""
+    masked and out-of-range ids as such).  attn_sink (fp32 [H]), a second key segment
+    (extra_kv records with extra_indptr / extra_indices) and kv_splits > 1 run
+    mla_sparse_fwd_ext.  kernel="staged" runs the test aid mla_sparse_fwd_staged (the second
+    kernel design) instead of mla_sparse_fwd."""
     dev = _cuda_device(q)
     _need(q, "q", (torch.bfloat16,), dev, ndim=3)
     _need(kv_records, "kv_records", _BYTE_TYPES, dev)
@@ -303,12 +310,43 @@ def sparse_fwd(q, kv_records, kv_indptr, kv_indices, softmax_scale, *, has_inval
         out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
     _need(out, "out", (torch.bfloat16,), dev, ndim=3)
     lse = torch.empty((T, H), dtype=torch.float32, device=dev) if return_lse else None
-    fn = {"gather": lib().mla_sparse_fwd, "staged": lib().mla_sparse_fwd_staged}[kernel]
+    ext = attn_sink is not None or extra_kv is not None or int(kv_splits) != 1
+    if not ext:
+        fn = {"gather": lib().mla_sparse_fwd, "staged": lib().mla_sparse_fwd_staged}[kernel]
+        with torch.cuda.device(dev):
+            _check(fn(
+                _ptr(q), q.stride(0), q.stride(1), _ptr(rec), rec.stride(0) * rec.element_size(), n_rec,
+                _ptr(kv_indptr), _ptr(kv_indices), n_idx, float(softmax_scale), int(bool(has_invalid)),
+                _ptr(out), out.stride(0), out.stride(1), _ptr(lse), T, H, _stream(q)))
+        return out, lse
+    if kernel != "gather":
+        raise ValueError("the sink, second segment and kv_splits are served by the gather kernel only")
+    rec2, n_rec2, n_idx2 = None, 0, 0
+    if extra_kv is not None:
+        _need(extra_kv, "extra_kv", _BYTE_TYPES, dev)
+        rec2 = extra_kv.reshape(-1, extra_kv.shape[-1]) if extra_kv.dim() != 2 else extra_kv
+        n_rec2 = rec2.shape[0]
+        if extra_indptr is None or extra_indices is None or extra_indptr.numel() != T + 1:
+            raise ValueError("extra_kv needs extra_indptr [T + 1] and extra_indices")
+        n_idx2 = extra_indices.numel()
+        extra_indptr = _index_i32(extra_indptr, "extra_indptr", dev, 0, min(n_idx2, _INT32_MAX))
+        extra_indices = _index_i32(extra_indices, "extra_indices", dev, -1, min(n_rec2, _INT32_MAX))
+    if attn_sink is not None:
+        _need(attn_sink, "attn_sink", (torch.float32,), dev, ndim=1, contiguous=True)
+        if attn_sink.numel() != H:
+            raise ValueError(f"attn_sink must have H = {H} entries")
     with torch.cuda.device(dev):
-        _check(fn(
+        need = int(lib().mla_sparse_fwd_ext_workspace_size(T, H, int(kv_splits), int(rec2 is not None),
+                                                          int(attn_sink is not None)))
+        if workspace is None and need > 0:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        _check(lib().mla_sparse_fwd_ext(
             _ptr(q), q.stride(0), q.stride(1), _ptr(rec), rec.stride(0) * rec.element_size(), n_rec,
-            _ptr(kv_indptr), _ptr(kv_indices), n_idx, float(softmax_scale), int(bool(has_invalid)),
-            _ptr(out), out.stride(0), out.stride(1), _ptr(lse), T, H, _stream(q)))
+            _ptr(kv_indptr), _ptr(kv_indices), n_idx, _ptr(rec2), 0 if rec2 is None else rec2.stride(0), n_rec2,
+            _ptr(extra_indptr) if rec2 is not None else None, _ptr(extra_indices) if rec2 is not None else None,
+            n_idx2, _ptr(attn_sink), int(kv_splits), float(softmax_scale), int(bool(has_invalid)), _ptr(out),
+            out.stride(0), out.stride(1), _ptr(lse), T, H, _ptr(workspace),
+            0 if workspace is None else workspace.numel() * workspace.element_size(), _stream(q)))
     return out, lse
 
 

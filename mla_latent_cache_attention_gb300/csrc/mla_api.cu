@@ -577,6 +577,119 @@ extern "C" int mla_sparse_fwd_staged(const void* q, int64_t q_s0, int64_t q_s1, 
                          n_indices, softmax_scale, has_invalid, out, o_s0, o_s1, lse, T, H, stream, true);
 }
 
+// ------------------------------------------------------------------------------------------
+// Sparse forward with the general op's extras.  Every launch of the gather-warp kernel writes
+// fp32 partials (one per split and segment) into the workspace; the LSE merge kernel combines
+// them (and the sink) into out / lse.
+static size_t sparse_ext_partials(int32_t kv_splits, bool has_extra) {
+  return static_cast<size_t>(kv_splits) * (has_extra ? 2 : 1);
+}
+
+extern "C" size_t mla_sparse_fwd_ext_workspace_size(int32_t T, int32_t H, int32_t kv_splits, int has_extra,
+                                                    int has_sink) {
+  if (T <= 0 || H <= 0 || kv_splits < 1) return 0;
+  const size_t S = sparse_ext_partials(kv_splits, has_extra != 0);
+  if (S == 1 && !has_sink) return 0;
+  return workspace_bytes_for(T, H, SplitPlan{static_cast<int>(S < 2 ? 2 : S), 0});
+}
+
+extern "C" int mla_sparse_fwd_ext(const void* q, int64_t q_s0, int64_t q_s1, const void* kv_records,
+                                  int64_t record_stride_bytes, int64_t num_records, const int32_t* kv_indptr,
+                                  const int32_t* kv_indices, int64_t n_indices, const void* extra_records,
+                                  int64_t extra_record_stride_bytes, int64_t extra_num_records,
+                                  const int32_t* extra_indptr, const int32_t* extra_indices, int64_t n_extra_indices,
+                                  const float* attn_sink, int32_t kv_splits, float softmax_scale, int has_invalid,
+                                  void* out, int64_t o_s0, int64_t o_s1, float* lse, int32_t T, int32_t H,
+                                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  const bool has_extra = extra_records != nullptr;
+  if (has_extra != (extra_indptr != nullptr))
+    return fail(MLA_ERR_INVALID, "extra_records and extra_indptr must be given together");
+  if (kv_splits < 1 || kv_splits > 64) return fail(MLA_ERR_UNSUPPORTED, "kv_splits must be in [1, 64], got %d", kv_splits);
+  const size_t S = sparse_ext_partials(kv_splits, has_extra);
+  if (S == 1 && !attn_sink)       // nothing beyond the plain forward
+    return sparse_fwd_impl(q, q_s0, q_s1, kv_records, record_stride_bytes, num_records, kv_indptr, kv_indices,
+                           n_indices, softmax_scale, has_invalid, out, o_s0, o_s1, lse, T, H, stream, false);
+  if (T < 0) return fail(MLA_ERR_INVALID, "T must be >= 0");
+  if (H < 1 || H > 128) return fail(MLA_ERR_UNSUPPORTED, "H must be in [1, 128], got %d", H);
+  if (T == 0) return ok();
+  if (!q || !kv_records || !kv_indptr || !out) return fail(MLA_ERR_INVALID, "a required pointer is NULL");
+  if (n_indices < 0 || n_indices >= (int64_t(1) << 31) || n_extra_indices < 0 || n_extra_indices >= (int64_t(1) << 31))
+    return fail(MLA_ERR_UNSUPPORTED, "index counts must be in [0, 2^31)");
+  if ((n_indices > 0 && !kv_indices) || (has_extra && n_extra_indices > 0 && !extra_indices))
+    return fail(MLA_ERR_INVALID, "an index array is NULL");
+  if (num_records < 1 || (has_extra && extra_num_records < 1)) return fail(MLA_ERR_INVALID, "num_records must be >= 1");
+  if (record_stride_bytes < 656 || record_stride_bytes % 16 || !aligned(kv_records, 16) ||
+      (has_extra && (extra_record_stride_bytes < 656 || extra_record_stride_bytes % 16 || !aligned(extra_records, 16))))
+    return fail(MLA_ERR_INVALID, "records need a 16-byte aligned base and a pitch that is a multiple of 16 (>= 656)");
+  if (!aligned(q, 16) || q_s1 < 576 || q_s1 % 8 || q_s0 % 8 || q_s0 < static_cast<int64_t>(H) * q_s1)
+    return fail(MLA_ERR_INVALID, "q must be 16-byte aligned with strides that are multiples of 8 elements");
+  if (!aligned(out, 2) || o_s1 < 512 || o_s0 < static_cast<int64_t>(H) * o_s1)
+    return fail(MLA_ERR_INVALID, "bad out strides");
+  if (lse && !aligned(lse, 4)) return fail(MLA_ERR_INVALID, "lse must be 4-byte aligned");
+  if (attn_sink && !aligned(attn_sink, 4)) return fail(MLA_ERR_INVALID, "attn_sink must be 4-byte aligned");
+  const size_t need = mla_sparse_fwd_ext_workspace_size(T, H, kv_splits, has_extra ? 1 : 0, attn_sink ? 1 : 0);
+  if (!workspace || workspace_bytes < need)
+    return fail(MLA_ERR_INVALID, "workspace too small: need %zu bytes, got %zu", need, workspace_bytes);
+  if (!aligned(workspace, 256)) return fail(MLA_ERR_INVALID, "workspace must be 256-byte aligned");
+  const int G = (H + 15) / 16;
+  const int64_t items = static_cast<int64_t>(kv_splits) * T * G;
+  if (items >= (int64_t(1) << 31)) return fail(MLA_ERR_UNSUPPORTED, "too many work items");
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  const size_t po = S * static_cast<size_t>(T) * H * kLora * sizeof(float);
+  float* part_o = static_cast<float*>(workspace);
+  float* part_lse = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ((po + 255) & ~size_t(255)));
+  prof_begin(stream);
+  for (int seg = 0; seg < (has_extra ? 2 : 1); ++seg) {
+    DsParams p{};
+    p.q = static_cast<const uint8_t*>(q);
+    p.q_s0b = q_s0 * 2;
+    p.q_s1b = q_s1 * 2;
+    p.H = H;
+    p.q_len = 1;
+    p.B = T;
+    p.G = G;
+    p.cols = H;
+    p.records = static_cast<const uint8_t*>(seg ? extra_records : kv_records);
+    p.rec_stride = seg ? extra_record_stride_bytes : record_stride_bytes;
+    p.num_records = seg ? extra_num_records : num_records;
+    p.indptr = seg ? extra_indptr : kv_indptr;
+    p.indices = seg ? extra_indices : kv_indices;
+    p.has_invalid = has_invalid ? 1 : 0;
+    p.n_splits = kv_splits;
+    p.n_rows = T;
+    p.n_items = static_cast<int>(items);
+    p.sig2 = softmax_scale * 1.4426950408889634f;
+    p.part_o = part_o;
+    p.part_lse = part_lse;
+    p.err = d->err;
+    p.partial = 1;
+    p.split_base = seg * kv_splits;
+    if (launch_ds_sparse(p, grid_for(items, d->sms), stream) != cudaSuccess) {
+      prof_end(stream);
+      return fail(MLA_ERR_CUDA, "sparse attention launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+    }
+  }
+  prof_end(stream);
+  MergeParams m{};
+  m.part_o = part_o;
+  m.part_lse = part_lse;
+  m.S = static_cast<int>(S);
+  m.n_rows = T;
+  m.H = H;
+  m.seq_lens = nullptr;
+  m.q_len = 1;
+  m.chunk = 1;
+  m.out = static_cast<uint8_t*>(out);
+  m.o_s0b = o_s0 * 2;
+  m.o_s1b = o_s1 * 2;
+  m.lse = lse;
+  m.sink = attn_sink;
+  if (launch_merge(m, stream) != cudaSuccess)
+    return fail(MLA_ERR_CUDA, "merge launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  return ok();
+}
+
 extern "C" void mla_debug_stall_next_decode(int32_t wait_us) { g_stall_next_us = wait_us > 0 ? wait_us : 0; }
 
 // ------------------------------------------------------------------------------------------
@@ -688,6 +801,7 @@ extern "C" int mla_paged_decode(const void* q, int64_t q_s0, int64_t q_s1, const
     p.part_lse = part_lse;
     p.sched = sched;
     p.err = d->err;
+    p.partial = sp.n_splits > 1 ? 1 : 0;
     if (sched && cudaMemsetAsync(sched, 0, sizeof(uint32_t), stream) != cudaSuccess)
       return fail(MLA_ERR_CUDA, "scheduler reset failed");
     prof_begin(stream);

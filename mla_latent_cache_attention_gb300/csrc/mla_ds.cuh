@@ -64,6 +64,8 @@ struct DsParams {
   float* part_lse;
   uint32_t* sched;
   uint32_t* err;
+  int partial;                    // write fp32 partials (part_o / part_lse) instead of out / lse
+  int split_base;                 // sparse: partial index of this launch's split 0
 };
 
 template <bool kSparse>
@@ -184,17 +186,22 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
     it.g = item % p.G;
     it.pad = 0;
     if (kSparse) {
-      const int b0 = p.indptr[it.b], b1 = p.indptr[it.b + 1];
-      it.k0 = b0;
-      it.n = max(b1 - b0, 0);
+      // split s of the row: keys [s c, (s + 1) c) of its list, c = ceil(n / n_splits) rounded
+      // up to whole tiles; every split runs (an empty one writes a 0 / -inf partial)
+      const int b0 = p.indptr[it.b], nr = max(p.indptr[it.b + 1] - b0, 0);
+      const int c = p.n_splits > 1 ? ((nr + p.n_splits - 1) / p.n_splits + kTile - 1) / kTile * kTile : nr;
+      const int s0 = min(it.s * c, nr);
+      it.k0 = b0 + s0;
+      it.n = min(c, nr - s0);
       it.L = it.k0 + it.n;
+      it.s += p.split_base;
     } else {
       it.L = max(p.seq_lens[it.b], 0);
       it.k0 = it.s * p.chunk;
       it.n = min(max(it.L - it.k0, 0), p.chunk);
     }
     it.ntiles = (it.n + kTile - 1) / kTile;
-    return it.n > 0 || p.n_splits == 1;
+    return kSparse || it.n > 0 || p.n_splits == 1;
   };
 
   if (warp == 0 && kSparse) {
@@ -773,7 +780,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
       float inv[NQ];
 #pragma unroll
       for (int c = 0; c < NQ; ++c) inv[c] = __shfl_sync(0xFFFFFFFFu, inv_l, c);
-      const bool final_out = (p.n_splits == 1);
+      const bool final_out = !p.partial;
       const int64_t flat0 = static_cast<int64_t>(it.b) * p.q_len * p.H + cgb;
       const int ncol = min(NQ, p.cols - cgb);
       const int qi0 = cgb / p.H, h0 = cgb % p.H;

@@ -75,6 +75,7 @@ struct MergeParams {
   uint8_t* out;            // bf16 rows
   int64_t o_s0b, o_s1b;
   float* lse;              // [n_rows, H] or null
+  const float* sink;       // [H] per-head sink logit joining the denominator, or null
 };
 
 // Chunked-context gather: rows of a chunk's context entries through the block table.

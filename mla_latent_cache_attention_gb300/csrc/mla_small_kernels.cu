@@ -327,8 +327,9 @@ cudaError_t launch_prefill_epilogue(int fmt, const PrefillEpiParams& p, int Tp, 
 // ------------------------------------------------------------------------------------------
 // Split-K merge: out = sum_s exp(lse_s - lse) * O_s, lse = ln sum_s exp(lse_s).  The same
 // combine as vLLM's merge_attn_states ("vllm.models.kimi_k3.nvidia.mla",
-// _forward_prefill_fused) applied across the key splits of one decode row.  One CTA of 128
-// threads per (row, head); each thread owns 4 of the 512 columns.
+// _forward_prefill_fused) applied across the key splits of one decode row, or of one sparse
+// row (with an optional per-head sink logit e^{sink} added to the denominator).  One CTA of
+// 128 threads per (row, head); each thread owns 4 of the 512 columns.
 __global__ void __launch_bounds__(128) mla_merge_kernel(const MergeParams p) {
   // launched as a programmatic dependent of the attention kernel: wait until its grid has
   // finished and its partials are visible (a no-op under an ordinary launch)
@@ -352,7 +353,10 @@ __global__ void __launch_bounds__(128) mla_merge_kernel(const MergeParams p) {
   if (lane == 0) red[0][warp] = m;
   __syncthreads();
   m = fmaxf(fmaxf(red[0][0], red[0][1]), fmaxf(red[0][2], red[0][3]));
-  float ws = 0.f;
+  // a sink logit joins the denominator with a zero value
+  const float sk = p.sink ? p.sink[h] : -CUDART_INF_F;
+  m = fmaxf(m, sk);
+  float ws = (tid == 0 && sk != -CUDART_INF_F) ? expf(sk - m) : 0.f;
   for (int s = tid; s < S; s += 128) {
     const float ls = p.part_lse[s * stride + rh];
     const float w = (m == -CUDART_INF_F || ls == -CUDART_INF_F) ? 0.f : expf(ls - m);
