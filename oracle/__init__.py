@@ -90,6 +90,8 @@ def lib():
             L.orc_sparse_fwd_ext.argtypes = [vp, i64, i64, vp, i64, i64, vp, vp, vp, i64, i64, vp, vp, vp, dbl, i32,
                                              i32, i32, vp, vp]
             L.orc_sparse_fwd_ext.restype = i32
+            L.orc_head_bmm.argtypes = [vp, i64, i64, vp, vp, i64, i32, i32, i32, i32, vp]
+            L.orc_head_bmm.restype = None
             L.orc_ds_tile_exponent.argtypes = [dbl]
             L.orc_ds_tile_exponent.restype = i32
             L.orc_rope_fp32.argtypes = [vp, vp, vp]
@@ -405,3 +407,23 @@ def merge_attn_states(prefix, prefix_lse, suffix, suffix_lse):
     lib().orc_merge_attn_states(_P(prefix), prefix.strides[0] // 2, prefix.strides[1] // 2, _P(pl), _P(suffix),
                                 suffix.strides[0] // 2, suffix.strides[1] // 2, _P(sl), T, H, D, _P(out), _P(lse))
     return out, lse
+
+
+def head_bmm(x, w, gate=None):
+    """y[b, h, f] = sum_k x[b, h, k] w[h, k, f] (times sigmoid(gate[b, h*F + f]) when a gate is
+    given), exact in fp64.  x: uint16 bf16 bits [B, H, K] (last stride 1); w: uint16 [H, K, F];
+    gate: uint16 [B, H*F] (last stride 1) or None.  Returns fp64 [B, H, F]."""
+    x = np.asarray(x)
+    assert x.dtype == np.uint16 and x.strides[2] == 2
+    w = np.ascontiguousarray(w, dtype=np.uint16)
+    B, H, K = x.shape
+    assert w.shape[:2] == (H, K)
+    F = w.shape[2]
+    g = None
+    if gate is not None:
+        g = np.asarray(gate)
+        assert g.dtype == np.uint16 and g.strides[1] == 2 and g.shape == (B, H * F)
+    y = np.zeros((B, H, F), dtype=np.float64)
+    lib().orc_head_bmm(_P(x), x.strides[0] // 2, x.strides[1] // 2, _P(w), _P(g), 0 if g is None else g.strides[0] // 2,
+                       B, H, K, F, _P(y))
+    return y

@@ -28,6 +28,8 @@
  *    key [k_nope | k_pe] per head, q RoPE in place, latent insert) and
  *    fused_mla_qkv_quant_kv_cache_fp8_insert (fp8 q / k / v with separate scales, cache with
  *    its own scale).
+ *  - "vllm.models.kimi_k3.nvidia.mla", _attention / _v_up_proj / forward: BMM1 of the decode
+ *    query with W_UK_T, the W_UV up-projection of the latent output, the sigmoid output gate.
  *  - "vllm.models.kimi_k3.nvidia.mla", _compute_prefill_context / _gather_context_latent (the
  *    chunked context gathered from the paged cache into a dense workspace, up-converted or as
  *    stored) and _forward_prefill_fused (merge_attn_states of prefix and suffix partials).
@@ -746,6 +748,45 @@ void orc_merge_attn_states(const uint16_t* prefix, int64_t p_s0, int64_t p_s1, c
       out_lse[(int64_t)h * T + t] = l;
     }
   free(parts);
+}
+
+/* ------------------------------------------------------------------------------------ */
+/* Absorbed decode around the attention core: the query into latent space (BMM1 with    */
+/* W_UK_T) and the latent output back to the value space (W_UV), with the output gate.   */
+/* ------------------------------------------------------------------------------------ */
+
+/* "vllm.models.kimi_k3.nvidia.mla", _attention (BMM1: ql_nope = q_nope x W_UK_T per head)
+ * and _v_up_proj (out = latent x W_UV per head): for token b and head h,
+ *   y[b, h, f] = sum_k x[b, h, k] * w[h, k, f]
+ * with x bf16 [B, H, K] (element strides x_s0, x_s1), w bf16 [H, K, F] contiguous, y fp64
+ * [B, H, F], computed exactly in fp64.  When g is given (the output gate of forward,
+ * _gate_sigmoid_mul, g bf16 [B, H * F] with row stride g_s0) the result is multiplied by
+ * sigmoid(g[b, h * F + f]) in fp64; the rounding steps of the bf16 pipeline (the product to
+ * bf16, the gate bf16(sigmoid(g)), the gated value to bf16) are left to the comparison's
+ * tolerance. */
+void orc_head_bmm(const uint16_t* x, int64_t x_s0, int64_t x_s1, const uint16_t* w, const uint16_t* g, int64_t g_s0,
+                  int B, int H, int K, int F, double* y) {
+  int b;
+#pragma omp parallel for schedule(static)
+  for (b = 0; b < B; ++b) {
+    int h, k, f;
+    double* acc = (double*)malloc(sizeof(double) * (size_t)F);
+    for (h = 0; h < H; ++h) {
+      const uint16_t* xr = x + (int64_t)b * x_s0 + (int64_t)h * x_s1;
+      for (f = 0; f < F; ++f) acc[f] = 0.0;
+      for (k = 0; k < K; ++k) {
+        const double xv = orc_bf16_to_double(xr[k]);
+        const uint16_t* wr = w + ((int64_t)h * K + k) * F;
+        for (f = 0; f < F; ++f) acc[f] += xv * orc_bf16_to_double(wr[f]);
+      }
+      for (f = 0; f < F; ++f) {
+        double v = acc[f];
+        if (g) v *= 1.0 / (1.0 + exp(-orc_bf16_to_double(g[(int64_t)b * g_s0 + (int64_t)h * F + f])));
+        y[((int64_t)b * H + h) * F + f] = v;
+      }
+    }
+    free(acc);
+  }
 }
 
 /* Exposed for the self-tests: the tile exponent rule and the fp32 rotation. */
