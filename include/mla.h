@@ -373,6 +373,38 @@ MLA_API int mla_merge_attn_states(void* output, int64_t o_s0, int64_t o_s1, floa
                                   int32_t T, int32_t H, int32_t D, cudaStream_t stream);
 
 /*
+ * Absorbed decode query: the per-head BMM1 that takes the NoPE query into the latent space
+ * before the decode epilogue.
+ * Follows: "vllm.models.kimi_k3.nvidia.mla", _attention (BMM1: (N, B, P) x (N, P, L) -> (B, N, L))
+ * and process_weights_after_loading (W_UK_T = the key part of kv_b_proj, [N, P, L]).
+ *   ql_nope[b, h, l] = sum_p q_nope[b, h, p] * w_uk_t[h, p, l]
+ * on the tensor cores (bf16 operands, fp32 accumulation), rounded once to bf16.
+ *
+ *   q_nope   device bf16 [B, H, P], element strides (qn_s0, qn_s1), unit innermost stride
+ *            (e.g. the first P values of a [B, H, P + 64] query); P in 64..512, a multiple of 64.
+ *   w_uk_t   device bf16 [H, P, 512] contiguous, 16-byte aligned.
+ *   ql_nope  device out bf16 [B, H, 512], element strides (ql_s0, ql_s1).
+ */
+MLA_API int mla_absorb_q(const void* q_nope, int64_t qn_s0, int64_t qn_s1, const void* w_uk_t, void* ql_nope,
+                         int64_t ql_s0, int64_t ql_s1, int32_t B, int32_t H, int32_t P, cudaStream_t stream);
+
+/*
+ * Value up-projection of the latent attention output, with the optional output gate.
+ * Follows: "vllm.models.kimi_k3.nvidia.mla", _v_up_proj ((N, B, L) x (N, L, V) -> (B, N, V))
+ * and forward (_gate_sigmoid_mul of the output with the g_proj gate).
+ *   y[b, h, v] = bf16(sum_l latent[b, h, l] * w_uv[h, l, v])      (fp32 accumulation)
+ *   out[b, h, v] = gate ? bf16(y * bf16(sigmoid(gate[b, h * V + v]))) : y
+ *
+ *   latent   device bf16 [B, H, 512], element strides (l_s0, l_s1).
+ *   w_uv     device bf16 [H, 512, V] contiguous, 16-byte aligned; V a multiple of 128.
+ *   gate     device bf16 [B, H * V] gate pre-activations (row stride g_s0), or NULL.
+ *   out      device out bf16 [B, H, V], element strides (o_s0, o_s1) (e.g. [B, H * V]).
+ */
+MLA_API int mla_v_up_proj(const void* latent, int64_t l_s0, int64_t l_s1, const void* w_uv, const void* gate,
+                          int64_t g_s0, void* out, int64_t o_s0, int64_t o_s1, int32_t B, int32_t H, int32_t V,
+                          cudaStream_t stream);
+
+/*
  * Gather-and-dequantise (test and debugging aid): out[i, 0..575] = the exact fp32 values of
  * the entry at slots[i] (paged addressing as in mla_paged_decode; NoPE times its tile scale
  * for DS_MLA, raw E4M3 values for FP8).  Same record addressing and decode as the attention

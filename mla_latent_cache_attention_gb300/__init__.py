@@ -15,6 +15,8 @@ Entry points (same names as the C ABI, without the ``mla_`` prefix):
                          own scales, latent insert with the cache scale
   sparse_fwd             sparse CSR forward over 656-byte fp8_ds_mla records
   paged_decode           paged decode / spec-verify (split-K + LSE merge)
+  absorb_q               BMM1: q_nope . W_UK_T per head -> ql_nope (latent query)
+  v_up_proj              latent output . W_UV per head (+ sigmoid output gate)
   gather_context         chunked-context gather of paged entries (bf16 values or stored bytes)
   merge_attn_states      prefix / suffix merge of partial attentions by their LSEs
   gather_dequant         paged entries -> exact fp32 values (test aid)
@@ -78,6 +80,8 @@ def lib():
         L.mla_sparse_fwd_ext_workspace_size.restype = sz
         L.mla_sparse_fwd_ext.argtypes = [vp, i64, i64, vp, i64, i64, vp, vp, i64, vp, i64, i64, vp, vp, i64, vp, i32,
                                          f32, i32, vp, i64, i64, vp, i32, i32, vp, sz, vp]
+        L.mla_absorb_q.argtypes = [vp, i64, i64, vp, vp, i64, i64, i32, i32, i32, vp]
+        L.mla_v_up_proj.argtypes = [vp, i64, i64, vp, vp, i64, vp, i64, i64, i32, i32, i32, vp]
         L.mla_gather_context.argtypes = [vp, i32, i64, i64, i64, i32, vp, i64, vp, vp, i32, i64, i32, f32, vp, i64, vp]
         L.mla_merge_attn_states.argtypes = [vp, i64, i64, vp, vp, i64, i64, vp, vp, i64, i64, vp, i32, i32, i32, vp]
         L.mla_key_concat_cache_insert.argtypes = [vp, i64, i64, vp, i64, i64, vp, i64, vp, i64, vp, vp, i32, i64, i64,
@@ -89,7 +93,8 @@ def lib():
         L.mla_debug_stall_next_decode.restype = None
         for f in ("mla_q_concat_cache_insert", "mla_sparse_fwd", "mla_sparse_fwd_staged", "mla_paged_decode",
                   "mla_gather_dequant", "mla_key_concat_cache_insert", "mla_qkv_quant_cache_fp8_insert",
-                  "mla_gather_context", "mla_merge_attn_states", "mla_sparse_fwd_ext"):
+                  "mla_gather_context", "mla_merge_attn_states", "mla_sparse_fwd_ext", "mla_absorb_q",
+                  "mla_v_up_proj"):
             getattr(L, f).restype = ctypes.c_int
         L.mla_read_device_errors.restype = ctypes.c_int
         _lib = L
@@ -386,6 +391,49 @@ def paged_decode(q, kv_cache, block_table, seq_lens, *, fmt, q_len=1, max_contex
             _ptr(lse), _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size(),
             _stream(q)))
     return out, lse
+
+
+def absorb_q(q_nope, w_uk_t, *, ql_nope=None):
+    """BMM1: ql_nope[b, h] = q_nope[b, h] . w_uk_t[h]; q_nope bf16 [B, H, P] (unit innermost
+    stride), w_uk_t bf16 [H, P, 512].  Returns ql_nope [B, H, 512] bf16."""
+    dev = _cuda_device(q_nope)
+    _need(q_nope, "q_nope", (torch.bfloat16,), dev, ndim=3)
+    _need(w_uk_t, "w_uk_t", (torch.bfloat16,), dev, ndim=3, contiguous=True)
+    B, H, P = q_nope.shape
+    if tuple(w_uk_t.shape) != (H, P, 512):
+        raise ValueError(f"w_uk_t must be [H, P, 512] = {(H, P, 512)}, got {tuple(w_uk_t.shape)}")
+    if ql_nope is None:
+        ql_nope = torch.empty((B, H, 512), dtype=torch.bfloat16, device=dev)
+    _need(ql_nope, "ql_nope", (torch.bfloat16,), dev, ndim=3)
+    with torch.cuda.device(dev):
+        _check(lib().mla_absorb_q(_ptr(q_nope), q_nope.stride(0), q_nope.stride(1), _ptr(w_uk_t), _ptr(ql_nope),
+                                  ql_nope.stride(0), ql_nope.stride(1), B, H, P, _stream(q_nope)))
+    return ql_nope
+
+
+def v_up_proj(latent, w_uv, gate=None, *, out=None):
+    """out[b, h] = latent[b, h] . w_uv[h] (times bf16(sigmoid(gate[b, h*V:(h+1)*V])) when a
+    gate is given); latent bf16 [B, H, 512], w_uv bf16 [H, 512, V], gate bf16 [B, H * V].
+    Returns out [B, H, V] bf16."""
+    dev = _cuda_device(latent)
+    _need(latent, "latent", (torch.bfloat16,), dev, ndim=3)
+    _need(w_uv, "w_uv", (torch.bfloat16,), dev, ndim=3, contiguous=True)
+    B, H, L = latent.shape
+    if L != 512 or w_uv.shape[0] != H or w_uv.shape[1] != 512:
+        raise ValueError("latent must be [B, H, 512] and w_uv [H, 512, V]")
+    V = w_uv.shape[2]
+    if gate is not None:
+        _need(gate, "gate", (torch.bfloat16,), dev, ndim=2)
+        if tuple(gate.shape) != (B, H * V):
+            raise ValueError(f"gate must be [B, H * V] = {(B, H * V)}")
+    if out is None:
+        out = torch.empty((B, H, V), dtype=torch.bfloat16, device=dev)
+    _need(out, "out", (torch.bfloat16,), dev, ndim=3)
+    with torch.cuda.device(dev):
+        _check(lib().mla_v_up_proj(_ptr(latent), latent.stride(0), latent.stride(1), _ptr(w_uv), _ptr(gate),
+                                   0 if gate is None else gate.stride(0), _ptr(out), out.stride(0), out.stride(1), B, H,
+                                   V, _stream(latent)))
+    return out
 
 
 def gather_context(kv_cache, block_table, cu_seq_lens, seq_starts=None, *, fmt, num_tokens, raw=False,

@@ -19,7 +19,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmla.so")
 
 SOURCES = ["mla_api.cu", "mla_small_kernels.cu", "mla_attn_bf16.cu", "mla_attn_fp8.cu", "mla_attn_ds.cu",
-           "mla_noalloc.cu", "mla_paged_tma_bf16.cu", "mla_paged_tma_fp8.cu", "mla_ds.cu"]
+           "mla_noalloc.cu", "mla_paged_tma_bf16.cu", "mla_paged_tma_fp8.cu", "mla_ds.cu", "mla_head_bmm.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

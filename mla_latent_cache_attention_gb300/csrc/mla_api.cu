@@ -1071,3 +1071,53 @@ extern "C" int mla_merge_attn_states(void* output, int64_t o_s0, int64_t o_s1, f
     return fail(MLA_ERR_CUDA, "merge launch failed: %s", cudaGetErrorString(cudaGetLastError()));
   return ok();
 }
+
+// ------------------------------------------------------------------------------------------
+// Per-head contractions around the attention core.
+static int head_bmm(const void* x, int64_t x_s0, int64_t x_s1, const void* w, const void* gate, int64_t g_s0, void* y,
+                    int64_t y_s0, int64_t y_s1, int32_t B, int32_t H, int32_t K, int32_t F, cudaStream_t stream) {
+  if (B < 0 || H < 1) return fail(MLA_ERR_INVALID, "bad shape B=%d H=%d", B, H);
+  if (K < 64 || K > 512 || K % 64) return fail(MLA_ERR_UNSUPPORTED, "the contraction length must be 64..512 in steps of 64, got %d", K);
+  if (F < 128 || F % 128) return fail(MLA_ERR_UNSUPPORTED, "the output width must be a multiple of 128, got %d", F);
+  if (B == 0) return ok();
+  if (!x || !w || !y) return fail(MLA_ERR_INVALID, "a required pointer is NULL");
+  if (x_s1 < K || x_s0 < static_cast<int64_t>(H) * x_s1 || y_s1 < F || y_s0 < static_cast<int64_t>(H) * y_s1 ||
+      (gate && g_s0 < static_cast<int64_t>(H) * F))
+    return fail(MLA_ERR_INVALID, "strides overlap rows");
+  if (!aligned(w, 16) || !aligned(x, 2) || !aligned(y, 2) || (gate && !aligned(gate, 2)))
+    return fail(MLA_ERR_INVALID, "the weights must be 16-byte aligned, bf16 tensors 2-byte aligned");
+  if (static_cast<int64_t>(H) > 65535 || (static_cast<int64_t>(B) + 63) / 64 > 65535)
+    return fail(MLA_ERR_UNSUPPORTED, "grid too large");
+  DevInfo* d = nullptr;
+  if (int rc = dev_info(&d)) return rc;
+  HeadBmmParams p{};
+  p.x = static_cast<const uint16_t*>(x);
+  p.x_s0 = x_s0;
+  p.x_s1 = x_s1;
+  p.w = static_cast<const uint16_t*>(w);
+  p.gate = static_cast<const uint16_t*>(gate);
+  p.g_s0 = g_s0;
+  p.y = static_cast<uint16_t*>(y);
+  p.y_s0 = y_s0;
+  p.y_s1 = y_s1;
+  p.B = B;
+  p.H = H;
+  p.K = K;
+  p.F = F;
+  p.vec = aligned(x, 16) && x_s0 % 8 == 0 && x_s1 % 8 == 0;
+  p.err = d->err;
+  if (launch_head_bmm(p, stream) != cudaSuccess)
+    return fail(MLA_ERR_CUDA, "per-head contraction launch failed: %s", cudaGetErrorString(cudaGetLastError()));
+  return ok();
+}
+
+extern "C" int mla_absorb_q(const void* q_nope, int64_t qn_s0, int64_t qn_s1, const void* w_uk_t, void* ql_nope,
+                            int64_t ql_s0, int64_t ql_s1, int32_t B, int32_t H, int32_t P, cudaStream_t stream) {
+  return head_bmm(q_nope, qn_s0, qn_s1, w_uk_t, nullptr, 0, ql_nope, ql_s0, ql_s1, B, H, P, kLora, stream);
+}
+
+extern "C" int mla_v_up_proj(const void* latent, int64_t l_s0, int64_t l_s1, const void* w_uv, const void* gate,
+                             int64_t g_s0, void* out, int64_t o_s0, int64_t o_s1, int32_t B, int32_t H, int32_t V,
+                             cudaStream_t stream) {
+  return head_bmm(latent, l_s0, l_s1, w_uv, gate, g_s0, out, o_s0, o_s1, B, H, kLora, V, stream);
+}

@@ -111,6 +111,21 @@ struct MergeStatesParams {
   int vec;                 // rows 16-byte aligned, D a multiple of 8
 };
 
+// Per-head contraction y[b, h, :] = x[b, h, :K] . w[h] (w bf16 [H, K, F] contiguous), bf16
+// out, optional sigmoid gate (bf16 [B, H * F] pre-activation).
+struct HeadBmmParams {
+  const uint16_t* x;
+  int64_t x_s0, x_s1;
+  const uint16_t* w;
+  const uint16_t* gate;
+  int64_t g_s0;
+  uint16_t* y;
+  int64_t y_s0, y_s1;
+  int B, H, K, F;
+  int vec;                 // x rows 16-byte aligned
+  uint32_t* err;
+};
+
 struct GatherParams {
   const uint8_t* cache;
   int64_t num_blocks, block_stride, entry_stride;
@@ -132,6 +147,8 @@ cudaError_t launch_gather(int fmt, const GatherParams& p, cudaStream_t stream);
 // kind 0: bf16 values, 1: stored bytes
 cudaError_t launch_gather_context(int fmt, int kind, const GatherCtxParams& p, cudaStream_t stream);
 cudaError_t launch_merge_states(const MergeStatesParams& p, cudaStream_t stream);
+// K a multiple of 64 in [64, 512], F a multiple of 128
+cudaError_t launch_head_bmm(const HeadBmmParams& p, cudaStream_t stream);
 
 // Attention launchers (one translation unit per cache format).  `grid` CTAs, each looping
 // over work items; dynamic shared memory is set up on first use per device.
