@@ -15,7 +15,10 @@ end-to-end figure and CPU-oracle baseline:
 
 Metric: achieved GB/s of algorithmic bytes (entries gathered + query read + output written
 (+ lse)), with query-rows/s beside it.  Timing: CUDA events per step after warm-up, L2
-flushed (256 MiB write) between steps outside the timed events; max over ranks.  The
+flushed (256 MiB write) between steps outside the timed events; max over ranks.  A step's
+launches are captured once into a CUDA graph and replayed per timed step (the serving
+pattern: no host marshalling between the step's kernels); the attention kernel's own time
+(roofline) comes from per-launch events around ordinary calls.  The
 headline times exactly --steps steps; each per-config entry times at least --steps steps and
 at least --min-ms of GPU time (so that clock samples land under load).
 `--impl reference` times the fp64 CPU oracle on a bounded sample of the same workload.
@@ -273,6 +276,41 @@ def job_rate(world: int, units_per_rank: float, steps: int, total_ms: float) -> 
     return world * units_per_rank * steps / (total_ms * 1e-3)
 
 
+def capture_step(r, torch):
+    """The step's launches captured once into a CUDA graph (replayed per timed step, so that
+    the host's per-call marshalling does not leave the GPU idle between the step's kernels);
+    None if capture is not possible."""
+    try:
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            r.step()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            r.step()
+        torch.cuda.synchronize()
+        return g
+    except Exception:
+        torch.cuda.synchronize()
+        return None
+
+
+def graph_steps(g, flush, steps, torch):
+    """`steps` replays of the captured step, each bracketed by CUDA events, L2 flushed before
+    each outside the events.  Returns the step times in ms."""
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.fill_(i & 255)
+        ev[i][0].record()
+        g.replay()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
 def timed_steps(r, flush, steps, torch, prof=True):
     """`steps` steps, each bracketed by CUDA events on the current stream (the attention launch
     by the library's profiling hook), L2 flushed before each step outside the events.
@@ -331,10 +369,20 @@ def measure(w: Work, dev, flush, steps: int, warmup: int, min_ms: float, dist, w
     if min_ms > 0:
         probe, _ = timed_steps(r, flush, 2, torch, prof=False)
         K = max(steps, int(np.ceil(min_ms / max(min(probe), 1e-3))))
+    graph = capture_step(r, torch)
+    if graph is not None:
+        for _ in range(2):
+            graph.replay()
+    assert m.read_device_errors() == 0, f"device error word set during the graph capture of {w.name}"
+    # the attention kernel's own time: per-launch events of ordinary calls
+    _, attn_ms = timed_steps(r, flush, K, torch)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
-    step_ms, attn_ms = timed_steps(r, flush, K, torch)
+    if graph is not None:
+        step_ms = graph_steps(graph, flush, K, torch)
+    else:
+        step_ms, _ = timed_steps(r, flush, K, torch, prof=False)
     total_ms = float(sum(step_ms))
     e2e_ms = e2e_steps(r, flush, K, torch)
     assert m.read_device_errors() == 0, f"device error word set during the timed steps of {w.name}"
@@ -356,8 +404,9 @@ def measure(w: Work, dev, flush, steps: int, warmup: int, min_ms: float, dist, w
                 "h2d_bytes_per_step": int(r.h2d), "d2h_bytes_per_step": int(r.d2h)},
         "gpu_launches": int(r.launches_per_step * K),
         "dtype": w.dtype,
-        "config": dict(w.cfg),
+        "config": dict(w.cfg, step_launch="cuda graph replay" if graph is not None else "direct calls"),
     }
+    del graph
     del r
     torch.cuda.empty_cache()
     if cpu_seconds > 0:
@@ -408,7 +457,7 @@ def run_native(args, rank, world, dist):
         "metric": METRIC, "value": head["value"], "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded numpy)",
-        "config": dict(w.cfg, l2="flushed between steps (256 MiB write, outside the timed events)",
+        "config": dict(head["config"], l2="flushed between steps (256 MiB write, outside the timed events)",
                        parallelism="replicas" if world > 1 else "single GPU",
                        config_index_reading="BASELINE configs 2-4 read 0-based: sparse prefill, fp8 spec-verify, "
                                             "ds_mla H=96 decode"),
