@@ -21,6 +21,10 @@ pattern: no host marshalling between the step's kernels); the attention kernel's
 (roofline) comes from per-launch events around ordinary calls.  The
 headline times exactly --steps steps; each per-config entry times at least --steps steps and
 at least --min-ms of GPU time (so that clock samples land under load).
+The "e2e" figure goes through the public API with the step's inputs copied from pinned
+host memory and its results copied back inside the timed region: the sparse prefill streams
+its rows in four chunks (kv_indptr slices) so that copies overlap the kernel; the paged
+workloads replay one CUDA graph of the copies and calls ("e2e.mode" says which).
 `--impl reference` times the fp64 CPU oracle on a bounded sample of the same workload.
 Multi-GPU (torchrun): every rank runs an independent replica ("replicas only").
 """
@@ -165,7 +169,7 @@ class GpuRunner:
         m, w, c = self.m, self.w, self.w.case
         if w.kind == "sparse":
             m.sparse_fwd(self.q, self.rec, self.indptr, self.indices, c.softmax_scale, has_invalid=True,
-                         out=self.out, return_lse=True)
+                         out=self.out, return_lse=True, lse=self.lse)
             return
         q = self.q
         if w.name == "decode_bf16_epilogue":
@@ -173,7 +177,7 @@ class GpuRunner:
                                         fmt=c.fmt, positions=self.pos, cos_sin_cache=self.cs, mqa_q=self.q)
         m.paged_decode(q, self.cache, self.bt, self.sl, fmt=c.fmt, q_len=c.q_len, max_context=c.max_context,
                        softmax_scale=c.softmax_scale, q_scale=c.q_scale, k_scale=c.k_scale, out=self.out,
-                       return_lse=c.return_lse, workspace=self.ws)
+                       return_lse=c.return_lse, workspace=self.ws, lse=self.lse if c.return_lse else None)
 
     # ---- end-to-end: the per-step inputs come from pinned host memory, the result goes back
     def e2e_setup(self):
@@ -202,13 +206,73 @@ class GpuRunner:
             self.d2h += self.h_lse.numel() * 4
         self.ret_lse = ret_lse
 
-    def e2e_step(self):
+        # the sparse prefill streams its rows in chunks: the copies of chunk i + 1 and the
+        # results of chunk i - 1 move while chunk i computes (a kv_indptr slice addresses the
+        # same kv_indices); the small paged steps replay a CUDA graph of the API calls and copies
+        torch = self.torch
+        self.copy_s, self.d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+        self.e2e_graph = None
+        if w.kind == "sparse":
+            self.e2e_mode = "row chunks pipelined over copy / compute / copy-back streams"
+            self.h_ptr = c.indptr.astype(np.int64)
+            T = c.q.shape[0]
+            self.bounds = [T * i // self.E2E_CHUNKS for i in range(self.E2E_CHUNKS + 1)]
+            return
+        try:
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                self.e2e_direct()
+            torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.e2e_direct()
+            torch.cuda.synchronize()
+            self.e2e_graph = g
+            self.e2e_mode = "CUDA graph of the API calls with their input copies and result copies"
+        except Exception:
+            torch.cuda.synchronize()
+            self.e2e_mode = "direct API calls"
+
+    E2E_CHUNKS = 4
+
+    def e2e_direct(self):
         for h, d in self.h_in:
             d.copy_(h, non_blocking=True)
         self.step()
         self.h_out.copy_(self.out, non_blocking=True)
         if self.ret_lse:
             self.h_lse.copy_(self.lse, non_blocking=True)
+
+    def e2e_step(self):
+        torch, m, c = self.torch, self.m, self.w.case
+        if self.e2e_graph is not None:
+            self.e2e_graph.replay()
+            return
+        if self.w.kind != "sparse":
+            self.e2e_direct()
+            return
+        cur = torch.cuda.current_stream()
+        (hq, _), (hptr, _), (hidx, _) = self.h_in
+        self.copy_s.wait_stream(cur)
+        self.d2h_s.wait_stream(cur)
+        with torch.cuda.stream(self.copy_s):
+            self.indptr.copy_(hptr, non_blocking=True)
+        for i in range(self.E2E_CHUNKS):
+            r0, r1 = self.bounds[i], self.bounds[i + 1]
+            k0, k1 = int(self.h_ptr[r0]), int(self.h_ptr[r1])
+            with torch.cuda.stream(self.copy_s):
+                self.q[r0:r1].copy_(hq[r0:r1], non_blocking=True)
+                self.indices[k0:k1].copy_(hidx[k0:k1], non_blocking=True)
+            cur.wait_stream(self.copy_s)
+            m.sparse_fwd(self.q[r0:r1], self.rec, self.indptr[r0:r1 + 1], self.indices, c.softmax_scale,
+                         has_invalid=True, out=self.out[r0:r1], return_lse=True, lse=self.lse[r0:r1])
+            self.d2h_s.wait_stream(cur)
+            with torch.cuda.stream(self.d2h_s):
+                self.h_out[r0:r1].copy_(self.out[r0:r1], non_blocking=True)
+                self.h_lse[r0:r1].copy_(self.lse[r0:r1], non_blocking=True)
+        cur.wait_stream(self.d2h_s)
 
 
 class ClockSampler:
@@ -401,7 +465,7 @@ def measure(w: Work, dev, flush, steps: int, warmup: int, min_ms: float, dist, w
                      "kernel_ms": round(attn_avg, 5), "kernel_ms_min": round(float(np.min(attn_ms)), 5),
                      "bytes_per_launch": w.attn_bytes},
         "e2e": {"value": round(job_rate(world, w.step_bytes, K, e2e_ms) / 1e9, 2), "unit": "GB/s",
-                "h2d_bytes_per_step": int(r.h2d), "d2h_bytes_per_step": int(r.d2h)},
+                "h2d_bytes_per_step": int(r.h2d), "d2h_bytes_per_step": int(r.d2h), "mode": r.e2e_mode},
         "gpu_launches": int(r.launches_per_step * K),
         "dtype": w.dtype,
         "config": dict(w.cfg, step_launch="cuda graph replay" if graph is not None else "direct calls"),

@@ -292,7 +292,7 @@ def qkv_quant_cache_fp8_insert(q, k_nope, k_pe, kv_c_normed, v, kv_cache, slot_m
 
 def sparse_fwd(q, kv_records, kv_indptr, kv_indices, softmax_scale, *, has_invalid=False, out=None,
                return_lse=False, num_records=None, kernel="gather", attn_sink=None, extra_kv=None, extra_indptr=None,
-               extra_indices=None, kv_splits=1, workspace=None):
+               extra_indices=None, kv_splits=1, workspace=None, lse=None):
     """Sparse forward over fp8_ds_mla records [N, >=656] (uint8).  Returns (out, lse).
 
     kv_indptr / kv_indices may be int32 or int64 (int64 is narrowed on the device, keeping
@@ -314,7 +314,12 @@ def sparse_fwd(q, kv_records, kv_indptr, kv_indices, softmax_scale, *, has_inval
     if out is None:
         out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=dev)
     _need(out, "out", (torch.bfloat16,), dev, ndim=3)
-    lse = torch.empty((T, H), dtype=torch.float32, device=dev) if return_lse else None
+    if return_lse and lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _need(lse, "lse", (torch.float32,), dev, ndim=2, contiguous=True)
+        if tuple(lse.shape) != (T, H):
+            raise ValueError(f"lse must be [T, H] = {(T, H)}")
     ext = attn_sink is not None or extra_kv is not None or int(kv_splits) != 1
     if not ext:
         fn = {"gather": lib().mla_sparse_fwd, "staged": lib().mla_sparse_fwd_staged}[kernel]
@@ -360,7 +365,7 @@ def paged_decode_workspace_size(B, q_len, H, max_context, num_sms=0) -> int:
 
 
 def paged_decode(q, kv_cache, block_table, seq_lens, *, fmt, q_len=1, max_context, softmax_scale,
-                 q_scale=1.0, k_scale=1.0, out=None, return_lse=False, workspace=None):
+                 q_scale=1.0, k_scale=1.0, out=None, return_lse=False, workspace=None, lse=None):
     """Paged decode / spec-verify.  q [B*q_len, H, 576] (bf16, or uint8 E4M3 codes for fp8).
     Returns (out [B*q_len, H, 512] bf16, lse or None)."""
     fmt = _fmt(fmt)
@@ -376,7 +381,12 @@ def paged_decode(q, kv_cache, block_table, seq_lens, *, fmt, q_len=1, max_contex
     if out is None:
         out = torch.empty((rows, H, 512), dtype=torch.bfloat16, device=dev)
     _need(out, "out", (torch.bfloat16,), dev, ndim=3)
-    lse = torch.empty((rows, H), dtype=torch.float32, device=dev) if return_lse else None
+    if return_lse and lse is None:
+        lse = torch.empty((rows, H), dtype=torch.float32, device=dev)
+    if lse is not None:
+        _need(lse, "lse", (torch.float32,), dev, ndim=2, contiguous=True)
+        if tuple(lse.shape) != (rows, H):
+            raise ValueError(f"lse must be [B * q_len, H] = {(rows, H)}")
     with torch.cuda.device(dev):
         need = paged_decode_workspace_size(B, q_len, H, max_context)
         if workspace is None and need > 0:

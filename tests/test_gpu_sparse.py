@@ -200,3 +200,26 @@ def test_config2_full_size_all_rows(m, kern):
     assert_attn_close(o, ro, "config2")
     assert_lse_close(l, rl, "config2")
     assert m.read_device_errors() == 0
+
+
+def test_row_chunks_through_indptr_slices(m, kern):
+    """Rows served in chunks, each call given a slice of kv_indptr (first offset non-zero)
+    over the whole kv_indices and slices of out / lse, give the full call's result bit for
+    bit; chunks run on a second stream."""
+    c = synth.sparse_case(37, T=11, H=16, N=900, per_row=300, p_invalid=0.1, replace=True, ragged=True)
+    q, rec, ptr, idx = t_bf16(c.q), t_u8(c.records), t_i32(c.indptr), t_i32(c.indices)
+    o_full, l_full = m.sparse_fwd(q, rec, ptr, idx, c.softmax_scale, has_invalid=True, return_lse=True, kernel=kern)
+    out = torch.full_like(o_full, 3.0)
+    lse = torch.full_like(l_full, 5.0)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for r0, r1 in [(0, 3), (3, 4), (4, 10), (10, 11)]:
+            m.sparse_fwd(q[r0:r1], rec, ptr[r0:r1 + 1], idx, c.softmax_scale, has_invalid=True,
+                         out=out[r0:r1], return_lse=True, lse=lse[r0:r1], kernel=kern)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    assert torch.equal(out, o_full) and torch.equal(lse, l_full)
+    ro, rl = oracle.sparse_fwd(c.q, c.records, c.indptr, c.indices, c.softmax_scale, True)
+    assert_attn_close(out, ro, "row chunks")
+    assert_lse_close(lse, rl, "row chunks")
