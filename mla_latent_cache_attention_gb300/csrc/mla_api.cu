@@ -802,8 +802,8 @@ extern "C" int mla_paged_decode(const void* q, int64_t q_s0, int64_t q_s1, const
     p.sched = sched;
     p.err = d->err;
     p.partial = sp.n_splits > 1 ? 1 : 0;
-    if (sched && cudaMemsetAsync(sched, 0, sizeof(uint32_t), stream) != cudaSuccess)
-      return fail(MLA_ERR_CUDA, "scheduler reset failed");
+    if (sched && launch_sched_reset(sched, stream) != cudaSuccess)
+      return fail(MLA_ERR_CUDA, "scheduler reset failed: %s", cudaGetErrorString(cudaGetLastError()));
     prof_begin(stream);
     const cudaError_t e = launch_ds_paged(p, &tkv, &tsc, grid_for(items, d->sms), stream);
     prof_end(stream);
@@ -883,8 +883,8 @@ extern "C" int mla_paged_decode(const void* q, int64_t q_s0, int64_t q_s1, const
     p.wait_us = g_stall_next_us;
     p.stall = g_stall_next_us > 0 ? 1 : 0;
     g_stall_next_us = 0;
-    if (sched && cudaMemsetAsync(sched, 0, sizeof(uint32_t), stream) != cudaSuccess)
-      return fail(MLA_ERR_CUDA, "scheduler reset failed");
+    if (sched && launch_sched_reset(sched, stream) != cudaSuccess)
+      return fail(MLA_ERR_CUDA, "scheduler reset failed: %s", cudaGetErrorString(cudaGetLastError()));
     const int grid = grid_for(items, d->sms);
     prof_begin(stream);
     e = fmt == MLA_CACHE_BF16 ? launch_paged_tma_bf16(cp.nq, p, &tkv, &tq, grid, stream)

@@ -424,6 +424,10 @@ __global__ void __launch_bounds__(kThreads, 1) mla_attn_kernel(const __grid_cons
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // launched as a programmatic dependent of the previous kernel in the stream: the setup above
+  // overlaps that kernel's tail, and its writes (a decode epilogue's query and cache entry, the
+  // scheduler reset) are visible past this wait
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == 0) {
     // ------------------------------------------------------------------ producer

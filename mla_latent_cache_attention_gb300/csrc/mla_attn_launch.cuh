@@ -18,8 +18,7 @@ cudaError_t launch_attn(const AttnParams& p, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  mla_attn_kernel<F, kSparse><<<grid, kThreads, Smem<F>::kAlloc, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(mla_attn_kernel<F, kSparse>, dim3(grid), dim3(kThreads), Smem<F>::kAlloc, stream, p);
 }
 
 }  // namespace mla

@@ -21,8 +21,7 @@ cudaError_t launch_t(const DsParams& p, const void* tkv, const void* tsc, int gr
   CUtensorMap dummy{};
   const CUtensorMap& a = tkv ? *static_cast<const CUtensorMap*>(tkv) : dummy;
   const CUtensorMap& b = tsc ? *static_cast<const CUtensorMap*>(tsc) : dummy;
-  mla_ds_kernel<kSparse><<<grid, C::kThreads, C::kAlloc, stream>>>(p, a, b);
-  return cudaGetLastError();
+  return launch_pdl(mla_ds_kernel<kSparse>, dim3(grid), dim3(C::kThreads), C::kAlloc, stream, p, a, b);
 }
 
 }  // namespace

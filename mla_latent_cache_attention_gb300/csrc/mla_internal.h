@@ -2,9 +2,30 @@
 // units (not part of the public C ABI).
 #pragma once
 #include <cstdint>
+#include <utility>
 #include <cuda_runtime.h>
 
 namespace mla {
+
+// Launch as a programmatic dependent of the previous kernel in the stream: the grid may be
+// scheduled while that kernel finishes, so the kernel must execute griddepcontrol.wait before
+// it touches memory that the earlier work writes (after a non-kernel operation, or a kernel
+// that never triggers, this is an ordinary launch).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 struct AttnParams;
 
@@ -143,6 +164,7 @@ cudaError_t launch_epilogue(int fmt, const EpiParams& p, int B, cudaStream_t str
 // fmt 0 / 2: key concat for the bf16 / fp8_ds_mla cache; fmt 1: fp8 q / k / v quant.
 cudaError_t launch_prefill_epilogue(int fmt, const PrefillEpiParams& p, int Tp, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream);
+cudaError_t launch_sched_reset(uint32_t* sched, cudaStream_t stream);
 cudaError_t launch_gather(int fmt, const GatherParams& p, cudaStream_t stream);
 // kind 0: bf16 values, 1: stored bytes
 cudaError_t launch_gather_context(int fmt, int kind, const GatherCtxParams& p, cudaStream_t stream);

@@ -18,9 +18,8 @@ cudaError_t launch_nq(const PagedParams& p, const void* tkv, const void* tq, int
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
-  mla_paged_tma_kernel<kFP8, NQ><<<grid, C::kThreads, C::kAlloc, stream>>>(
-      p, *static_cast<const CUtensorMap*>(tkv), *static_cast<const CUtensorMap*>(tq));
-  return cudaGetLastError();
+  return launch_pdl(mla_paged_tma_kernel<kFP8, NQ>, dim3(grid), dim3(C::kThreads), C::kAlloc, stream, p,
+                    *static_cast<const CUtensorMap*>(tkv), *static_cast<const CUtensorMap*>(tq));
 }
 
 }  // namespace

@@ -105,6 +105,9 @@ __device__ __forceinline__ void insert_latent(uint8_t* ent, const uint16_t* __re
 template <int F>
 __global__ void __launch_bounds__(128) mla_epilogue_kernel(const EpiParams p) {
   const int b = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
+  // the decode launched next (a programmatic dependent) may be scheduled now; it waits for
+  // this grid before it reads the query and the cache
+  if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const float qinv = (F == 1) ? *p.q_scale_inv : 1.f;
   const float cinv = (F == 1) ? *p.cache_scale_inv : 1.f;
   const float* __restrict__ cs = nullptr;
@@ -329,7 +332,10 @@ cudaError_t launch_prefill_epilogue(int fmt, const PrefillEpiParams& p, int Tp, 
 // combine as vLLM's merge_attn_states ("vllm.models.kimi_k3.nvidia.mla",
 // _forward_prefill_fused) applied across the key splits of one decode row, or of one sparse
 // row (with an optional per-head sink logit e^{sink} added to the denominator).  One CTA of
-// 128 threads per (row, head); each thread owns 4 of the 512 columns.
+// 128 threads per (row, head); each thread owns 4 of the 512 columns and keeps kBatch splits'
+// loads in flight (the launch picks the smallest batch that covers the split count, since a
+// larger one costs registers and so resident CTAs).
+template <int kBatch>
 __global__ void __launch_bounds__(128) mla_merge_kernel(const MergeParams p) {
   // launched as a programmatic dependent of the attention kernel: wait until its grid has
   // finished and its partials are visible (a no-op under an ordinary launch)
@@ -342,12 +348,15 @@ __global__ void __launch_bounds__(128) mla_merge_kernel(const MergeParams p) {
     const int64_t L = max(p.seq_lens[row / p.q_len], 0);
     S = static_cast<int>(min(static_cast<int64_t>(S), (L + p.chunk - 1) / p.chunk));
   }
-  // the split weights exp(lse_s - max) are formed once, with the LSEs loaded in parallel
+  // the split weights exp(lse_s - max) are formed once: thread s loads the LSE of split s
+  // (and of s + 128, ...) once
   __shared__ float wsh[128];
   __shared__ float red[2][4];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  float m = -CUDART_INF_F;
-  for (int s = tid; s < S; s += 128) m = fmaxf(m, p.part_lse[s * stride + rh]);
+  const int64_t lbase = rh;
+  const float ls0 = tid < S ? p.part_lse[tid * stride + lbase] : -CUDART_INF_F;
+  float m = ls0;
+  for (int s = tid + 128; s < S; s += 128) m = fmaxf(m, p.part_lse[s * stride + lbase]);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
   if (lane == 0) red[0][warp] = m;
@@ -356,13 +365,11 @@ __global__ void __launch_bounds__(128) mla_merge_kernel(const MergeParams p) {
   // a sink logit joins the denominator with a zero value
   const float sk = p.sink ? p.sink[h] : -CUDART_INF_F;
   m = fmaxf(m, sk);
-  float ws = (tid == 0 && sk != -CUDART_INF_F) ? expf(sk - m) : 0.f;
-  for (int s = tid; s < S; s += 128) {
-    const float ls = p.part_lse[s * stride + rh];
-    const float w = (m == -CUDART_INF_F || ls == -CUDART_INF_F) ? 0.f : expf(ls - m);
-    if (s < 128) wsh[s] = w;
-    ws += w;
-  }
+  auto weight = [&](float ls) { return (m == -CUDART_INF_F || ls == -CUDART_INF_F) ? 0.f : expf(ls - m); };
+  const float w0 = weight(ls0);
+  wsh[tid] = w0;
+  float ws = w0 + ((tid == 0 && sk != -CUDART_INF_F) ? expf(sk - m) : 0.f);
+  for (int s = tid + 128; s < S; s += 128) ws += weight(p.part_lse[s * stride + lbase]);
 #pragma unroll
   for (int o = 16; o >= 1; o >>= 1) ws += __shfl_xor_sync(0xFFFFFFFFu, ws, o);
   if (lane == 0) red[1][warp] = ws;
@@ -371,32 +378,22 @@ __global__ void __launch_bounds__(128) mla_merge_kernel(const MergeParams p) {
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   const float4* po = reinterpret_cast<const float4*>(p.part_o + rh * 512) + tid;
   const int64_t step4 = stride * 128;      // one split, in float4
-  int s = 0;
-  for (; s + 4 <= S; s += 4) {             // four independent loads in flight
-    float w4[4];
-    float4 o4[4];
+  for (int s0 = 0; s0 < S; s0 += kBatch) {
+    float wb[kBatch];
+    float4 ob[kBatch];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int ss = s + u;
-      w4[u] = ss < 128 ? wsh[ss] : expf(p.part_lse[ss * stride + rh] - m);
-      o4[u] = w4[u] != 0.f ? po[ss * step4] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int u = 0; u < kBatch; ++u) {
+      const int ss = s0 + u;
+      wb[u] = ss >= S ? 0.f : ss < 128 ? wsh[ss] : weight(p.part_lse[ss * stride + lbase]);
+      ob[u] = wb[u] != 0.f ? po[ss * step4] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      acc.x += w4[u] * o4[u].x;
-      acc.y += w4[u] * o4[u].y;
-      acc.z += w4[u] * o4[u].z;
-      acc.w += w4[u] * o4[u].w;
+    for (int u = 0; u < kBatch; ++u) {
+      acc.x += wb[u] * ob[u].x;
+      acc.y += wb[u] * ob[u].y;
+      acc.z += wb[u] * ob[u].z;
+      acc.w += wb[u] * ob[u].w;
     }
-  }
-  for (; s < S; ++s) {
-    const float w = s < 128 ? wsh[s] : expf(p.part_lse[s * stride + rh] - m);
-    if (w == 0.f) continue;
-    const float4 o = po[s * step4];
-    acc.x += w * o.x;
-    acc.y += w * o.y;
-    acc.z += w * o.z;
-    acc.w += w * o.w;
   }
   const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
   __nv_bfloat16* dst = reinterpret_cast<__nv_bfloat16*>(p.out + row * p.o_s0b + h * p.o_s1b) + 4 * tid;
@@ -455,6 +452,19 @@ cudaError_t launch_epilogue(int fmt, const EpiParams& p, int B, cudaStream_t str
   return cudaGetLastError();
 }
 
+// Scheduler reset: zero the work-item counter of a persistent decode kernel.  Chained to the
+// kernels on either side as programmatic dependents (it waits for the previous kernel, so the
+// decode kernel's own wait covers both), it lets the decode's setup overlap the epilogue.
+__global__ void mla_sched_reset_kernel(uint32_t* sched) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (threadIdx.x == 0) *sched = 0u;
+}
+
+cudaError_t launch_sched_reset(uint32_t* sched, cudaStream_t stream) {
+  return launch_pdl(mla_sched_reset_kernel, dim3(1), dim3(32), 0, stream, sched);
+}
+
 cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   const int64_t n = static_cast<int64_t>(p.n_rows) * p.H;
   if (n == 0) return cudaSuccess;
@@ -470,7 +480,9 @@ cudaError_t launch_merge(const MergeParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, mla_merge_kernel, p);
+  if (p.S <= 4) return cudaLaunchKernelEx(&cfg, mla_merge_kernel<4>, p);
+  if (p.S <= 8) return cudaLaunchKernelEx(&cfg, mla_merge_kernel<8>, p);
+  return cudaLaunchKernelEx(&cfg, mla_merge_kernel<16>, p);
 }
 
 cudaError_t launch_gather(int fmt, const GatherParams& p, cudaStream_t stream) {
