@@ -442,6 +442,16 @@ MLA_API int mla_sparse_fwd_staged(const void* q, int64_t q_s0, int64_t q_s1, con
  */
 MLA_API void mla_debug_stall_next_decode(int32_t wait_us);
 
+/*
+ * Test aid: how mla_paged_decode runs an fp8_ds_mla cache on the calling host thread.  With
+ * enable != 0 (the default) a request whose q_len * H columns make an even number (>= 2) of
+ * 16-column groups is served by CTA pairs (2-CTA clusters): the two CTAs of a pair take two
+ * adjacent groups of the same request and split range, and each issues half of every page
+ * tile's copies with cluster multicast into both CTAs, so each key crosses L2 -> SM once per
+ * pair.  enable == 0 runs one CTA per group.  The results are the same bit for bit.
+ */
+MLA_API void mla_debug_ds_pairs(int32_t enable);
+
 #ifdef __cplusplus
 }
 #endif

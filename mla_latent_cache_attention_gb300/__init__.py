@@ -91,6 +91,8 @@ def lib():
                                                      i32, i32, i32, i32, vp]
         L.mla_debug_stall_next_decode.argtypes = [i32]
         L.mla_debug_stall_next_decode.restype = None
+        L.mla_debug_ds_pairs.argtypes = [i32]
+        L.mla_debug_ds_pairs.restype = None
         for f in ("mla_q_concat_cache_insert", "mla_sparse_fwd", "mla_sparse_fwd_staged", "mla_paged_decode",
                   "mla_gather_dequant", "mla_key_concat_cache_insert", "mla_qkv_quant_cache_fp8_insert",
                   "mla_gather_context", "mla_merge_attn_states", "mla_sparse_fwd_ext", "mla_absorb_q",
@@ -516,3 +518,10 @@ def debug_stall_next_decode(wait_us: int):
     """Test aid (mla_debug_stall_next_decode): the next page-kernel decode on this thread
     issues no loads and its waits give up after wait_us microseconds."""
     lib().mla_debug_stall_next_decode(int(wait_us))
+
+
+def debug_ds_pairs(enable: bool) -> None:
+    """Test aid (mla_debug_ds_pairs): whether fp8_ds_mla decodes on this host thread run
+    head-group pairs as 2-CTA clusters sharing each page tile (the default) or one CTA per
+    group."""
+    lib().mla_debug_ds_pairs(1 if enable else 0)

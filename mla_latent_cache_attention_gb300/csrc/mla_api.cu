@@ -113,6 +113,9 @@ size_t workspace_bytes_for(int64_t n_rows, int H, const SplitPlan& sp) {
 // Test aid: wait limit (microseconds) of the next page-kernel launch on this thread, whose
 // producer then issues no loads; 0 = none armed.
 thread_local int g_stall_next_us = 0;
+// fp8_ds_mla paged decode: run head-group pairs as 2-CTA clusters where the grouping allows
+// (set per host thread by the test aid mla_debug_ds_pairs)
+thread_local int g_ds_pairs = 1;
 
 int grid_for(int64_t items, int sms) {
   return static_cast<int>(items < sms ? items : sms);
@@ -692,6 +695,8 @@ extern "C" int mla_sparse_fwd_ext(const void* q, int64_t q_s0, int64_t q_s1, con
 
 extern "C" void mla_debug_stall_next_decode(int32_t wait_us) { g_stall_next_us = wait_us > 0 ? wait_us : 0; }
 
+extern "C" void mla_debug_ds_pairs(int32_t enable) { g_ds_pairs = enable ? 1 : 0; }
+
 // ------------------------------------------------------------------------------------------
 extern "C" size_t mla_paged_decode_workspace_size(int32_t B, int32_t q_len, int32_t H,
                                                   int32_t max_context, int32_t num_sms) {
@@ -764,7 +769,9 @@ extern "C" int mla_paged_decode(const void* q, int64_t q_s0, int64_t q_s1, const
   if (fmt == MLA_CACHE_FP8_DS_MLA && tma_rows > 0 && aligned(q, 16) && (q_s0 * 2) % 16 == 0 && (q_s1 * 2) % 16 == 0 &&
       num_blocks < (int64_t(1) << 31) && max_context < (1 << 30)) {
     const int G = (q_len * H + 15) / 16;
-    const int64_t items = static_cast<int64_t>(sp.n_splits) * B * G;
+    // an even number of 16-column groups runs as CTA pairs that share each page tile
+    const int pair_cap = (g_ds_pairs && G >= 2 && G % 2 == 0) ? ds_pair_capacity() : 0;
+    const int64_t items = static_cast<int64_t>(sp.n_splits) * B * (pair_cap > 0 ? G / 2 : G);
     if (items >= (int64_t(1) << 31)) return fail(MLA_ERR_UNSUPPORTED, "too many work items");
     CUtensorMap tkv, tsc;
     const uint64_t kd[3] = {656, static_cast<uint64_t>(block_size), static_cast<uint64_t>(num_blocks)};
@@ -805,7 +812,8 @@ extern "C" int mla_paged_decode(const void* q, int64_t q_s0, int64_t q_s1, const
     if (sched && launch_sched_reset(sched, stream) != cudaSuccess)
       return fail(MLA_ERR_CUDA, "scheduler reset failed: %s", cudaGetErrorString(cudaGetLastError()));
     prof_begin(stream);
-    const cudaError_t e = launch_ds_paged(p, &tkv, &tsc, grid_for(items, d->sms), stream);
+    const cudaError_t e = pair_cap > 0 ? launch_ds_paged_pairs(p, &tkv, &tsc, grid_for(items, pair_cap), stream)
+                                       : launch_ds_paged(p, &tkv, &tsc, grid_for(items, d->sms), stream);
     prof_end(stream);
     if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "decode attention launch failed: %s", cudaGetErrorString(e));
     if (sp.n_splits > 1) {

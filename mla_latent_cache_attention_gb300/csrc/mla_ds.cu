@@ -5,32 +5,92 @@
 namespace mla {
 namespace {
 
-template <bool kSparse>
-cudaError_t launch_t(const DsParams& p, const void* tkv, const void* tsc, int grid, cudaStream_t stream) {
-  using C = DsCfg<kSparse>;
+template <bool kSparse, int kCl>
+cudaError_t configure(int dev) {
   static bool configured[64] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!configured[dev]) {
-    e = cudaFuncSetAttribute(mla_ds_kernel<kSparse>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kAlloc);
+    const cudaError_t e = cudaFuncSetAttribute(mla_ds_kernel<kSparse, kCl>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, DsCfg<kSparse>::kAlloc);
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
+  return cudaSuccess;
+}
+
+template <bool kSparse>
+cudaError_t launch_t(const DsParams& p, const void* tkv, const void* tsc, int grid, cudaStream_t stream) {
+  using C = DsCfg<kSparse>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = configure<kSparse, 1>(dev)) != cudaSuccess) return e;
   CUtensorMap dummy{};
   const CUtensorMap& a = tkv ? *static_cast<const CUtensorMap*>(tkv) : dummy;
   const CUtensorMap& b = tsc ? *static_cast<const CUtensorMap*>(tsc) : dummy;
-  return launch_pdl(mla_ds_kernel<kSparse>, dim3(grid), dim3(C::kThreads), C::kAlloc, stream, p, a, b);
+  return launch_pdl(mla_ds_kernel<kSparse, 1>, dim3(grid), dim3(C::kThreads), C::kAlloc, stream, p, a, b);
 }
 
 }  // namespace
+
+// How many CTA pairs of the paged kernel can be resident at once on this device (0 when the
+// query fails): the persistent grid must not exceed it.
+int ds_pair_capacity() {
+  static int cap[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (cap[dev] > 0) return cap[dev];
+  if (configure<false, 2>(dev) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(DsCfg<false>::kThreads);
+  cfg.dynamicSmemBytes = DsCfg<false>::kAlloc;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, mla_ds_kernel<false, 2>, &cfg) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return 0;
+  }
+  cap[dev] = n;
+  return n;
+}
 
 cudaError_t launch_ds_sparse(const DsParams& p, int grid, cudaStream_t stream) {
   return launch_t<true>(p, nullptr, nullptr, grid, stream);
 }
 cudaError_t launch_ds_paged(const DsParams& p, const void* tkv, const void* tsc, int grid, cudaStream_t stream) {
   return launch_t<false>(p, tkv, tsc, grid, stream);
+}
+
+// The paged kernel as CTA pairs: `pairs` 2-CTA clusters, p.n_items counting pair items.
+cudaError_t launch_ds_paged_pairs(const DsParams& p, const void* tkv, const void* tsc, int pairs, cudaStream_t stream) {
+  using C = DsCfg<false>;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if ((e = configure<false, 2>(dev)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(C::kThreads);
+  cfg.dynamicSmemBytes = C::kAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, mla_ds_kernel<false, 2>, p, *static_cast<const CUtensorMap*>(tkv),
+                            *static_cast<const CUtensorMap*>(tsc));
 }
 
 }  // namespace mla

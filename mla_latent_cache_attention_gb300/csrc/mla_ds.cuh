@@ -89,9 +89,10 @@ struct DsCfg {
   static constexpr int kValid = kRj + 4 * 8 * 4;                  // [2][128] row flags (sparse)
   static constexpr int kItems = kValid + 2 * kTile;
   static constexpr int kBar = kItems + kItemDepth * 32;
-  static constexpr int kNumBars = R + 9 + 2 * kItemDepth;
+  // + ring_free[2] and xitem_full[kItemDepth] of the CTA-pair kernel
+  static constexpr int kNumBars = R + 9 + 2 * kItemDepth + 2 + kItemDepth;
   static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kTotal = kMisc + 16;
+  static constexpr int kTotal = kMisc + 32;     // TMEM slot, abort word, the peer's ring position
   static constexpr int kAlloc = kTotal + 1024;
   static_assert(kAlloc <= kSmemLimit, "shared memory budget");
   static constexpr int kS = 0;                                    // S (144 columns): S_j at 32 j, rope at 128
@@ -112,11 +113,20 @@ __device__ __forceinline__ int e4m3_fit_exponent(float a) {
   return e;
 }
 
-template <bool kSparse>
+// kCl = 2 (paged source only): the kernel runs as CTA pairs (2-CTA clusters).  The two CTAs
+// of a pair take the same item (request, split) for two adjacent column groups: the pair's
+// first CTA takes the tickets and passes each item to the second through a mailbox in its
+// shared memory; each CTA issues half of every tile's page boxes with cluster multicast, so
+// both rings receive the whole tile while each SM's copy engine issues half of it and L2
+// serves each key once per pair; a ring slot is reused only once both CTAs' PV of the tile
+// before has finished with it (a multicast commit into a two-arrival barrier of each CTA).
+template <bool kSparse, int kCl>
 __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
     mla_ds_kernel(const __grid_constant__ DsParams p, const __grid_constant__ CUtensorMap tm_kv,
                   const __grid_constant__ CUtensorMap tm_sc) {
+  static_assert(kCl == 1 || (kCl == 2 && !kSparse), "CTA pairs serve the paged source");
   using C = DsCfg<kSparse>;
+  static_assert(C::kItems % 16 == 0 && C::kMisc % 8 == 0, "queue slots are read as 16-byte words");
   constexpr int R = C::R, NB = C::NB, NQ = C::NQ;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -140,8 +150,13 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
   uint64_t* item_full = bars + R + 8;
   uint64_t* item_empty = item_full + kItemDepth;
   uint64_t* fin_pv = item_empty + kItemDepth;
+  uint64_t* ring_free = fin_pv + 1;       // [2] pair: both CTAs' PV of the tile is done
+  uint64_t* xitem_full = ring_free + 2;   // [kItemDepth] pair: the first CTA's item k is posted
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
+  int64_t* peer_pos = reinterpret_cast<int64_t*>(smem + C::kMisc + 16);   // pair: the other producer's positions
+  const uint32_t crank = kCl > 1 ? cluster_ctarank() : 0u;
+  constexpr uint16_t kMask = static_cast<uint16_t>((1u << kCl) - 1u);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   TL_DECL;
@@ -161,10 +176,15 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
     mbar_init(s_free, 1);
     for (int k = 0; k < kItemDepth; ++k) {
       mbar_init(&item_full[k], 1);
-      mbar_init(&item_empty[k], 3 + C::kGatherWarps);
+      // the pair's first CTA also waits for the second one's producer to have read item k
+      mbar_init(&item_empty[k], 3 + C::kGatherWarps + ((kCl > 1 && crank == 0) ? kCl - 1 : 0));
+      mbar_init(&xitem_full[k], 1);
     }
+    mbar_init(&ring_free[0], kCl);
+    mbar_init(&ring_free[1], kCl);
     *abort_flag = 0;
     abort_flag[1] = 0;
+    *peer_pos = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -174,6 +194,8 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // pair: both CTAs' barriers exist before either signals the other or copies into it
+  if (kCl > 1) cluster_sync();
   const uint32_t tmem = *tmem_slot;
   // launched as a programmatic dependent of the previous kernel in the stream: the setup above
   // overlaps that kernel's tail, and its writes (a decode epilogue's query and cache entry, the
@@ -181,13 +203,15 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // items: (split s, request / row b, column group g)
+  // pair: an item covers kCl adjacent column groups, the one of CTA r being kCl * g' + r
   auto decode = [&](int item, WorkItem& it) -> bool {     // false: an empty split (skipped)
     it.b = -1;
     if (item >= p.n_items) return true;
-    const int bg = p.B * p.G;
+    const int Gc = (p.G + kCl - 1) / kCl;
+    const int bg = p.B * Gc;
     it.s = item / bg;
-    it.b = (item % bg) / p.G;
-    it.g = item % p.G;
+    it.b = (item % bg) / Gc;
+    it.g = (item % Gc) * kCl + static_cast<int>(crank);
     it.pad = 0;
     if (kSparse) {
       // split s of the row: keys [s c, (s + 1) c) of its list, c = ceil(n / n_splits) rounded
@@ -302,35 +326,68 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
     uint32_t errbits = 0;
     int nitem = 0, stride_k = 0, gt_next = 0;
     bool ok = true;
+    // tickets: one counter per launch (or a static stride when there is none); a pair's
+    // tickets are taken by its first CTA
+    const int unit = static_cast<int>(blockIdx.x) / kCl, n_units = static_cast<int>(gridDim.x) / kCl;
     auto take_ticket = [&]() -> int {
       int item = 0;
-      if (lane == 0)
-        item = p.sched ? static_cast<int>(atomicAdd(p.sched, 1u)) : static_cast<int>(blockIdx.x + stride_k * gridDim.x);
+      if (lane == 0) item = p.sched ? static_cast<int>(atomicAdd(p.sched, 1u)) : unit + stride_k * n_units;
       ++stride_k;
       return __shfl_sync(0xFFFFFFFFu, item, 0);
     };
-    auto next_item = [&]() -> WorkItem {
-      WorkItem it{};
-      while (!decode(take_ticket(), it)) {
+    // the next item of this CTA (false: a wait ran out).  The pair's second CTA reads item
+    // nitem from the first CTA's queue slot once it is posted, then releases that slot.
+    auto fetch = [&](WorkItem& it) -> bool {
+      if (kCl == 1 || crank == 0) {
+        while (!decode(take_ticket(), it)) {
+        }
+        return true;
       }
-      return it;
+      const int k = nitem % kItemDepth;
+      if (!warp_wait_cl(&xitem_full[k], static_cast<uint32_t>(nitem / kItemDepth) & 1u, abort_flag)) return false;
+      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+      if (lane == 0) {
+        const uint32_t src = mapa_shared(&items[k], 0);
+        v0 = ld_cluster_v4(src);
+        v1 = ld_cluster_v4(src + 16);
+        mbar_arrive_remote(mapa_shared(&item_empty[k], 0));
+      }
+      const uint32_t f[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      uint32_t g[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) g[i] = __shfl_sync(0xFFFFFFFFu, f[i], 0);
+      static_assert(sizeof(WorkItem) == 32, "a queue slot is two 16-byte words");
+      memcpy(&it, g, sizeof(WorkItem));
+      if (it.b >= 0) it.g += static_cast<int>(crank);
+      return true;
+    };
+    // post item `it` to this CTA's roles (and, from a pair's first CTA, to the second CTA)
+    auto push = [&](const WorkItem& it) -> bool {
+      const int k = nitem % kItemDepth;
+      if (nitem >= kItemDepth) {
+        const uint32_t par = static_cast<uint32_t>((nitem / kItemDepth) - 1) & 1u;
+        const bool w = (kCl > 1 && crank == 0) ? warp_wait_cl(&item_empty[k], par, abort_flag)
+                                               : warp_wait(&item_empty[k], par, abort_flag);
+        if (!w) return false;
+      }
+      if (lane == 0) {
+        items[k] = it;
+        mbar_arrive(&item_full[k]);
+        if (kCl > 1 && crank == 0)
+          for (int r = 1; r < kCl; ++r) mbar_arrive_remote(mapa_shared(&xitem_full[k], static_cast<uint32_t>(r)));
+      }
+      ++nitem;
+      return true;
     };
     const int NPG = kTile / max(p.BR, 1);
     int64_t pos = 0;
     int t_waited = -1;
-    WorkItem cur = next_item();
+    WorkItem cur{};
+    ok = fetch(cur);
     while (ok && cur.b >= 0) {
-      {
-        const int k = nitem % kItemDepth;
-        if (nitem >= kItemDepth && !warp_wait(&item_empty[k], ((nitem / kItemDepth) - 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        if (lane == 0) {
-          items[k] = cur;
-          mbar_arrive(&item_full[k]);
-        }
-        ++nitem;
+      if (!push(cur)) {
+        ok = false;
+        break;
       }
       {
         for (int t = 0; t < cur.ntiles && ok; ++t) {
@@ -348,10 +405,12 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
               }
             }
           }
-          // the two-tile ring: tile gt reuses the slots of tile gt - 2
+          // the two-tile ring: tile gt reuses the slots of tile gt - 2 (a pair: in both CTAs)
           if (lane == 0) TL(0, 1);
           if (gt >= 2 && gt - 2 != t_waited) {
-            if (!warp_wait(&pv_done[gt & 1], static_cast<uint32_t>((gt - 2) >> 1) & 1u, abort_flag)) {
+            const uint32_t par = static_cast<uint32_t>((gt - 2) >> 1) & 1u;
+            if (!(kCl > 1 ? warp_wait_cl(&ring_free[gt & 1], par, abort_flag)
+                          : warp_wait(&pv_done[gt & 1], par, abort_flag))) {
               ok = false;
               break;
             }
@@ -361,6 +420,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
 #pragma unroll 1
           for (int b = 0; b < NB; ++b, ++pos) {
             const int slot = static_cast<int>(pos % R);
+            // the slot's whole tile lands here (a pair: half from each CTA's boxes)
             const uint32_t bytes = kSlotBytes + (b == NB - 1 ? static_cast<uint32_t>(kTile * 16) : 0u);
             if (lane == 0) mbar_arrive_expect_tx(&full[slot], bytes);
             __syncwarp();
@@ -368,31 +428,35 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
             for (int q = 0; q < NPG; ++q) {
               const int z = __shfl_sync(0xFFFFFFFFu, blk, q);
               const int yy = __shfl_sync(0xFFFFFFFFu, y, q);
-              if (lane == 0) {
-                tma_load_3d(ring + slot * kSlotBytes + q * p.BR * 128, &tm_kv, x, yy, z, &full[slot]);
-                if (b == NB - 1)
-                  tma_load_3d(reinterpret_cast<uint8_t*>(scl + (gt & 1) * kTile) + q * p.BR * 16, &tm_sc, 512, yy, z,
-                              &full[slot]);
+              if (lane == 0 && (kCl == 1 || (b * NPG + q) % kCl == static_cast<int>(crank))) {
+                uint8_t* dk = ring + slot * kSlotBytes + q * p.BR * 128;
+                uint8_t* ds = reinterpret_cast<uint8_t*>(scl + (gt & 1) * kTile) + q * p.BR * 16;
+                if (kCl > 1) {
+                  tma_load_3d_mc(dk, &tm_kv, x, yy, z, &full[slot], kMask);
+                  if (b == NB - 1) tma_load_3d_mc(ds, &tm_sc, 512, yy, z, &full[slot], kMask);
+                } else {
+                  tma_load_3d(dk, &tm_kv, x, yy, z, &full[slot]);
+                  if (b == NB - 1) tma_load_3d(ds, &tm_sc, 512, yy, z, &full[slot]);
+                }
               }
             }
           }
         }
       }
       gt_next += cur.ntiles;
-      if (ok) cur = next_item();
+      if (ok) ok = fetch(cur);
     }
     if (ok) {
-      const int k = nitem % kItemDepth;
-      if (nitem < kItemDepth || warp_wait(&item_empty[k], ((nitem / kItemDepth) - 1) & 1, abort_flag)) {
-        if (lane == 0) {
-          WorkItem e{};
-          e.b = -1;
-          items[k] = e;
-          mbar_arrive(&item_full[k]);
-        }
-      }
+      WorkItem e{};
+      e.b = -1;
+      (void)push(e);
     }
-    if (lane == 0) {     // never leave copies in flight behind us
+    if (kCl > 1) {
+      // the other producer's issued positions reach this CTA's drain (after the final cluster
+      // barrier, when neither producer issues any more)
+      if (lane == 0) st_cluster_u64(mapa_shared(peer_pos, crank ^ 1u), static_cast<uint64_t>(pos));
+      if (lane == 0) *reinterpret_cast<int64_t*>(smem + C::kMisc + 24) = pos;
+    } else if (lane == 0) {     // never leave copies in flight behind us
       volatile int no_abort[2] = {0, 0};
       const int64_t first = pos > R ? pos - R : 0;
       for (int64_t q = first; q < pos; ++q) mbar_wait(&full[q % R], static_cast<uint32_t>(q / R) & 1u, no_abort);
@@ -868,6 +932,8 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
                         (t > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&pv_done[gt & 1]);
+          // pair: this CTA's share of "tile gt's slots are free", in both CTAs
+          if (kCl > 1) mma_commit_mc(&ring_free[gt & 1], kMask);
           TL(2, 4);
         }
         g += it.ntiles;
@@ -964,6 +1030,22 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (kCl > 1) {
+    // pair: both producers have stopped issuing; wait (bounded) until every copy that either
+    // issued into this CTA's ring has landed, so that no copy targets it once it exits.  A
+    // position that one producer never issued (after an abort) keeps its phase open: the wait
+    // then runs to its limit, by which time the other copies of that position have landed.
+    cluster_sync();
+    if (tid == 0) {
+      const int64_t own = *reinterpret_cast<int64_t*>(smem + C::kMisc + 24);
+      const int64_t hi = max(own, *peer_pos);
+      const int64_t first = hi > R ? hi - R : 0;
+      volatile int drain[2] = {0, 0};
+      for (int64_t q = first; q < hi; ++q)
+        if (!mbar_wait(&full[q % R], static_cast<uint32_t>(q / R) & 1u, drain)) break;
+    }
+    __syncthreads();
+  }
   if (tid == 0 && *abort_flag == 2) set_device_error(p.err, 16u);
   if (warp == 1) {
     tc_fence_after();

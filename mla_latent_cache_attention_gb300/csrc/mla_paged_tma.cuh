@@ -150,6 +150,17 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* tm, in
       : "memory");
 }
 
+// The same box written at the same offset into every CTA of `mask` (cluster multicast); each
+// destination's mbarrier at `bar`'s offset receives the box's bytes.
+__device__ __forceinline__ void tma_load_3d_mc(void* dst, const CUtensorMap* tm, int x, int y, int z, uint64_t* bar,
+                                               uint16_t mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
+      "{%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(tm), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)), "h"(mask)
+      : "memory");
+}
+
 // Contiguous global bytes into L2 (address and size multiples of 16).
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
@@ -165,6 +176,15 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* tm, int x, in
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
   bool w = true;
   if ((threadIdx.x & 31) == 0) w = mbar_wait(bar, parity, abort_flag);
+  w = __shfl_sync(0xFFFFFFFFu, w ? 1 : 0, 0) != 0;
+  __syncwarp();
+  return w;
+}
+
+// The same with acquire at cluster scope (phases completed by another CTA's arrivals).
+__device__ __forceinline__ bool warp_wait_cl(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  bool w = true;
+  if ((threadIdx.x & 31) == 0) w = mbar_wait_cl(bar, parity, abort_flag);
   w = __shfl_sync(0xFFFFFFFFu, w ? 1 : 0, 0) != 0;
   __syncwarp();
   return w;
