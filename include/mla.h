@@ -443,14 +443,15 @@ MLA_API int mla_sparse_fwd_staged(const void* q, int64_t q_s0, int64_t q_s1, con
 MLA_API void mla_debug_stall_next_decode(int32_t wait_us);
 
 /*
- * Test aid: how mla_paged_decode runs an fp8_ds_mla cache on the calling host thread.  With
- * enable != 0 (the default) a request whose q_len * H columns make an even number (>= 2) of
- * 16-column groups is served by CTA pairs (2-CTA clusters): the two CTAs of a pair take two
- * adjacent groups of the same request and split range, and each issues half of every page
- * tile's copies with cluster multicast into both CTAs, so each key crosses L2 -> SM once per
- * pair.  enable == 0 runs one CTA per group.  The results are the same bit for bit.
+ * Test aid: how mla_paged_decode runs an fp8_ds_mla cache on the calling host thread.  The
+ * q_len * H columns of a request form G groups of 16.  size 2, 3 or 6: where size divides G,
+ * the groups run as clusters of that many CTAs, which take adjacent groups of the same request
+ * and split range and each issue a share of every page tile's copies with cluster multicast
+ * into all of them, so each key crosses L2 -> SM once per cluster.  size 1: one CTA per group.
+ * Any other value restores the library's choice (pairs where G is even).  The results are the
+ * same bit for bit.
  */
-MLA_API void mla_debug_ds_pairs(int32_t enable);
+MLA_API void mla_debug_ds_cluster(int32_t size);
 
 #ifdef __cplusplus
 }

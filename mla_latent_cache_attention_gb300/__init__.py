@@ -91,8 +91,8 @@ def lib():
                                                      i32, i32, i32, i32, vp]
         L.mla_debug_stall_next_decode.argtypes = [i32]
         L.mla_debug_stall_next_decode.restype = None
-        L.mla_debug_ds_pairs.argtypes = [i32]
-        L.mla_debug_ds_pairs.restype = None
+        L.mla_debug_ds_cluster.argtypes = [i32]
+        L.mla_debug_ds_cluster.restype = None
         for f in ("mla_q_concat_cache_insert", "mla_sparse_fwd", "mla_sparse_fwd_staged", "mla_paged_decode",
                   "mla_gather_dequant", "mla_key_concat_cache_insert", "mla_qkv_quant_cache_fp8_insert",
                   "mla_gather_context", "mla_merge_attn_states", "mla_sparse_fwd_ext", "mla_absorb_q",
@@ -520,8 +520,8 @@ def debug_stall_next_decode(wait_us: int):
     lib().mla_debug_stall_next_decode(int(wait_us))
 
 
-def debug_ds_pairs(enable: bool) -> None:
-    """Test aid (mla_debug_ds_pairs): whether fp8_ds_mla decodes on this host thread run
-    head-group pairs as 2-CTA clusters sharing each page tile (the default) or one CTA per
-    group."""
-    lib().mla_debug_ds_pairs(1 if enable else 0)
+def debug_ds_cluster(size: int = 0) -> None:
+    """Test aid (mla_debug_ds_cluster): fp8_ds_mla decodes on this host thread run the head
+    groups of a request as clusters of `size` CTAs (2, 3 or 6) that share each page tile, one
+    CTA per group (1), or as the library chooses (0: pairs where the group count is even)."""
+    lib().mla_debug_ds_cluster(int(size))

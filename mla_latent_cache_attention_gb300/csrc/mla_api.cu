@@ -113,9 +113,23 @@ size_t workspace_bytes_for(int64_t n_rows, int H, const SplitPlan& sp) {
 // Test aid: wait limit (microseconds) of the next page-kernel launch on this thread, whose
 // producer then issues no loads; 0 = none armed.
 thread_local int g_stall_next_us = 0;
-// fp8_ds_mla paged decode: run head-group pairs as 2-CTA clusters where the grouping allows
-// (set per host thread by the test aid mla_debug_ds_pairs)
-thread_local int g_ds_pairs = 1;
+// fp8_ds_mla paged decode: the cluster size for the head groups of a request (0: the
+// library's choice; set per host thread by the test aid mla_debug_ds_cluster)
+thread_local int g_ds_cluster = 0;
+
+// Cluster size for G 16-column groups: the largest allowed size that divides G and can be
+// resident, the library's default being pairs (measured best), or 1.
+int ds_cluster_for(int G) {
+  const int want = g_ds_cluster;
+  if (want == 1 || G < 2) return 1;
+  const int sizes[3] = {6, 3, 2};
+  for (int sz : sizes) {
+    if (want != 0 && sz != want) continue;
+    if (want == 0 && sz != 2) continue;
+    if (G % sz == 0 && ds_cluster_capacity(sz) > 0) return sz;
+  }
+  return 1;
+}
 
 int grid_for(int64_t items, int sms) {
   return static_cast<int>(items < sms ? items : sms);
@@ -695,7 +709,9 @@ extern "C" int mla_sparse_fwd_ext(const void* q, int64_t q_s0, int64_t q_s1, con
 
 extern "C" void mla_debug_stall_next_decode(int32_t wait_us) { g_stall_next_us = wait_us > 0 ? wait_us : 0; }
 
-extern "C" void mla_debug_ds_pairs(int32_t enable) { g_ds_pairs = enable ? 1 : 0; }
+extern "C" void mla_debug_ds_cluster(int32_t size) {
+  g_ds_cluster = (size == 1 || size == 2 || size == 3 || size == 6) ? size : 0;
+}
 
 // ------------------------------------------------------------------------------------------
 extern "C" size_t mla_paged_decode_workspace_size(int32_t B, int32_t q_len, int32_t H,
@@ -769,9 +785,9 @@ extern "C" int mla_paged_decode(const void* q, int64_t q_s0, int64_t q_s1, const
   if (fmt == MLA_CACHE_FP8_DS_MLA && tma_rows > 0 && aligned(q, 16) && (q_s0 * 2) % 16 == 0 && (q_s1 * 2) % 16 == 0 &&
       num_blocks < (int64_t(1) << 31) && max_context < (1 << 30)) {
     const int G = (q_len * H + 15) / 16;
-    // an even number of 16-column groups runs as CTA pairs that share each page tile
-    const int pair_cap = (g_ds_pairs && G >= 2 && G % 2 == 0) ? ds_pair_capacity() : 0;
-    const int64_t items = static_cast<int64_t>(sp.n_splits) * B * (pair_cap > 0 ? G / 2 : G);
+    // head groups of a request run as a cluster of CTAs that share each page tile
+    const int csize = ds_cluster_for(G);
+    const int64_t items = static_cast<int64_t>(sp.n_splits) * B * (G / csize);
     if (items >= (int64_t(1) << 31)) return fail(MLA_ERR_UNSUPPORTED, "too many work items");
     CUtensorMap tkv, tsc;
     const uint64_t kd[3] = {656, static_cast<uint64_t>(block_size), static_cast<uint64_t>(num_blocks)};
@@ -812,8 +828,9 @@ extern "C" int mla_paged_decode(const void* q, int64_t q_s0, int64_t q_s1, const
     if (sched && launch_sched_reset(sched, stream) != cudaSuccess)
       return fail(MLA_ERR_CUDA, "scheduler reset failed: %s", cudaGetErrorString(cudaGetLastError()));
     prof_begin(stream);
-    const cudaError_t e = pair_cap > 0 ? launch_ds_paged_pairs(p, &tkv, &tsc, grid_for(items, pair_cap), stream)
-                                       : launch_ds_paged(p, &tkv, &tsc, grid_for(items, d->sms), stream);
+    const cudaError_t e =
+        csize > 1 ? launch_ds_paged_clusters(p, &tkv, &tsc, csize, grid_for(items, ds_cluster_capacity(csize)), stream)
+                  : launch_ds_paged(p, &tkv, &tsc, grid_for(items, d->sms), stream);
     prof_end(stream);
     if (e != cudaSuccess) return fail(MLA_ERR_CUDA, "decode attention launch failed: %s", cudaGetErrorString(e));
     if (sp.n_splits > 1) {

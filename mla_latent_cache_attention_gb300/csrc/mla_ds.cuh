@@ -92,7 +92,7 @@ struct DsCfg {
   // + ring_free[2] and xitem_full[kItemDepth] of the CTA-pair kernel
   static constexpr int kNumBars = R + 9 + 2 * kItemDepth + 2 + kItemDepth;
   static constexpr int kMisc = kBar + kNumBars * 8;
-  static constexpr int kTotal = kMisc + 32;     // TMEM slot, abort word, the peer's ring position
+  static constexpr int kTotal = kMisc + 16 + 8 * 8;   // TMEM slot, abort word, cluster CTAs' ring positions
   static constexpr int kAlloc = kTotal + 1024;
   static_assert(kAlloc <= kSmemLimit, "shared memory budget");
   static constexpr int kS = 0;                                    // S (144 columns): S_j at 32 j, rope at 128
@@ -113,18 +113,18 @@ __device__ __forceinline__ int e4m3_fit_exponent(float a) {
   return e;
 }
 
-// kCl = 2 (paged source only): the kernel runs as CTA pairs (2-CTA clusters).  The two CTAs
-// of a pair take the same item (request, split) for two adjacent column groups: the pair's
-// first CTA takes the tickets and passes each item to the second through a mailbox in its
-// shared memory; each CTA issues half of every tile's page boxes with cluster multicast, so
-// both rings receive the whole tile while each SM's copy engine issues half of it and L2
-// serves each key once per pair; a ring slot is reused only once both CTAs' PV of the tile
-// before has finished with it (a multicast commit into a two-arrival barrier of each CTA).
+// kCl = 2, 3 or 6 (paged source only): the kernel runs as clusters of kCl CTAs.  The CTAs of a
+// cluster take the same item (request, split) for kCl adjacent column groups: the cluster's
+// first CTA takes the tickets and passes each item to the others through a mailbox in its
+// shared memory; each CTA issues 1/kCl of every tile's page boxes with cluster multicast, so
+// every ring receives the whole tile while each SM's copy engine issues a share of it and L2
+// serves each key once per cluster; a ring slot is reused only once every CTA's PV of the tile
+// before has finished with it (a multicast commit into a kCl-arrival barrier of each CTA).
 template <bool kSparse, int kCl>
 __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
     mla_ds_kernel(const __grid_constant__ DsParams p, const __grid_constant__ CUtensorMap tm_kv,
                   const __grid_constant__ CUtensorMap tm_sc) {
-  static_assert(kCl == 1 || (kCl == 2 && !kSparse), "CTA pairs serve the paged source");
+  static_assert(kCl == 1 || ((kCl == 2 || kCl == 3 || kCl == 6) && !kSparse), "clusters serve the paged source");
   using C = DsCfg<kSparse>;
   static_assert(C::kItems % 16 == 0 && C::kMisc % 8 == 0, "queue slots are read as 16-byte words");
   constexpr int R = C::R, NB = C::NB, NQ = C::NQ;
@@ -150,11 +150,11 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
   uint64_t* item_full = bars + R + 8;
   uint64_t* item_empty = item_full + kItemDepth;
   uint64_t* fin_pv = item_empty + kItemDepth;
-  uint64_t* ring_free = fin_pv + 1;       // [2] pair: both CTAs' PV of the tile is done
-  uint64_t* xitem_full = ring_free + 2;   // [kItemDepth] pair: the first CTA's item k is posted
+  uint64_t* ring_free = fin_pv + 1;       // [2] cluster: every CTA's PV of the tile is done
+  uint64_t* xitem_full = ring_free + 2;   // [kItemDepth] cluster: the first CTA's item k is posted
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
-  int64_t* peer_pos = reinterpret_cast<int64_t*>(smem + C::kMisc + 16);   // pair: the other producer's positions
+  int64_t* cl_pos = reinterpret_cast<int64_t*>(smem + C::kMisc + 16);   // [kCl] cluster: positions each producer issued
   const uint32_t crank = kCl > 1 ? cluster_ctarank() : 0u;
   constexpr uint16_t kMask = static_cast<uint16_t>((1u << kCl) - 1u);
 
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
     mbar_init(s_free, 1);
     for (int k = 0; k < kItemDepth; ++k) {
       mbar_init(&item_full[k], 1);
-      // the pair's first CTA also waits for the second one's producer to have read item k
+      // the cluster's first CTA also waits for the other producers to have read item k
       mbar_init(&item_empty[k], 3 + C::kGatherWarps + ((kCl > 1 && crank == 0) ? kCl - 1 : 0));
       mbar_init(&xitem_full[k], 1);
     }
@@ -184,7 +184,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
     mbar_init(&ring_free[1], kCl);
     *abort_flag = 0;
     abort_flag[1] = 0;
-    *peer_pos = 0;
+    for (int r = 0; r < 8; ++r) cl_pos[r] = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // pair: both CTAs' barriers exist before either signals the other or copies into it
+  // cluster: every CTA's barriers exist before any CTA signals another or copies into it
   if (kCl > 1) cluster_sync();
   const uint32_t tmem = *tmem_slot;
   // launched as a programmatic dependent of the previous kernel in the stream: the setup above
@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   // items: (split s, request / row b, column group g)
-  // pair: an item covers kCl adjacent column groups, the one of CTA r being kCl * g' + r
+  // cluster: an item covers kCl adjacent column groups, the one of CTA r being kCl * g' + r
   auto decode = [&](int item, WorkItem& it) -> bool {     // false: an empty split (skipped)
     it.b = -1;
     if (item >= p.n_items) return true;
@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
     uint32_t errbits = 0;
     int nitem = 0, stride_k = 0, gt_next = 0;
     bool ok = true;
-    // tickets: one counter per launch (or a static stride when there is none); a pair's
+    // tickets: one counter per launch (or a static stride when there is none); a cluster's
     // tickets are taken by its first CTA
     const int unit = static_cast<int>(blockIdx.x) / kCl, n_units = static_cast<int>(gridDim.x) / kCl;
     auto take_ticket = [&]() -> int {
@@ -335,8 +335,8 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
       ++stride_k;
       return __shfl_sync(0xFFFFFFFFu, item, 0);
     };
-    // the next item of this CTA (false: a wait ran out).  The pair's second CTA reads item
-    // nitem from the first CTA's queue slot once it is posted, then releases that slot.
+    // the next item of this CTA (false: a wait ran out).  The cluster's other CTAs read item
+    // nitem from the first CTA's queue slot once it is posted, then release that slot.
     auto fetch = [&](WorkItem& it) -> bool {
       if (kCl == 1 || crank == 0) {
         while (!decode(take_ticket(), it)) {
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
       if (it.b >= 0) it.g += static_cast<int>(crank);
       return true;
     };
-    // post item `it` to this CTA's roles (and, from a pair's first CTA, to the second CTA)
+    // post item `it` to this CTA's roles (and, from a cluster's first CTA, to the others)
     auto push = [&](const WorkItem& it) -> bool {
       const int k = nitem % kItemDepth;
       if (nitem >= kItemDepth) {
@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
               }
             }
           }
-          // the two-tile ring: tile gt reuses the slots of tile gt - 2 (a pair: in both CTAs)
+          // the two-tile ring: tile gt reuses the slots of tile gt - 2 (a cluster: in every CTA)
           if (lane == 0) TL(0, 1);
           if (gt >= 2 && gt - 2 != t_waited) {
             const uint32_t par = static_cast<uint32_t>((gt - 2) >> 1) & 1u;
@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
 #pragma unroll 1
           for (int b = 0; b < NB; ++b, ++pos) {
             const int slot = static_cast<int>(pos % R);
-            // the slot's whole tile lands here (a pair: half from each CTA's boxes)
+            // the slot's whole tile lands here (a cluster: a share from each CTA's boxes)
             const uint32_t bytes = kSlotBytes + (b == NB - 1 ? static_cast<uint32_t>(kTile * 16) : 0u);
             if (lane == 0) mbar_arrive_expect_tx(&full[slot], bytes);
             __syncwarp();
@@ -452,10 +452,11 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
       (void)push(e);
     }
     if (kCl > 1) {
-      // the other producer's issued positions reach this CTA's drain (after the final cluster
-      // barrier, when neither producer issues any more)
-      if (lane == 0) st_cluster_u64(mapa_shared(peer_pos, crank ^ 1u), static_cast<uint64_t>(pos));
-      if (lane == 0) *reinterpret_cast<int64_t*>(smem + C::kMisc + 24) = pos;
+      // every CTA's drain learns the positions this producer issued (it runs after the final
+      // cluster barrier, when no producer issues any more)
+      if (lane == 0)
+        for (int r = 0; r < kCl; ++r)
+          st_cluster_u64(mapa_shared(&cl_pos[crank], static_cast<uint32_t>(r)), static_cast<uint64_t>(pos));
     } else if (lane == 0) {     // never leave copies in flight behind us
       volatile int no_abort[2] = {0, 0};
       const int64_t first = pos > R ? pos - R : 0;
@@ -932,7 +933,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
                         (t > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&pv_done[gt & 1]);
-          // pair: this CTA's share of "tile gt's slots are free", in both CTAs
+          // cluster: this CTA's share of "tile gt's slots are free", in every CTA
           if (kCl > 1) mma_commit_mc(&ring_free[gt & 1], kMask);
           TL(2, 4);
         }
@@ -1031,14 +1032,14 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
   tc_fence_before();
   __syncthreads();
   if (kCl > 1) {
-    // pair: both producers have stopped issuing; wait (bounded) until every copy that either
-    // issued into this CTA's ring has landed, so that no copy targets it once it exits.  A
-    // position that one producer never issued (after an abort) keeps its phase open: the wait
-    // then runs to its limit, by which time the other copies of that position have landed.
+    // cluster: every producer has stopped issuing; wait (bounded) until every copy that any
+    // of them issued into this CTA's ring has landed, so that no copy targets it once it exits.
+    // A position that one producer never issued (after an abort) keeps its phase open: the
+    // wait then runs to its limit, by which time the other copies of that position have landed.
     cluster_sync();
     if (tid == 0) {
-      const int64_t own = *reinterpret_cast<int64_t*>(smem + C::kMisc + 24);
-      const int64_t hi = max(own, *peer_pos);
+      int64_t hi = 0;
+      for (int r = 0; r < kCl; ++r) hi = max(hi, cl_pos[r]);
       const int64_t first = hi > R ? hi - R : 0;
       volatile int drain[2] = {0, 0};
       for (int64_t q = first; q < hi; ++q)

@@ -189,8 +189,9 @@ struct DsParams;
 // boxes for the scales).
 cudaError_t launch_ds_sparse(const DsParams& p, int grid, cudaStream_t stream);
 cudaError_t launch_ds_paged(const DsParams& p, const void* tkv, const void* tsc, int grid, cudaStream_t stream);
-cudaError_t launch_ds_paged_pairs(const DsParams& p, const void* tkv, const void* tsc, int pairs, cudaStream_t stream);
-int ds_pair_capacity();
+cudaError_t launch_ds_paged_clusters(const DsParams& p, const void* tkv, const void* tsc, int size, int clusters,
+                                     cudaStream_t stream);
+int ds_cluster_capacity(int size);
 cudaError_t launch_paged_tma_bf16(int nq, const PagedParams& p, const void* tkv, const void* tq, int grid,
                                   cudaStream_t stream);
 cudaError_t launch_paged_tma_fp8(int nq, const PagedParams& p, const void* tkv, const void* tq, int grid,
