@@ -533,9 +533,7 @@ def run_native(args, rank, world, dist):
         "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded numpy)",
         "config": dict(head["config"], l2="flushed between steps (256 MiB write, outside the timed events)",
-                       parallelism="replicas" if world > 1 else "single GPU",
-                       config_index_reading="BASELINE configs 2-4 read 0-based: sparse prefill, fp8 spec-verify, "
-                                            "ds_mla H=96 decode"),
+                       parallelism="replicas" if world > 1 else "single GPU"),
         "query_rows_per_s": head["query_rows_per_s"], "row_heads_per_s": head["row_heads_per_s"],
         "pct_of_hbm_peak": head["pct_of_hbm_peak"],
         "roofline": head["roofline"], "e2e": head["e2e"], "gpu_launches": head["gpu_launches"],
