@@ -64,6 +64,15 @@ def peaks():
         return 6800.0, "fallback"
 
 
+def bf16_peak():
+    """Dense bf16 tensor peak in TFLOP/s (measured burst figure when present)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured bf16_tflops"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 # ------------------------------------------------------------------------------------ workloads
 
 class Work:
@@ -114,6 +123,13 @@ class Work:
             self.dtype = {0: "bf16 (kind::f16 MMA, fp32 accumulate)",
                           1: "fp8 e4m3 operands (kind::f8f6f4 MMA, fp32 accumulate)",
                           2: "fp8_ds_mla: e4m3 codes (kind::f8f6f4) + bf16 rope (kind::f16), fp32 accumulate"}[c.fmt]
+        # the dense contraction per (query row, head, visible key): 2 * 576 (QK) + 2 * 512 (PV)
+        if self.kind == "sparse":
+            visible = int(np.count_nonzero((c.indices >= 0) & (c.indices < c.records.shape[0])))
+        else:
+            L = c.seq_lens.astype(np.int64)
+            visible = int(sum(np.clip(L - c.q_len + i + 1, 0, None).sum() for i in range(c.q_len)))
+        self.flops = visible * self.heads * (2 * 576 + 2 * 512)
         self.epi_bytes = 0
         if name == "decode_bf16_epilogue":
             B, H = self.epi.ql_nope.shape[:2]
@@ -477,6 +493,11 @@ def measure(w: Work, dev, flush, steps: int, warmup: int, min_ms: float, dist, w
                      "bytes_per_launch": w.attn_bytes},
         "e2e": {"value": round(job_rate(world, w.step_bytes, K, e2e_ms) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": int(r.h2d), "d2h_bytes_per_step": int(r.d2h), "mode": r.e2e_mode},
+        # tensor-core check: the dense contraction of the launch (rows x heads x visible keys x
+        # (2*576 + 2*512) FLOP) over the attention kernel's time, against the bf16 dense peak
+        "tensor": {"flops_per_launch": int(w.flops), "achieved_tflops": round(w.flops / (attn_avg * 1e-3) / 1e12, 2),
+                   "bf16_peak_tflops": bf16_peak()[0], "frac_of_bf16_peak":
+                       round(w.flops / (attn_avg * 1e-3) / 1e12 / bf16_peak()[0], 4), "peak_source": bf16_peak()[1]},
         "gpu_launches": int(r.launches_per_step * K),
         "dtype": w.dtype,
         "config": dict(w.cfg, step_launch="cuda graph replay" if graph is not None else "direct calls"),
@@ -533,10 +554,13 @@ def run_native(args, rank, world, dist):
         "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded numpy)",
         "config": dict(head["config"], l2="flushed between steps (256 MiB write, outside the timed events)",
-                       parallelism="replicas" if world > 1 else "single GPU"),
+                       parallelism="replicas" if world > 1 else "single GPU",
+                       targets="the three large workloads: sparse prefill (this line), fp8 spec-verify and "
+                               "ds_mla H=96 decode (per_config)"),
         "query_rows_per_s": head["query_rows_per_s"], "row_heads_per_s": head["row_heads_per_s"],
         "pct_of_hbm_peak": head["pct_of_hbm_peak"],
-        "roofline": head["roofline"], "e2e": head["e2e"], "gpu_launches": head["gpu_launches"],
+        "roofline": head["roofline"], "tensor": head["tensor"], "e2e": head["e2e"],
+        "gpu_launches": head["gpu_launches"],
         "clocks": clocks,
     }
     if "cpu_baseline" in head:
