@@ -81,3 +81,32 @@ def test_sparse_graph_replays_bit_exact(m):
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(out, ref_out) and torch.equal(res["lse"], ref_lse)
+
+
+def test_ds_cluster_decode_graph_replays_bit_exact(m):
+    """The fp8_ds_mla decode of 96 heads runs as 2-CTA clusters (multicast page tiles), with
+    split-K and the merge: captured and replayed, it gives the direct call's bits."""
+    case = synth.paged_case(61, synth.DS_MLA, B=6, q_len=1, H=96, L_lo=1500, L_hi=5000, block_size=64,
+                            max_context=32768)
+    q, cache = t_bf16(case.q.view(np.uint16)), t_u8(case.cache)
+    bt, sl = t_i32(case.block_table), t_i32(case.seq_lens)
+    ws = torch.empty(max(m.paged_decode_workspace_size(6, 1, 96, 32768), 256), dtype=torch.uint8, device="cuda")
+    assert ws.numel() > 256
+    out = torch.empty((6, 96, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((6, 96), dtype=torch.float32, device="cuda")
+
+    def step():
+        m.paged_decode(q, cache, bt, sl, fmt=synth.DS_MLA, max_context=32768, softmax_scale=case.softmax_scale,
+                       out=out, workspace=ws, lse=lse)
+
+    step()
+    torch.cuda.synchronize()
+    ref_out, ref_lse = out.clone(), lse.clone()
+    g = capture(step)
+    for _ in range(3):
+        out.zero_()
+        lse.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_out) and torch.equal(lse, ref_lse)
+    assert m.read_device_errors() == 0
