@@ -1,4 +1,5 @@
-"""Seeded random shapes against the fp64 oracle: the paged decode over all three cache
+"""Seeded random shapes against the fp64 oracle: the decode epilogue (bit-exact), the paged
+decode over all three cache
 formats (head counts 1..128, q_len 1..5, block sizes 1..256, zero-length and short requests,
 split-K from a max_context above the lengths, padded entry pitch, fp8 scales), and the
 sparse forward on both kernel designs (head counts 1..128, ragged and empty rows, masked
@@ -84,3 +85,18 @@ def test_sparse_random_shapes(m, seed, kern):
     assert_attn_close(o, ro, f"sparse {a}")
     assert_lse_close(l, rl, f"sparse {a}")
     assert m.read_device_errors() == 0
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_epilogue_random_shapes(m, seed):
+    """The decode epilogue (q concat + latent insert), bit-exact: random format, batch, head
+    count, block size, pitch, RoPE on / off and skipped slots."""
+    from tests.test_gpu_epilogue import run_both
+    rng = np.random.default_rng(50_000 + seed)
+    fmt = int(rng.integers(0, 3))
+    B = int(rng.integers(1, 65))
+    H = int(rng.choice([1, 2, 5, 16, 33, 64, 128]))
+    bs = int(rng.choice([1, 4, 16, 64]))
+    nb = int(np.ceil(B / bs)) + int(rng.integers(0, 5))
+    run_both(m, fmt, B=B, H=H, bs=bs, nb=nb, seed=60_000 + seed, rope=bool(rng.integers(0, 2)),
+             entry_pad=int(rng.choice([0, 16, 48])), neg_slot=bool(rng.integers(0, 2)))
