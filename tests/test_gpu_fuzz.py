@@ -1,10 +1,9 @@
-"""Seeded random shapes against the fp64 oracle: the decode epilogue (bit-exact), the paged
-decode over all three cache
+"""Seeded random shapes against the fp64 oracle: the paged decode over all three cache
 formats (head counts 1..128, q_len 1..5, block sizes 1..256, zero-length and short requests,
-split-K from a max_context above the lengths, padded entry pitch, fp8 scales), and the
-sparse forward on both kernel designs (head counts 1..128, ragged and empty rows, masked
-and duplicate indices).  Each case is sized so that the oracle finishes in well under a
-second."""
+split-K from a max_context above the lengths, padded entry pitch, fp8 scales), the sparse
+forward on both kernel designs (head counts 1..128, ragged and empty rows, masked and
+duplicate indices) and the decode epilogue (bit-exact).  Each case is sized so that the
+oracle finishes in well under a second."""
 import numpy as np
 import pytest
 import torch
