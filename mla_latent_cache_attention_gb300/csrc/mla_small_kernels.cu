@@ -1,5 +1,6 @@
 // mla_small_kernels.cu -- the memory-bound kernels around the attention core:
-//   * the decode epilogue (q concat + latent insert), one CTA per (token, 4 heads);
+//   * the decode epilogue (q concat + latent insert), one CTA per (token, 4 heads) and one
+//     per token for the insert;
 //   * the split-K merge of partial attentions by their log-sum-exp;
 //   * gather-and-dequantise of cache entries (a test aid with the kernels' addressing).
 #include <cuda_bf16.h>
@@ -99,25 +100,40 @@ __device__ __forceinline__ void insert_latent(uint8_t* ent, const uint16_t* __re
   }
 }
 
-// Grid (B, ceil(H / 4)): CTA (b, g) builds the query rows of heads 4g..4g+3 of token b; the
-// CTAs with g == 0 also insert token b's latent.  Loads go through restrict-qualified
-// pointers in batches of 8 so that they are all in flight before the stores.
+// Grid (B, ceil(H / 4) + 1): CTA (b, g < ceil(H / 4)) builds the query rows of heads
+// 4g..4g+3 of token b; CTA (b, ceil(H / 4)) inserts token b's latent, in parallel with them.
+// Loads go through restrict-qualified pointers in batches of 8 so that they are all in
+// flight before the stores.
 template <int F>
 __global__ void __launch_bounds__(128) mla_epilogue_kernel(const EpiParams p) {
   const int b = blockIdx.x, g = blockIdx.y, tid = threadIdx.x;
   // the decode launched next (a programmatic dependent) may be scheduled now; it waits for
   // this grid before it reads the query and the cache
   if (tid == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const bool inserter = g == static_cast<int>(gridDim.y) - 1;
+  const int64_t slot = inserter ? p.slot_mapping[b] : -1;     // loaded with the position
   const float qinv = (F == 1) ? *p.q_scale_inv : 1.f;
   const float cinv = (F == 1) ? *p.cache_scale_inv : 1.f;
   const float* __restrict__ cs = nullptr;
   if (p.positions) {
     int64_t pos = p.positions[b];
     if (pos < 0 || pos >= p.max_position) {
-      if (tid == 0 && g == 0) set_device_error(p.err, 8u);
+      if (tid == 0 && inserter) set_device_error(p.err, 8u);
       pos = pos < 0 ? 0 : p.max_position - 1;
     }
     cs = p.cos_sin + pos * 64;
+  }
+  if (inserter) {
+    // ---- latent insert
+    if (slot < 0) return;
+    const int64_t blk = slot / p.block_size;
+    if (blk >= p.num_blocks) {
+      if (tid == 0) set_device_error(p.err, 4u);
+      return;
+    }
+    insert_latent<F>(p.cache + blk * p.block_stride + (slot % p.block_size) * p.entry_stride, p.kv_c + b * p.kv_s0,
+                     p.k_pe + b * p.kp_s0, cs, cinv, tid);
+    return;
   }
   const int H = p.H;
   const int h_lo = 4 * g, h_hi = min(H, 4 * g + 4);
@@ -171,17 +187,6 @@ __global__ void __launch_bounds__(128) mla_epilogue_kernel(const EpiParams p) {
       q16[o + 1] = bf16_bits(y1);
     }
   }
-  if (g != 0) return;
-  // ---- latent insert
-  const int64_t slot = p.slot_mapping[b];
-  if (slot < 0) return;
-  const int64_t blk = slot / p.block_size;
-  if (blk >= p.num_blocks) {
-    if (tid == 0) set_device_error(p.err, 4u);
-    return;
-  }
-  insert_latent<F>(p.cache + blk * p.block_stride + (slot % p.block_size) * p.entry_stride, p.kv_c + b * p.kv_s0,
-                   p.k_pe + b * p.kp_s0, cs, cinv, tid);
 }
 
 // ------------------------------------------------------------------------------------------
@@ -442,7 +447,7 @@ __global__ void mla_gather_kernel(const GatherParams p) {
 
 // ------------------------------------------------------------------------------------------
 cudaError_t launch_epilogue(int fmt, const EpiParams& p, int B, cudaStream_t stream) {
-  const dim3 grid(B, (p.H + 3) / 4);
+  const dim3 grid(B, (p.H + 3) / 4 + 1);
   if (fmt == 0)
     mla_epilogue_kernel<0><<<grid, 128, 0, stream>>>(p);
   else if (fmt == 1)
