@@ -171,7 +171,8 @@ class GpuRunner:
             self.out = torch.empty((self.q.shape[0], c.H, 512), dtype=torch.bfloat16, device=dev)
             need = m.paged_decode_workspace_size(c.seq_lens.size, c.q_len, c.H, c.max_context)
             self.ws = torch.empty(max(need, 256), dtype=torch.uint8, device=dev)
-            self.launches_per_step = 1 + (1 if need > 0 else 0)
+            # the attention kernel, and with split-K the scheduler reset and the merge
+            self.launches_per_step = 1 + (2 if need > 0 else 0)
             if w.name == "decode_bf16_epilogue":
                 e = w.epi
                 b16 = lambda a: to_dev(a.view(np.int16), torch, dev).view(torch.bfloat16)
