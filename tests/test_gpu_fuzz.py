@@ -202,3 +202,35 @@ def test_absorbed_contractions_random_shapes(m, seed):
     g = synth.normal_bf16_bits(rng, (B, H * V)) if gated else None
     out = m.v_up_proj(t_bf16(lat), t_bf16(wv), None if g is None else t_bf16(g))
     check(bf16_bits(out), lat, wv, oracle.head_bmm(lat, wv, g), gate_terms=3 if gated else 1)
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_sparse_extras_random_shapes(m, seed):
+    """The sparse forward's extras (per-head sink, second key segment, kv_splits) in random
+    combinations over random row lengths, head counts and masks."""
+    from tests.test_gpu_sparse_ext import run, second_segment
+    rng = np.random.default_rng(95_000 + seed)
+    T = int(rng.integers(1, 24))
+    H = int(rng.choice([1, 5, 16, 20, 64, 128]))
+    hi = int(max(2, min(1500, WORK_CAP / (T * H * 1088 * 2))))
+    lens = rng.integers(0, hi, size=T)
+    N = int(rng.integers(1, 2500))
+    c = synth.sparse_case(96_000 + seed, T=T, H=H, N=N, per_row=1, p_invalid=0.0, replace=True)
+    c.indptr = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+    c.indices = rng.integers(0, N, size=c.indptr[-1]).astype(np.int32)
+    c.indices[rng.random(c.indices.size) < float(rng.choice([0.0, 0.1, 0.6]))] = -1
+    c.q = synth.normal_bf16_bits(rng, (T, H, 576))
+    sink = None
+    if rng.integers(0, 2):
+        sink = rng.uniform(-5.0, 20.0, size=H).astype(np.float32)
+        sink[rng.random(H) < 0.2] = -np.inf
+    seg = second_segment(97_000 + seed, T, N2=int(rng.integers(1, 800)), hi=hi) if rng.integers(0, 2) else None
+    kv_splits = int(rng.choice([1, 1, 2, 3, 7]))
+    if sink is None and seg is None and kv_splits == 1:
+        kv_splits = 2
+    m.read_device_errors()
+    o, l, ro, rl = run(m, c, sink=sink, seg=seg, kv_splits=kv_splits)
+    what = f"T={T} H={H} sink={sink is not None} seg={seg is not None} kv_splits={kv_splits}"
+    assert_attn_close(o, ro, what)
+    assert_lse_close(l, rl, what)
+    assert m.read_device_errors() == 0
