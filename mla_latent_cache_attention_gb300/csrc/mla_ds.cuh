@@ -146,7 +146,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
   uint64_t* p_full = bars + R + 4;
   uint64_t* q_full = bars + R + 5;
   uint64_t* fin = bars + R + 6;
-  uint64_t* s_free = bars + R + 7;        // the softmax has read S
+  uint64_t* s_free = bars + R + 7;        // the softmax warps have read S (four arrivals)
   uint64_t* item_full = bars + R + 8;
   uint64_t* item_empty = item_full + kItemDepth;
   uint64_t* fin_pv = item_empty + kItemDepth;
@@ -173,7 +173,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
     mbar_init(q_full, 1);
     mbar_init(fin, 1);
     mbar_init(fin_pv, 1);
-    mbar_init(s_free, 1);
+    mbar_init(s_free, 4);     // one arrival per softmax warp
     for (int k = 0; k < kItemDepth; ++k) {
       mbar_init(&item_full[k], 1);
       // the cluster's first CTA also waits for the other producers to have read item k
@@ -646,6 +646,11 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
           float sr[16];
           tmem_ld16(sb + 128, sr);
           tmem_ld_wait();
+          // all of S is in this warp's registers: release its lanes of the buffer to the next
+          // QK now, ahead of the combine and the vote (one arrival per softmax warp)
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(s_free);
 #pragma unroll
           for (int c = 0; c < NQ; ++c) s[c] = rv ? p.sig2 * fmaf(colf[c], s[c], sr[c]) : -CUDART_INF_F;
         }
@@ -669,7 +674,6 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         tc_fence_before();
         const bool rare = named_bar_or(1, NT, need || !w);
         if (stid == 0) TL(3, rare ? 6 : 5);
-        if (stid == 0) mbar_arrive(s_free);     // S is in registers: the next QK may overwrite it
         bool pv_waited = false;
         if (rare) {
           ok = named_bar_and(1, NT, w);
