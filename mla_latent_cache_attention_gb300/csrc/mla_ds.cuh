@@ -857,6 +857,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
       const int64_t flat0 = static_cast<int64_t>(it.b) * p.q_len * p.H + cgb;
       const int ncol = min(NQ, p.cols - cgb);
       const int qi0 = cgb / p.H, h0 = cgb % p.H;
+      const int64_t o_wrap = p.o_s0b - static_cast<int64_t>(p.H) * p.o_s1b;
 #pragma unroll 1
       for (int j = 0; j < 4; ++j) {
         float o[16];
@@ -871,17 +872,28 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         }
         const float ur = (rj[j] > 0.f) ? 1.f / rj[j] : 0.f;     // exact: a power of two
         const int d = 128 * j + row;
-        if (final_out) {
-          int qi = qi0, h = h0;
-          uint8_t* base = p.out + static_cast<int64_t>(it.b) * p.q_len * p.o_s0b + 2 * d;
+        if (final_out && (kSparse || p.q_len == 1)) {
+          // One query token per row (always so for the sparse rows): the group's columns are
+          // heads cgb .. cgb + ncol - 1 of one token and never wrap.
+          uint8_t* ptr = p.out + static_cast<int64_t>(it.b) * p.o_s0b + static_cast<int64_t>(cgb) * p.o_s1b + 2 * d;
 #pragma unroll
           for (int c = 0; c < NQ; ++c) {
-            if (c < ncol)
-              *reinterpret_cast<__nv_bfloat16*>(base + qi * p.o_s0b + h * p.o_s1b) =
-                  __float2bfloat16_rn(o[c] * ur * inv[c]);
+            if (c < ncol) *reinterpret_cast<__nv_bfloat16*>(ptr) = __float2bfloat16_rn(o[c] * ur * inv[c]);
+            ptr += p.o_s1b;
+          }
+        } else if (final_out) {
+          // Running pointer over (token, head): column c + 1 is the next head, or head 0 of the
+          // next token after head H - 1 (no per-store index multiply).
+          uint8_t* ptr = p.out + (static_cast<int64_t>(it.b) * p.q_len + qi0) * p.o_s0b +
+                         static_cast<int64_t>(h0) * p.o_s1b + 2 * d;
+          int h = h0;
+#pragma unroll
+          for (int c = 0; c < NQ; ++c) {
+            if (c < ncol) *reinterpret_cast<__nv_bfloat16*>(ptr) = __float2bfloat16_rn(o[c] * ur * inv[c]);
+            ptr += p.o_s1b;
             if (++h == p.H) {
               h = 0;
-              ++qi;
+              ptr += o_wrap;
             }
           }
         } else {

@@ -982,6 +982,7 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
       // row * H + head is b * q_len * H + cg
       const int64_t flat0 = static_cast<int64_t>(it.b) * p.q_len * p.H + cgb;
       const int ncol = min(NC, p.cols - cgb);
+      const int64_t o_wrap = p.o_s0b - static_cast<int64_t>(p.H) * p.o_s1b;
       // O / l in slices of 16 columns (keeps the epilogue's live registers low)
 #pragma unroll 1
       for (int jq = 0; jq < 4 * (NC / 16); ++jq) {
@@ -996,16 +997,19 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
         }
         const int d = 128 * j + row;
         if (final_out) {
-          int qi = (cgb + cs) / p.H, h = (cgb + cs) % p.H;
-          uint8_t* base = p.out + static_cast<int64_t>(it.b) * p.q_len * p.o_s0b + 2 * d;
+          // Running pointer over (token, head): the next column is the next head, or head 0 of
+          // the next token after head H - 1 (no per-store index multiply).
+          int h = (cgb + cs) % p.H;
+          uint8_t* ptr = p.out + (static_cast<int64_t>(it.b) * p.q_len + (cgb + cs) / p.H) * p.o_s0b +
+                         static_cast<int64_t>(h) * p.o_s1b + 2 * d;
 #pragma unroll
           for (int c = 0; c < 16; ++c) {
             const float iv = __shfl_sync(0xFFFFFFFFu, inv_l, cs + c);
-            if (cs + c < ncol)
-              *reinterpret_cast<__nv_bfloat16*>(base + qi * p.o_s0b + h * p.o_s1b) = __float2bfloat16_rn(o[c] * iv);
+            if (cs + c < ncol) *reinterpret_cast<__nv_bfloat16*>(ptr) = __float2bfloat16_rn(o[c] * iv);
+            ptr += p.o_s1b;
             if (++h == p.H) {
               h = 0;
-              ++qi;
+              ptr += o_wrap;
             }
           }
         } else {
