@@ -41,7 +41,7 @@ enum : int { kBF16 = 0, kFP8 = 1, kDS = 2 };
 #ifdef MLA_TIMELINE
 // Debug timeline (never in the product build): per CTA (first 4) and role, a log of
 // (event id, %globaltimer) pairs.  Store-only: the marking thread counts in a register.
-constexpr int kTlCtas = 4, kTlRoles = 4, kTlEvents = 512;
+constexpr int kTlCtas = 4, kTlRoles = 12, kTlEvents = 512;
 __device__ unsigned long long g_tl[kTlCtas][kTlRoles][kTlEvents][2];
 __device__ int g_tl_n[kTlCtas][kTlRoles];
 __device__ __forceinline__ void tl_mark(int role, int ev, int& n) {

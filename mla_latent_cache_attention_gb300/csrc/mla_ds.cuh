@@ -287,16 +287,17 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
           const int gt = pv_g + pv_t;
           if (mbar_test_wait(p_full, static_cast<uint32_t>(gt) & 1u)) {
             tc_fence_after();
+            TL(0, 1);
+            const uint64_t aT = desc_add(dV0, (((gt & 1) * NB) * kSlotBytes) >> 4);
+            const uint32_t acc0 = pv_t > 0 ? 1u : 0u;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const uint64_t aV = dV0 + ((((gt & 1) * NB + j) * kSlotBytes) >> 4);
-              const uint64_t bP = dP0 + ((j * kTile * 64) >> 4);
+            for (int j = 0; j < 4; ++j)
 #pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                mma_f8_ss(tmem + C::kTmemO + 64 * j, aV + ((kk * 4096) >> 4), bP + ((kk * 2048) >> 4), kIdPv,
-                          (pv_t > 0 || kk > 0) ? 1u : 0u);
-            }
+                mma_f8_ss(tmem + C::kTmemO + 64 * j, desc_add(aT, (j * kSlotBytes + kk * 4096) >> 4),
+                          desc_add(dP0, (j * kTile * 64 + kk * 2048) >> 4), kIdPv, kk > 0 ? 1u : acc0);
             mma_commit(&pv_done[gt & 1]);
+            TL(0, 2);
             ++pv_t;
             prog = true;
           }
@@ -483,6 +484,32 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         tc_fence_after();
         TL(2, 5);
         const uint32_t dS = tmem + C::kS;
+        if (kSparse) {
+          // the gather warps arrive on the tile's first slot barrier only, after all their
+          // stores to the tile: one wait covers the five slots (fewer instructions for a thread
+          // that shares its sub-partition with busy warps).  The MMAs stay in a per-slot loop:
+          // issuing all 20 in a straight line measured slower.
+          const int s0 = (gt & 1) * NB;
+          if (!mbar_wait(&full[s0], static_cast<uint32_t>(gt >> 1) & 1u, abort_flag)) return false;
+          tc_fence_after();
+#pragma unroll 1
+          for (int b = 0; b < NB; ++b) {
+            const uint64_t aK = dK0 + (((s0 + b) * kSlotBytes) >> 4);
+            if (b < 4) {
+              const uint64_t bQ = dQ0 + ((b * 32 * 128) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f8_ss(dS + 32 * b, aK + ((kk * 32) >> 4), bQ + ((kk * 32) >> 4), kIdNope, kk > 0 ? 1u : 0u);
+            } else {
+#pragma unroll
+              for (int kk = 0; kk < 4; ++kk)
+                mma_f16_ss(dS + 128, aK + ((kk * 32) >> 4), dQr + ((kk * 32) >> 4), kIdRope, kk > 0 ? 1u : 0u);
+            }
+          }
+          mma_commit(&s_full[0]);
+          TL(2, 2);
+          return true;
+        }
 #pragma unroll 1
         for (int b = 0; b < NB; ++b) {
           const int slot = slot_of(gt, b);
@@ -994,7 +1021,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
             }
           }
         }
-        if (warp == 6 && lane == 0) TL(1, 1);
+        if (lane == 0) TL(4 + gw, 1);
         uint4 v[21];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -1015,7 +1042,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
           ok = false;
           break;
         }
-        if (warp == 6 && lane == 0) TL(1, 2);
+        if (lane == 0) TL(4 + gw, 2);
         {
           uint8_t* codes = ring + ((gt & 1) * NB + (lane >> 3)) * kSlotBytes;
 #pragma unroll
@@ -1035,9 +1062,8 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         if (lane < 16) vrow[(gt & 1) * kTile + rbase + lane] = (idx >= 0) ? 1 : 0;
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0)
-          for (int b = 0; b < NB; ++b) mbar_arrive(&full[(gt & 1) * NB + b]);
-        if (warp == 6 && lane == 0) TL(1, 3);
+        if (lane == 0) mbar_arrive(&full[(gt & 1) * NB]);     // the tile's one full barrier
+        if (lane == 0) TL(4 + gw, 3);
       }
       g += it.ntiles;
     }

@@ -322,6 +322,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint
 }
 constexpr uint32_t kSwizzleNone = 0, kSwizzle128B = 2;
 
+// Descriptor d advanced by c (address units of 16 bytes): a 32-bit add of the low word.  The
+// address field (bits 0..13) holds a shared-memory address below 256 KB, so it never carries
+// into the fields above it, and one integer add replaces a 64-bit one per MMA.
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t c) {
+  return (d & 0xFFFFFFFF00000000ull) | static_cast<uint32_t>(static_cast<uint32_t>(d) + c);
+}
+
 // Instruction descriptor of kind::f16: fp32 accumulator, A / B type (0 = f16, 1 = bf16),
 // A / B major-ness (0 = K-major, 1 = MN-major), N >> 3 at bit 17, M >> 4 at bit 24.
 __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, int a_bf16, int b_bf16, int a_mn,
