@@ -113,6 +113,22 @@ __device__ __forceinline__ int e4m3_fit_exponent(float a) {
   return e;
 }
 
+// PV of tile gt: O_j (+)= V_j^T P_j for the four value tiles j (V_j: ring slot j of the tile's
+// half of the ring; P_j: 128 keys x 64 weights).  The descriptors advance by 32-bit adds: the
+// issuing thread shares its sub-partition with busy warps, and fewer instructions per MMA
+// measured faster.
+template <int NB>
+__device__ __forceinline__ void ds_issue_pv(uint32_t tmem_o, uint64_t dV0, uint64_t dP0, uint32_t id, int gt, bool first) {
+  const uint64_t aT = desc_add(dV0, (((gt & 1) * NB) * kSlotBytes) >> 4);
+  const uint32_t acc0 = first ? 0u : 1u;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      mma_f8_ss(tmem_o + 64 * j, desc_add(aT, (j * kSlotBytes + kk * 4096) >> 4),
+                desc_add(dP0, (j * kTile * 64 + kk * 2048) >> 4), id, kk > 0 ? 1u : acc0);
+}
+
 // kCl = 2, 3 or 6 (paged source only): the kernel runs as clusters of kCl CTAs.  The CTAs of a
 // cluster take the same item (request, split) for kCl adjacent column groups: the cluster's
 // first CTA takes the tickets and passes each item to the others through a mailbox in its
@@ -288,14 +304,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
           if (mbar_test_wait(p_full, static_cast<uint32_t>(gt) & 1u)) {
             tc_fence_after();
             TL(0, 1);
-            const uint64_t aT = desc_add(dV0, (((gt & 1) * NB) * kSlotBytes) >> 4);
-            const uint32_t acc0 = pv_t > 0 ? 1u : 0u;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_f8_ss(tmem + C::kTmemO + 64 * j, desc_add(aT, (j * kSlotBytes + kk * 4096) >> 4),
-                          desc_add(dP0, (j * kTile * 64 + kk * 2048) >> 4), kIdPv, kk > 0 ? 1u : acc0);
+            ds_issue_pv<NB>(tmem + C::kTmemO, dV0, dP0, kIdPv, gt, pv_t == 0);
             mma_commit(&pv_done[gt & 1]);
             TL(0, 2);
             ++pv_t;
@@ -966,15 +975,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
           }
           tc_fence_after();
           TL(2, 3);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint64_t aV = dV0 + ((((gt & 1) * NB + j) * kSlotBytes) >> 4);
-            const uint64_t bP = dP0 + ((j * kTile * 64) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_f8_ss(tmem + C::kTmemO + 64 * j, aV + ((kk * 4096) >> 4), bP + ((kk * 2048) >> 4), kIdPv,
-                        (t > 0 || kk > 0) ? 1u : 0u);
-          }
+          ds_issue_pv<NB>(tmem + C::kTmemO, dV0, dP0, kIdPv, gt, t == 0);
           mma_commit(&pv_done[gt & 1]);
           // cluster: this CTA's share of "tile gt's slots are free", in every CTA
           if (kCl > 1) mma_commit_mc(&ring_free[gt & 1], kMask);

@@ -265,6 +265,44 @@ __device__ __forceinline__ float2 e4m3x2_to_float2(uint32_t v) {
   return __half22float2(*reinterpret_cast<const __half2*>(&h));
 }
 
+// PV of tile gt (its first ring position is gt * NB): O_j (+)= V_j^T P for the four value
+// blocks j.  The slot index wraps by one subtraction and the descriptors advance by 32-bit
+// adds: the issuing thread shares its sub-partition with busy warps, so it is kept to a few
+// instructions per MMA.  bf16 takes V_j from the slot pair (2j, 2j + 1): an even ring length
+// keeps a pair from wrapping.
+template <class C, int F, int NQ>
+__device__ __forceinline__ void paged_issue_pv(uint32_t tmem, uint64_t dV0, uint64_t dP0, uint64_t* empty, int gt,
+                                               bool first) {
+  constexpr int R = C::kR, NB = C::kNB, KM = C::KM;
+  constexpr uint32_t kIdPv = F == kBF16 ? idesc_f16(128, NQ, 1, 1, 1, 1) : idesc_e4m3(128, NQ, 1, 1);
+  const int s0 = static_cast<int>((static_cast<int64_t>(gt) * NB) % R);
+  const uint32_t acc0 = first ? 0u : 1u;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t dO = tmem + C::kTmemO + j * NQ;
+    int sa = s0 + (F == kBF16 ? 2 * j : j);
+    if (sa >= R) sa -= R;
+    const uint64_t aV = desc_add(dV0, static_cast<uint32_t>(sa) * (C::kSlot >> 4));
+    if (F == kBF16) {
+#pragma unroll
+      for (int kk = 0; kk < KM / 16; ++kk)
+        mma_f16_ss(dO, desc_add(aV, (kk * 2048) >> 4), desc_add(dP0, (kk * NQ * 32) >> 4), kIdPv, kk > 0 ? 1u : acc0);
+      if (C::kSlotCommits) {
+        mma_commit(&empty[sa]);
+        mma_commit(&empty[sa + 1]);
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < KM / 32; ++kk) {
+        const uint64_t pb = desc_add(dP0, (kk * NQ * 32) >> 4);
+        mma_f8_ss(dO, desc_add(aV, (kk * 4096) >> 4), pb, kIdPv, kk > 0 ? 1u : acc0);
+        mma_f8_ss(dO, desc_add(aV, (kk * 4096) >> 4), desc_add(pb, (KM * NQ) >> 4), kIdPv, 1u);
+      }
+      if (C::kSlotCommits) mma_commit(&empty[sa]);
+    }
+  }
+}
+
 template <int F, int NQ>
 __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
     mla_paged_tma_kernel(const __grid_constant__ PagedParams p, const __grid_constant__ CUtensorMap tm_kv,
@@ -571,7 +609,6 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
       constexpr uint32_t kPLbo = F == kBF16 ? NQ * 16 : NQ * 8;   // 8-key groups of P
       const uint64_t dP0 = smem_desc(p_a, kPLbo, 128, kSwizzleNone);
       constexpr uint32_t kIdQk = F == kBF16 ? idesc_f16(KM, NQ, 1, 1, 0, 0) : idesc_e4m3(KM, NQ, 0, 0);
-      constexpr uint32_t kIdPv = F == kBF16 ? idesc_f16(128, NQ, 1, 1, 1, 1) : idesc_e4m3(128, NQ, 1, 1);
       auto slot_of = [&](int gt, int b) -> int { return static_cast<int>((static_cast<int64_t>(gt) * NB + b) % R); };
       auto use_of = [&](int gt, int b) -> uint32_t {
         return static_cast<uint32_t>(((static_cast<int64_t>(gt) * NB + b) / R) & 1);
@@ -583,29 +620,7 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
         if (!mbar_wait(p_full, static_cast<uint32_t>(gt) & 1u, abort_flag)) return false;
         tc_fence_after();
         TL(2, 3);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t dO = tmem + C::kTmemO + j * NQ;
-          if (F == kBF16) {
-            const uint64_t aV = dV0 + ((slot_of(gt, 2 * j) * C::kSlot) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < KM / 16; ++kk)
-              mma_f16_ss(dO, aV + ((kk * 2048) >> 4), dP0 + ((kk * NQ * 32) >> 4), kIdPv, (!first || kk > 0) ? 1u : 0u);
-            if (C::kSlotCommits) {
-              mma_commit(&empty[slot_of(gt, 2 * j)]);
-              mma_commit(&empty[slot_of(gt, 2 * j + 1)]);
-            }
-          } else {
-            const uint64_t aV = dV0 + ((slot_of(gt, j) * C::kSlot) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < KM / 32; ++kk) {
-              const uint64_t pb = dP0 + ((kk * NQ * 32) >> 4);
-              mma_f8_ss(dO, aV + ((kk * 4096) >> 4), pb, kIdPv, (!first || kk > 0) ? 1u : 0u);
-              mma_f8_ss(dO, aV + ((kk * 4096) >> 4), pb + ((KM * NQ) >> 4), kIdPv, 1u);
-            }
-            if (C::kSlotCommits) mma_commit(&empty[slot_of(gt, j)]);
-          }
-        }
+        paged_issue_pv<C, F, NQ>(tmem, dV0, dP0, empty, gt, first);
         mma_commit(&pv_done[gt & 1]);
         TL(2, 4);
         return true;
@@ -621,11 +636,17 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
         if (C::kPvSplit && gt >= 2 &&
             !mbar_wait(&s_free[gt & 1], static_cast<uint32_t>((gt - 2) >> 1) & 1u, abort_flag))
           return false;
+        // ring position gt * NB + b: its slot and the parity of its use, walked per block
+        int slot = slot_of(gt, 0);
+        uint32_t use = use_of(gt, 0);
 #pragma unroll 1
         for (int b = 0; b < NB; ++b) {
-          const int slot = slot_of(gt, b);
+          if (b > 0 && ++slot == R) {
+            slot = 0;
+            use ^= 1u;
+          }
           // wait for the block, but issue the pending PV as soon as its P is ready
-          if (pv_gt >= 0 && !mbar_test_wait(&full[slot], use_of(gt, b))) {
+          if (pv_gt >= 0 && !mbar_test_wait(&full[slot], use)) {
             const uint64_t t0 = globaltimer();
             for (uint32_t spin = 0;; ++spin) {
               if (mbar_test_wait(p_full, static_cast<uint32_t>(pv_gt) & 1u)) {
@@ -633,29 +654,30 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
                 pv_gt = -1;
                 break;
               }
-              if (mbar_try_wait_ns(&full[slot], use_of(gt, b), 200)) break;
+              if (mbar_try_wait_ns(&full[slot], use, 200)) break;
               if ((spin & 15u) == 15u && (*abort_flag || globaltimer() - t0 > kWaitNs)) break;   // the bounded wait below decides
             }
           }
-          if (!mbar_wait(&full[slot], use_of(gt, b), abort_flag)) return false;
+          if (!mbar_wait(&full[slot], use, abort_flag)) return false;
           if (b == 0 || b == NB - 1) TL(2, (b == 0 ? 1000 : 2000) + gt % 1000);
           tc_fence_after();
           if (F == kBF16 && b == 9) {
             if (C::kSlotCommits) mbar_arrive(&empty[slot]);
             continue;
           }
-          const uint64_t aK = dK0 + ((slot * C::kSlot) >> 4);
-          const uint64_t bQ = dQ0 + ((b * NQ * 128) >> 4);
+          const uint64_t aK = desc_add(dK0, static_cast<uint32_t>(slot) * (C::kSlot >> 4));
+          const uint64_t bQ = desc_add(dQ0, static_cast<uint32_t>(b) * (NQ * 128 >> 4));
+          const uint32_t acc0 = b > 0 ? 1u : 0u;
           if (F == kBF16) {
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_f16_ss(dS, aK + ((kk * 32) >> 4), bQ + ((kk * 32) >> 4), kIdQk, (b > 0 || kk > 0) ? 1u : 0u);
+              mma_f16_ss(dS, desc_add(aK, (kk * 32) >> 4), desc_add(bQ, (kk * 32) >> 4), kIdQk, kk > 0 ? 1u : acc0);
           } else {
             const int kk0 = (b == 4) ? 2 : 0;      // block 4 holds elements 448..575; 512.. are new
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
               if (kk >= kk0)
-                mma_f8_ss(dS, aK + ((kk * 32) >> 4), bQ + ((kk * 32) >> 4), kIdQk, (b > 0 || kk > 0) ? 1u : 0u);
+                mma_f8_ss(dS, desc_add(aK, (kk * 32) >> 4), desc_add(bQ, (kk * 32) >> 4), kIdQk, kk > 0 ? 1u : acc0);
           }
         }
         mma_commit(&s_full[gt & 1]);
@@ -707,8 +729,6 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
       const uint64_t dV0 = smem_desc(smem_u32(ring), C::kSlot, 1024, kSwizzle128B);
       constexpr uint32_t kPLbo = F == kBF16 ? NQ * 16 : NQ * 8;   // 8-key groups of P
       const uint64_t dP0 = smem_desc(smem_u32(ps), kPLbo, 128, kSwizzleNone);
-      constexpr uint32_t kIdPv = F == kBF16 ? idesc_f16(128, NQ, 1, 1, 1, 1) : idesc_e4m3(128, NQ, 1, 1);
-      auto slot_of = [&](int gt, int b) -> int { return static_cast<int>((static_cast<int64_t>(gt) * NB + b) % R); };
       bool ok = true;
       int nit = 0, g = 0;
       while (ok) {
@@ -726,29 +746,7 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
             break;
           }
           tc_fence_after();
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t dO = tmem + C::kTmemO + j * NQ;
-            if (F == kBF16) {
-              const uint64_t aV = dV0 + ((slot_of(gt, 2 * j) * C::kSlot) >> 4);
-#pragma unroll
-              for (int kk = 0; kk < KM / 16; ++kk)
-                mma_f16_ss(dO, aV + ((kk * 2048) >> 4), dP0 + ((kk * NQ * 32) >> 4), kIdPv, (!first || kk > 0) ? 1u : 0u);
-              if (C::kSlotCommits) {
-                mma_commit(&empty[slot_of(gt, 2 * j)]);
-                mma_commit(&empty[slot_of(gt, 2 * j + 1)]);
-              }
-            } else {
-              const uint64_t aV = dV0 + ((slot_of(gt, j) * C::kSlot) >> 4);
-#pragma unroll
-              for (int kk = 0; kk < KM / 32; ++kk) {
-                const uint64_t pb = dP0 + ((kk * NQ * 32) >> 4);
-                mma_f8_ss(dO, aV + ((kk * 4096) >> 4), pb, kIdPv, (!first || kk > 0) ? 1u : 0u);
-                mma_f8_ss(dO, aV + ((kk * 4096) >> 4), pb + ((KM * NQ) >> 4), kIdPv, 1u);
-              }
-              if (C::kSlotCommits) mma_commit(&empty[slot_of(gt, j)]);
-            }
-          }
+          paged_issue_pv<C, F, NQ>(tmem, dV0, dP0, empty, gt, first);
           mma_commit(&pv_done[gt & 1]);
         }
         g += it.ntiles;
