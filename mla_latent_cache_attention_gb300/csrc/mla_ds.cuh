@@ -90,7 +90,8 @@ struct DsCfg {
   static constexpr int kItems = kValid + 2 * kTile;
   static constexpr int kBar = kItems + kItemDepth * 32;
   // + ring_free[2] and xitem_full[kItemDepth] of the CTA-pair kernel
-  static constexpr int kNumBars = R + 9 + 2 * kItemDepth + 2 + kItemDepth;
+  // + p_full[4] (one per value tile)
+  static constexpr int kNumBars = R + 8 + 2 * kItemDepth + 2 + kItemDepth + 4;
   static constexpr int kMisc = kBar + kNumBars * 8;
   static constexpr int kTotal = kMisc + 16 + 8 * 8;   // TMEM slot, abort word, cluster CTAs' ring positions
   static constexpr int kAlloc = kTotal + 1024;
@@ -113,20 +114,20 @@ __device__ __forceinline__ int e4m3_fit_exponent(float a) {
   return e;
 }
 
-// PV of tile gt: O_j (+)= V_j^T P_j for the four value tiles j (V_j: ring slot j of the tile's
-// half of the ring; P_j: 128 keys x 64 weights).  The descriptors advance by 32-bit adds: the
-// issuing thread shares its sub-partition with busy warps, and fewer instructions per MMA
-// measured faster.
+// PV of value tile j of tile gt: O_j (+)= V_j^T P_j (V_j: ring slot j of the tile's half of
+// the ring; P_j: 128 keys x 64 weights).  Issued per value tile as soon as its P_j is written,
+// so the four PV blocks overlap the softmax's writing of the later P_j.  The descriptors
+// advance by 32-bit adds: the issuing thread shares its sub-partition with busy warps, and
+// fewer instructions per MMA measured faster.
 template <int NB>
-__device__ __forceinline__ void ds_issue_pv(uint32_t tmem_o, uint64_t dV0, uint64_t dP0, uint32_t id, int gt, bool first) {
-  const uint64_t aT = desc_add(dV0, (((gt & 1) * NB) * kSlotBytes) >> 4);
+__device__ __forceinline__ void ds_issue_pv_block(uint32_t tmem_o, uint64_t dV0, uint64_t dP0, uint32_t id, int gt,
+                                                  int j, bool first) {
+  const uint64_t aV = desc_add(dV0, (((gt & 1) * NB + j) * kSlotBytes) >> 4);
+  const uint64_t bP = desc_add(dP0, (j * kTile * 64) >> 4);
   const uint32_t acc0 = first ? 0u : 1u;
 #pragma unroll
-  for (int j = 0; j < 4; ++j)
-#pragma unroll
-    for (int kk = 0; kk < 4; ++kk)
-      mma_f8_ss(tmem_o + 64 * j, desc_add(aT, (j * kSlotBytes + kk * 4096) >> 4),
-                desc_add(dP0, (j * kTile * 64 + kk * 2048) >> 4), id, kk > 0 ? 1u : acc0);
+  for (int kk = 0; kk < 4; ++kk)
+    mma_f8_ss(tmem_o + 64 * j, desc_add(aV, (kk * 4096) >> 4), desc_add(bP, (kk * 2048) >> 4), id, kk > 0 ? 1u : acc0);
 }
 
 // kCl = 2, 3 or 6 (paged source only): the kernel runs as clusters of kCl CTAs.  The CTAs of a
@@ -159,15 +160,16 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
   uint64_t* full = bars;                  // [R] slot data landed (TMA bytes / gather warps)
   uint64_t* s_full = bars + R;            // [2]
   uint64_t* pv_done = bars + R + 2;       // [2]
-  uint64_t* p_full = bars + R + 4;
-  uint64_t* q_full = bars + R + 5;
-  uint64_t* fin = bars + R + 6;
-  uint64_t* s_free = bars + R + 7;        // the softmax warps have read S (four arrivals)
-  uint64_t* item_full = bars + R + 8;
+  uint64_t* q_full = bars + R + 4;
+  uint64_t* fin = bars + R + 5;
+  uint64_t* s_free = bars + R + 6;        // the softmax warps have read S (four arrivals)
+  uint64_t* item_full = bars + R + 7;
   uint64_t* item_empty = item_full + kItemDepth;
   uint64_t* fin_pv = item_empty + kItemDepth;
   uint64_t* ring_free = fin_pv + 1;       // [2] cluster: every CTA's PV of the tile is done
   uint64_t* xitem_full = ring_free + 2;   // [kItemDepth] cluster: the first CTA's item k is posted
+  // [4] P_j of the tile is written (one arrival per softmax warp): PV of value tile j may go
+  uint64_t* p_full = xitem_full + kItemDepth;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kMisc + 4);
   int64_t* cl_pos = reinterpret_cast<int64_t*>(smem + C::kMisc + 16);   // [kCl] cluster: positions each producer issued
@@ -185,7 +187,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(p_full, 1);
+    for (int j = 0; j < 4; ++j) mbar_init(&p_full[j], 4);
     mbar_init(q_full, 1);
     mbar_init(fin, 1);
     mbar_init(fin_pv, 1);
@@ -270,7 +272,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
       const uint64_t dP0 = smem_desc(smem_u32(ps), 512, 128, kSwizzleNone);
       constexpr uint32_t kIdPv = idesc_e4m3(128, 64, 1, 1) | (1u << 10);   // B (weights) in e5m2
       WorkItem cur = next_item(), pit{};
-      int npush = 0, npv = 0, pv_t = 0, pv_g = 0;
+      int npush = 0, npv = 0, pv_t = 0, pv_g = 0, pv_j = 0;
       bool push_done = false, have = false;
       uint64_t t_last = globaltimer();
       for (;;) {
@@ -301,13 +303,16 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
           }
         } else if (pv_t < pit.ntiles) {
           const int gt = pv_g + pv_t;
-          if (mbar_test_wait(p_full, static_cast<uint32_t>(gt) & 1u)) {
+          if (mbar_test_wait(&p_full[pv_j], static_cast<uint32_t>(gt) & 1u)) {
             tc_fence_after();
-            TL(0, 1);
-            ds_issue_pv<NB>(tmem + C::kTmemO, dV0, dP0, kIdPv, gt, pv_t == 0);
-            mma_commit(&pv_done[gt & 1]);
-            TL(0, 2);
-            ++pv_t;
+            if (pv_j == 0) TL(0, 1);
+            ds_issue_pv_block<NB>(tmem + C::kTmemO, dV0, dP0, kIdPv, gt, pv_j, pv_t == 0);
+            if (++pv_j == 4) {
+              pv_j = 0;
+              mma_commit(&pv_done[gt & 1]);
+              TL(0, 2);
+              ++pv_t;
+            }
             prog = true;
           }
         } else {
@@ -323,7 +328,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
             *abort_flag = 2;
             break;
           }
-          if (have && pv_t < pit.ntiles) (void)mbar_try_wait_ns(p_full, static_cast<uint32_t>(pv_g + pv_t) & 1u, 500);
+          if (have && pv_t < pit.ntiles) (void)mbar_try_wait_ns(&p_full[pv_j], static_cast<uint32_t>(pv_g + pv_t) & 1u, 500);
         }
       }
       mma_commit(fin_pv);
@@ -841,25 +846,24 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
             }
             *reinterpret_cast<uint4*>(pj + 128 * term) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
           }
-        }
-        if (stid == 0) TL(3, 8);
-        // rows past the item or masked: their codes never reach PV (stale slot contents);
-        // the gather warps already store zeros for them
-        if (!kSparse && !rv) {
-#pragma unroll 1
-          for (int j = 0; j < 4; ++j) {
+          // rows past the item or masked: their codes never reach PV (stale slot contents);
+          // the gather warps already store zeros for them
+          if (!kSparse && !rv) {
             uint4* dst = reinterpret_cast<uint4*>(ring + ((gt & 1) * NB + j) * kSlotBytes + row * 128);
 #pragma unroll
             for (int i = 0; i < 8; ++i) dst[i] = make_uint4(0, 0, 0, 0);
           }
+          // P_j of this warp's 32 keys is in place: PV of value tile j may start (the O
+          // rescale above has completed; a warp whose PV wait failed does not arrive, and the
+          // issuer's bounded wait then ends on the abort word)
+          fence_proxy_async_smem();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0 && w) mbar_arrive(&p_full[j]);
         }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        if (stid == 0) TL(3, 2);
+        if (stid == 0) TL(3, 8);
         ok = named_bar_and(1, NT, w);
         if (!ok) break;
-        if (stid == 0) mbar_arrive(p_full);
-        if (stid == 0) TL(3, 3);
       }
       if (!ok) break;
       // ---- epilogue
@@ -969,13 +973,13 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         if (it.b < 0) break;
         for (int t = 0; t < it.ntiles && ok; ++t) {
           const int gt = g + t;
-          if (!mbar_wait(p_full, static_cast<uint32_t>(gt) & 1u, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
           TL(2, 3);
-          ds_issue_pv<NB>(tmem + C::kTmemO, dV0, dP0, kIdPv, gt, t == 0);
+          for (int j = 0; j < 4 && ok; ++j) {
+            ok = mbar_wait(&p_full[j], static_cast<uint32_t>(gt) & 1u, abort_flag);
+            tc_fence_after();
+            if (ok) ds_issue_pv_block<NB>(tmem + C::kTmemO, dV0, dP0, kIdPv, gt, j, t == 0);
+          }
+          if (!ok) break;
           mma_commit(&pv_done[gt & 1]);
           // cluster: this CTA's share of "tile gt's slots are free", in every CTA
           if (kCl > 1) mma_commit_mc(&ring_free[gt & 1], kMask);
