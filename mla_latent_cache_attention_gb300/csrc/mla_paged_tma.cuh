@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&pv_done[i], 1);
     }
-    mbar_init(p_full, 1);
+    mbar_init(p_full, C::kSW);     // one arrival per softmax warp
     mbar_init(q_full, 1);
     mbar_init(fin, 1);
     mbar_init(fin_pv, 1);
@@ -939,12 +939,16 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
             *reinterpret_cast<uint4*>(ps + KM * NQ + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
           }
         }
+        // P of this warp's keys and columns is in place: one arrival per softmax warp, so PV
+        // starts without a barrier of the group (a warp whose wait failed does not arrive; the
+        // issuer's bounded wait then ends on the abort word)
         fence_proxy_async_smem();
         tc_fence_before();
+        __syncwarp();
+        if (lane == 0 && w) mbar_arrive(p_full);
+        if (stid == 0) TL(3, 3);
         ok = named_bar_and(1, NT, w);
         if (!ok) break;
-        if (stid == 0) mbar_arrive(p_full);
-        if (stid == 0) TL(3, 3);
         if (!kLReg) l_part[0] += warp_col_reduce<NC, false>(s, lane);   // while PV runs
       }
       if (!ok) break;
