@@ -746,8 +746,10 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
             break;
           }
           tc_fence_after();
+          TL(1, 1);
           paged_issue_pv<C, F, NQ>(tmem, dV0, dP0, empty, gt, first);
           mma_commit(&pv_done[gt & 1]);
+          TL(1, 2);
         }
         g += it.ntiles;
       }
