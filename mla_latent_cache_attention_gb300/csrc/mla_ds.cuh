@@ -973,7 +973,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         if (it.b < 0) break;
         for (int t = 0; t < it.ntiles && ok; ++t) {
           const int gt = g + t;
-          TL(2, 3);
+          TL(1, 3);
           for (int j = 0; j < 4 && ok; ++j) {
             ok = mbar_wait(&p_full[j], static_cast<uint32_t>(gt) & 1u, abort_flag);
             tc_fence_after();
@@ -983,7 +983,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
           mma_commit(&pv_done[gt & 1]);
           // cluster: this CTA's share of "tile gt's slots are free", in every CTA
           if (kCl > 1) mma_commit_mc(&ring_free[gt & 1], kMask);
-          TL(2, 4);
+          TL(1, 4);
         }
         g += it.ntiles;
       }
