@@ -31,6 +31,11 @@
 //     unswizzled map) into a two-tile ring.  Sparse source: eight gather warps load each
 //     record with 16-byte vector loads (a record is 41 of them) and store it in the same
 //     layout; masked or out-of-range indices store zeros and a row flag.
+//   * Roles hand over through mbarriers, each waited with a time limit: a gathered tile
+//     completes one barrier (one arrival per gather warp, after all its stores); S is released
+//     per softmax warp as soon as its TMEM loads are done; P_j completes a barrier of its own
+//     (one arrival per softmax warp), so the PV of value tile j runs while the later P_j are
+//     written.
 //
 // Warps: 0 scheduler (+ TMA producer for pages; + PV issuer for the sparse source), 1 QK issuer
 // (TMEM owner), 2..5 softmax + query preparation + epilogue, then 6 PV issuer (pages) or
