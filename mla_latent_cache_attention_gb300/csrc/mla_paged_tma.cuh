@@ -514,36 +514,89 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
         const bool av = in_cur || (nxt.b >= 0 && tta < nxt.ntiles);
         const int raw_a = (av && lane < NPG) ? page_raw(ia, tta, lane) : -2;
         if (lane == 0) TL(0, 1);
+        if constexpr (F == kBF16) {
+          // bf16 (nine boxes a tile): lane 0 issues the tile's boxes alone, so that the warp,
+          // which shares its sub-partition with busy warps, spends few instructions a copy
+          // (decode 65.2 -> 63.5 us).  fp8 keeps the warp-wide loop below: there the lean loop
+          // queued the next tiles' L2 prefetches straight behind a full copy queue and the
+          // producer reached the next tile later (0.864 -> 1.121 ms).
+          // the tile's pages (lane q < NPG resolved page q; NPG <= 8) in every lane's registers
+          int zq[8], yq[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            zq[q] = __shfl_sync(0xFFFFFFFFu, blk, q);
+            yq[q] = __shfl_sync(0xFFFFFFFFu, y, q);
+          }
+          // lane 0 issues the tile's boxes alone: the warp shares its sub-partition with busy
+          // warps, and the TMA engine is only kept busy if the loop costs few instructions a copy
+          if (lane == 0) {
 #pragma unroll 1
-        for (int b = 0; b < NB; ++b, ++pos) {
-          const int slot = static_cast<int>(pos % R);
-          if (C::kSlotCommits && pos >= R) {
-            if (!warp_wait(&empty[slot], static_cast<uint32_t>(pos / R - 1) & 1u, abort_flag)) {
-              ok = false;
-              break;
+            for (int b = 0; b < NB; ++b, ++pos) {
+              const int slot = static_cast<int>(pos % R);
+              if (C::kSlotCommits && pos >= R) {
+                if (!mbar_wait(&empty[slot], static_cast<uint32_t>(pos / R - 1) & 1u, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+              } else if (pos >= R) {
+                const int tu = static_cast<int>((pos - R) / NB);     // tile that last used the slot
+                if (tu != t_waited) {
+                  if (!mbar_wait(&pv_done[tu & 1], static_cast<uint32_t>(tu >> 1) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                  }
+                  t_waited = tu;
+                }
+              }
+              if (F == kBF16 && b == 9) {
+                mbar_arrive(&full[slot]);
+                continue;
+              }
+              mbar_arrive_expect_tx(&full[slot], C::kSlot);
+              if (b == 0 || b == NB - 1) TL(0, (b == 0 ? 1000 : 3000) + static_cast<int>((pos / NB) % 1000));
+              const int x = (F == kFP8 && b == 4) ? 448 : 128 * b;
+              uint8_t* dst = ring + slot * C::kSlot;
+#pragma unroll
+              for (int q = 0; q < 8; ++q)
+                if (q < NPG) tma_load_3d(dst + q * p.BR * 128, &tm_kv, x, yq[q], zq[q], &full[slot]);
             }
-          } else if (pos >= R) {
-            const int tu = static_cast<int>((pos - R) / NB);     // tile that last used the slot
-            if (tu != t_waited) {
-              if (!warp_wait(&pv_done[tu & 1], static_cast<uint32_t>(tu >> 1) & 1u, abort_flag)) {
+          }
+          // the warp goes on with lane 0's outcome
+          ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+          pos = static_cast<int64_t>(__shfl_sync(0xFFFFFFFFu, static_cast<unsigned long long>(pos), 0));
+          t_waited = __shfl_sync(0xFFFFFFFFu, t_waited, 0);
+        } else {
+#pragma unroll 1
+          for (int b = 0; b < NB; ++b, ++pos) {
+            const int slot = static_cast<int>(pos % R);
+            if (C::kSlotCommits && pos >= R) {
+              if (!warp_wait(&empty[slot], static_cast<uint32_t>(pos / R - 1) & 1u, abort_flag)) {
                 ok = false;
                 break;
               }
-              t_waited = tu;
+            } else if (pos >= R) {
+              const int tu = static_cast<int>((pos - R) / NB);     // tile that last used the slot
+              if (tu != t_waited) {
+                if (!warp_wait(&pv_done[tu & 1], static_cast<uint32_t>(tu >> 1) & 1u, abort_flag)) {
+                  ok = false;
+                  break;
+                }
+                t_waited = tu;
+              }
             }
-          }
-          if (F == kBF16 && b == 9) {
-            if (lane == 0) mbar_arrive(&full[slot]);
-            continue;
-          }
-          if (lane == 0) mbar_arrive_expect_tx(&full[slot], C::kSlot);
-          if (lane == 0 && (b == 0 || b == NB - 1)) TL(0, (b == 0 ? 1000 : 3000) + static_cast<int>((pos / NB) % 1000));
-          __syncwarp();
-          const int x = (F == kFP8 && b == 4) ? 448 : 128 * b;
-          for (int q = 0; q < NPG; ++q) {
-            const int z = __shfl_sync(0xFFFFFFFFu, blk, q);
-            const int yy = __shfl_sync(0xFFFFFFFFu, y, q);
-            if (lane == 0) tma_load_3d(ring + slot * C::kSlot + q * p.BR * 128, &tm_kv, x, yy, z, &full[slot]);
+            if (F == kBF16 && b == 9) {
+              if (lane == 0) mbar_arrive(&full[slot]);
+              continue;
+            }
+            if (lane == 0) mbar_arrive_expect_tx(&full[slot], C::kSlot);
+            if (lane == 0 && (b == 0 || b == NB - 1)) TL(0, (b == 0 ? 1000 : 3000) + static_cast<int>((pos / NB) % 1000));
+            __syncwarp();
+            const int x = (F == kFP8 && b == 4) ? 448 : 128 * b;
+            for (int q = 0; q < NPG; ++q) {
+              const int z = __shfl_sync(0xFFFFFFFFu, blk, q);
+              const int yy = __shfl_sync(0xFFFFFFFFu, y, q);
+              if (lane == 0) tma_load_3d(ring + slot * C::kSlot + q * p.BR * 128, &tm_kv, x, yy, z, &full[slot]);
+            }
           }
         }
         // finish the lookahead: queue its pages (and prefetch them into L2)
