@@ -1017,18 +1017,22 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&item_empty[k]);
       if (it.b < 0) break;
+      // lane l < 16: the index of record rbase + l of tile tt, loaded one tile ahead (its
+      // latency then hides behind this tile's wait and stores) and checked when used
+      auto raw_index = [&](int tt) -> int {
+        const int e = tt * kTile + rbase + lane;
+        return (lane < 16 && tt < it.ntiles && e < it.n) ? p.indices[it.k0 + e] : -1;
+      };
+      int raw_nx = raw_index(0);
       for (int t = 0; t < it.ntiles && ok; ++t) {
         const int gt = g + t;
         // lane l < 16: record rbase + l of the tile (-1: past the row, masked or bad)
         int idx = -1;
-        if (lane < 16) {
-          const int e = t * kTile + rbase + lane;
-          if (e < it.n) {
-            idx = p.indices[it.k0 + e];
-            if (idx < 0 || idx >= p.num_records) {
-              if (idx >= p.num_records || !p.has_invalid) errbits |= 1u;
-              idx = -1;
-            }
+        if (lane < 16 && t * kTile + rbase + lane < it.n) {
+          idx = raw_nx;
+          if (idx < 0 || idx >= p.num_records) {
+            if (idx >= p.num_records || !p.has_invalid) errbits |= 1u;
+            idx = -1;
           }
         }
         if (lane == 0) TL(4 + gw, 1);
@@ -1047,6 +1051,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
                           ? *reinterpret_cast<const uint4*>(p.records + static_cast<int64_t>(ri) * p.rec_stride + 16 * c)
                           : make_uint4(0, 0, 0, 0);
         }
+        raw_nx = raw_index(t + 1);
         // tile gt reuses the slots of tile gt - 2
         if (gt >= 2 && !warp_wait(&pv_done[gt & 1], static_cast<uint32_t>((gt - 2) >> 1) & 1u, abort_flag)) {
           ok = false;
