@@ -585,8 +585,65 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
     // and e5m2 (both past 2^15), and the lazy reference moves only on a jump of kTau
     constexpr float kTau = 10.f, kPExp = 4.f;
     constexpr int kOB = kSparse ? 32 : 64;      // TMEM columns per O-rescale round trip (registers)
+    // The query of item qi into the query buffer (every softmax thread; ends with the group
+    // barrier and the q_full arrival): thread (c = stid / 8, part = stid % 8) handles elements
+    // 64 part .. +63 of column c; hi / lo e4m3 of 2^e_c q into rows c / 16 + c, k_pe as it is
+    auto prep_query = [&](const WorkItem& qi) {
+      const int c = stid >> 3, part = stid & 7;
+      const int cg = qi.g * NQ + c;
+      const bool live = cg < p.cols;
+      const uint8_t* qrow = live ? p.q + (static_cast<int64_t>(qi.b) * p.q_len + cg / p.H) * p.q_s0b + (cg % p.H) * p.q_s1b
+                                 : nullptr;
+      uint4 v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] = live ? *reinterpret_cast<const uint4*>(qrow + part * 128 + 16 * i) : make_uint4(0, 0, 0, 0);
+      float amax = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t wv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          amax = fmaxf(amax, fabsf(__uint_as_float(wv[u] << 16)));
+          amax = fmaxf(amax, fabsf(__uint_as_float(wv[u] & 0xFFFF0000u)));
+        }
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+      const int e = e4m3_fit_exponent(amax);
+      const float sc = pow2i(e);
+      if (part == 0) colf[c] = pow2i(-e);
+      // 64 elements -> 64 hi bytes + 64 lo bytes at block part / 2, byte (part & 1) * 64
+      const int blk = part >> 1;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {     // 16 elements per 16-byte output chunk
+        uint32_t hw[4], lw[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 a = v[2 * i + (u >> 1)];
+          const uint32_t w0 = (u & 1) ? a.z : a.x, w1 = (u & 1) ? a.w : a.y;
+          const float x0 = __uint_as_float(w0 << 16) * sc, x1 = __uint_as_float(w0 & 0xFFFF0000u) * sc;
+          const float x2 = __uint_as_float(w1 << 16) * sc, x3 = __uint_as_float(w1 & 0xFFFF0000u) * sc;
+          const uint32_t h01 = e4m3x2_sat(x0, x1), h23 = e4m3x2_sat(x2, x3);
+          const float2 f01 = e4m3x2_to_float2(h01), f23 = e4m3x2_to_float2(h23);
+          hw[u] = h01 | (h23 << 16);
+          lw[u] = e4m3x2_sat(x0 - f01.x, x1 - f01.y) | (e4m3x2_sat(x2 - f23.x, x3 - f23.y) << 16);
+        }
+        const int chunk = (part & 1) * 4 + i;
+        uint8_t* base = qs + blk * (32 * 128);
+        *reinterpret_cast<uint4*>(base + sw128(c, chunk)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+        *reinterpret_cast<uint4*>(base + sw128(16 + c, chunk)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+      }
+      // k_pe part: 128 bytes per column, one 16-byte chunk per thread
+      const uint4 rv = live ? *reinterpret_cast<const uint4*>(qrow + 1024 + 16 * part) : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(qr + sw128(c, part)) = rv;
+      fence_proxy_async_smem();
+      named_bar_sync(1, NT);
+      if (stid == 0) mbar_arrive(q_full);
+    };
     int nit = 0, g = 0;
     bool ok = true;
+    bool q_ready = false;      // the query of the next item was prepared ahead of the epilogue
     while (ok) {
       const int k = nit % kItemDepth;
       bool w = warp_wait(&item_full[k], (nit / kItemDepth) & 1, abort_flag);
@@ -595,61 +652,8 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
       if (!named_bar_and(1, NT, w)) break;
       if (it.b < 0) break;
       const int cgb = it.g * NQ;     // first global column of the item
-      if (it.ntiles > 0) {
-        // query: thread (c = stid / 8, part = stid % 8) handles elements 64 part .. +63 of
-        // column c; hi / lo e4m3 of 2^e_c q into rows c / 16 + c, k_pe as it is
-        const int c = stid >> 3, part = stid & 7;
-        const int cg = cgb + c;
-        const bool live = cg < p.cols;
-        const uint8_t* qrow = live ? p.q + (static_cast<int64_t>(it.b) * p.q_len + cg / p.H) * p.q_s0b + (cg % p.H) * p.q_s1b
-                                   : nullptr;
-        uint4 v[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = live ? *reinterpret_cast<const uint4*>(qrow + part * 128 + 16 * i) : make_uint4(0, 0, 0, 0);
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t wv[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            amax = fmaxf(amax, fabsf(__uint_as_float(wv[u] << 16)));
-            amax = fmaxf(amax, fabsf(__uint_as_float(wv[u] & 0xFFFF0000u)));
-          }
-        }
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
-        const int e = e4m3_fit_exponent(amax);
-        const float sc = pow2i(e);
-        if (part == 0) colf[c] = pow2i(-e);
-        // 64 elements -> 64 hi bytes + 64 lo bytes at block part / 2, byte (part & 1) * 64
-        const int blk = part >> 1;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {     // 16 elements per 16-byte output chunk
-          uint32_t hw[4], lw[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint4 a = v[2 * i + (u >> 1)];
-            const uint32_t w0 = (u & 1) ? a.z : a.x, w1 = (u & 1) ? a.w : a.y;
-            const float x0 = __uint_as_float(w0 << 16) * sc, x1 = __uint_as_float(w0 & 0xFFFF0000u) * sc;
-            const float x2 = __uint_as_float(w1 << 16) * sc, x3 = __uint_as_float(w1 & 0xFFFF0000u) * sc;
-            const uint32_t h01 = e4m3x2_sat(x0, x1), h23 = e4m3x2_sat(x2, x3);
-            const float2 f01 = e4m3x2_to_float2(h01), f23 = e4m3x2_to_float2(h23);
-            hw[u] = h01 | (h23 << 16);
-            lw[u] = e4m3x2_sat(x0 - f01.x, x1 - f01.y) | (e4m3x2_sat(x2 - f23.x, x3 - f23.y) << 16);
-          }
-          const int chunk = (part & 1) * 4 + i;
-          uint8_t* base = qs + blk * (32 * 128);
-          *reinterpret_cast<uint4*>(base + sw128(c, chunk)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-          *reinterpret_cast<uint4*>(base + sw128(16 + c, chunk)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
-        }
-        // k_pe part: 128 bytes per column, one 16-byte chunk per thread
-        const uint4 rv = live ? *reinterpret_cast<const uint4*>(qrow + 1024 + 16 * part) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(qr + sw128(c, part)) = rv;
-        fence_proxy_async_smem();
-        named_bar_sync(1, NT);
-        if (stid == 0) mbar_arrive(q_full);
-      }
+      if (it.ntiles > 0 && !q_ready) prep_query(it);
+      q_ready = false;
       // the column reference maxima and rescale factors are the same for every thread: one
       // copy per warp in shared memory keeps them out of the registers
       float* mref = reinterpret_cast<float*>(smem + C::kMref) + quad * NQ;
@@ -871,6 +875,21 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         if (!ok) break;
       }
       if (!ok) break;
+      // The next item's query, ahead of this item's epilogue, when that item is already posted:
+      // QK of this item's last tile is done (its S was read), so the query buffer and the
+      // column factors are free, and the next item's QK then overlaps this epilogue (its PV
+      // still waits for its P, written after the epilogue has read O out).
+      {
+        const int kn = nit % kItemDepth;
+        const bool posted = mbar_test_wait(&item_full[kn], static_cast<uint32_t>(nit / kItemDepth) & 1u);
+        if (named_bar_and(1, NT, posted)) {
+          const WorkItem nx = items[kn];
+          if (nx.b >= 0 && nx.ntiles > 0) {
+            prep_query(nx);
+            q_ready = true;
+          }
+        }
+      }
       // ---- epilogue
       w = true;
       if (it.ntiles > 0) {
