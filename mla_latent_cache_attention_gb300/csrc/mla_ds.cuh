@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
   uint8_t* vrow = smem + C::kValid;                                 // [2][128]
   WorkItem* items = reinterpret_cast<WorkItem*>(smem + C::kItems);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
-  uint64_t* full = bars;                  // [R] slot data landed (TMA bytes / gather warps)
+  uint64_t* full = bars;                  // [R] slot data landed (TMA bytes; sparse: the gather warps complete a tile's first)
   uint64_t* s_full = bars + R;            // [2]
   uint64_t* pv_done = bars + R + 2;       // [2]
   uint64_t* q_full = bars + R + 4;
