@@ -18,11 +18,13 @@
 //     S_rope, so the per-key scale is applied in fp32.  k_pe . q_pe runs as a bf16 MMA.
 //   * PV on the e4m3 codes as well: O_j^T = V_j^T P_j with P_j = p * s_j * r_j, one P per value
 //     tile so that each key's scale multiplies its own term, as four e5m2 terms (stacked
-//     along N, 16 columns each; e4m3 codes x e5m2 weights), split on the f16 bits of P_j
-//     (an e5m2 is the upper byte of an f16): three terms keep 3 significant bits each of
-//     what is left and the fourth rounds the rest, so the split carries the f16 value of P_j
-//     (2^-11 relative), and e5m2 reaches down to 2^-16, which keeps the
-//     many small weights of a long row (whose values reach 448 times the scale) from being
+//     along N, 16 columns each; e4m3 codes x e5m2 weights): the first is P_j rounded to
+//     nearest e5m2 from fp32, and the exact rest (at most 2^-3 of P_j) is rounded once to
+//     f16 and split on its bits (an e5m2 is the upper byte of an f16: two terms keep 3
+//     significant bits each of what is left and the last rounds the rest), so the four carry
+//     P_j to about 2^-12 relative -- the outputs cancel terms up to 448 times a scale, and a
+//     plain f16 P (2^-11) measured up to 1.1 times the tolerance on random shapes -- and
+//     e5m2 reaches down to 2^-16, which keeps the many small weights of a long row from being
 //     lost under an e4m3 floor of 2^-9.  r_j is a power of two kept per item so
 //     that s_j r_j <= 1; when a later key needs a smaller r_j, O_j is rescaled by the (exact)
 //     ratio.
@@ -107,6 +109,15 @@ struct DsCfg {
 };
 
 __device__ __forceinline__ float pow2i(int e) { return __int_as_float((e + 127) << 23); }   // e in [-126, 127]
+
+// Two floats rounded to nearest even e5m2 (saturating), a in the low byte, and back.
+__device__ __forceinline__ uint32_t e5m2x2_rn(float a, float b) {
+  return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E5M2));
+}
+__device__ __forceinline__ float2 e5m2x2_to_float2(uint32_t v) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E5M2);
+  return __half22float2(*reinterpret_cast<const __half2*>(&h));
+}
 
 // 2^e with e the largest integer such that a * 2^e <= 448 (a > 0 finite), clamped to the
 // normal range.
@@ -821,21 +832,28 @@ __global__ void __launch_bounds__(DsCfg<kSparse>::kThreads, 1)
         }
         if (stid == 0) TL(3, 7);
         // P_j = p s_j r_j as four e5m2 terms (4 x 16 columns), 8 keys x 16 B core matrices.
-        // e5m2 is the upper byte of an f16 (same sign, exponent bias and subnormals): the
-        // first three terms keep the upper byte of what is left (the remainder, an exact f16
-        // subtraction, keeps the sign), the last rounds it to nearest even.
+        // The first term is P_j rounded to nearest e5m2 from fp32; the rest (exact in fp32, at
+        // most 2^-3 of P_j) is rounded once to f16 and split into three more terms: e5m2 is the
+        // upper byte of an f16 (same sign, exponent bias and subnormals), so the next two keep
+        // the upper byte of what is left (an exact f16 subtraction, which keeps the sign) and
+        // the last rounds it to nearest even.  The four carry P_j to about 2^-12 relative.
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const float f = rv ? sj[j] * rj[j] : 0.f;
           uint8_t* pj = ps + j * (kTile * 64) + (row >> 3) * 512 + (row & 7) * 16;
-          uint32_t a[8];
+          uint32_t a[8], w0[4];
 #pragma unroll
           for (int u = 0; u < 8; ++u) {
-            const __half2 h = __floats2half2_rn(s[2 * u] * f, s[2 * u + 1] * f);
+            const float x0 = s[2 * u] * f, x1 = s[2 * u + 1] * f;
+            const uint32_t e = e5m2x2_rn(x0, x1);         // column 2u in the low byte
+            const float2 t = e5m2x2_to_float2(e);
+            const __half2 h = __floats2half2_rn(x0 - t.x, x1 - t.y);
             a[u] = *reinterpret_cast<const uint32_t*>(&h);
+            w0[u >> 1] = (u & 1) ? (w0[u >> 1] | (e << 16)) : e;
           }
+          *reinterpret_cast<uint4*>(pj) = make_uint4(w0[0], w0[1], w0[2], w0[3]);
 #pragma unroll
-          for (int term = 0; term < 4; ++term) {
+          for (int term = 1; term < 4; ++term) {
             uint32_t wv[4];
 #pragma unroll
             for (int u = 0; u < 8; u += 2) {
