@@ -515,20 +515,18 @@ __global__ void __launch_bounds__(PagedCfg<F, NQ>::kThreads, 1)
         const int raw_a = (av && lane < NPG) ? page_raw(ia, tta, lane) : -2;
         if (lane == 0) TL(0, 1);
         if constexpr (F == kBF16) {
-          // bf16 (nine boxes a tile): lane 0 issues the tile's boxes alone, so that the warp,
-          // which shares its sub-partition with busy warps, spends few instructions a copy
-          // (decode 65.2 -> 63.5 us).  fp8 keeps the warp-wide loop below: there the lean loop
-          // queued the next tiles' L2 prefetches straight behind a full copy queue and the
-          // producer reached the next tile later (0.864 -> 1.121 ms).
-          // the tile's pages (lane q < NPG resolved page q; NPG <= 8) in every lane's registers
-          int zq[8], yq[8];
+          // bf16 (nine boxes a tile): lane 0 issues the tile's boxes alone, from registers that
+          // hold the tile's pages, so that the warp, which shares its sub-partition with busy
+          // warps, spends few instructions a copy (decode 65.2 -> 64.0 us).  fp8 keeps the
+          // warp-wide loop below: there the lean loop queued the next tiles' L2 prefetches
+          // straight behind a full copy queue and the producer reached the next tile later
+          // (0.864 -> 1.121 ms).
+          int zq[8], yq[8];     // lane q < NPG resolved page q (NPG <= 8)
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             zq[q] = __shfl_sync(0xFFFFFFFFu, blk, q);
             yq[q] = __shfl_sync(0xFFFFFFFFu, y, q);
           }
-          // lane 0 issues the tile's boxes alone: the warp shares its sub-partition with busy
-          // warps, and the TMA engine is only kept busy if the loop costs few instructions a copy
           if (lane == 0) {
 #pragma unroll 1
             for (int b = 0; b < NB; ++b, ++pos) {
