@@ -44,7 +44,7 @@ def paged_params(seed):
                 q_scale=qs, k_scale=ks)
 
 
-@pytest.mark.parametrize("seed", range(80))
+@pytest.mark.parametrize("seed", range(200))
 def test_paged_random_shapes(m, seed):
     a = paged_params(seed)
     mc = max(max(a["lens"]), 1) * a["mc_mul"]
@@ -81,7 +81,7 @@ def sparse_params(seed):
 
 
 @pytest.mark.parametrize("kern", ["gather", "staged"])
-@pytest.mark.parametrize("seed", range(40))
+@pytest.mark.parametrize("seed", range(100))
 def test_sparse_random_shapes(m, seed, kern):
     a = sparse_params(seed)
     c = synth.sparse_case(40_000 + seed, **a)
